@@ -1,0 +1,217 @@
+/*
+ * mm3idx.h -- C ABI of the GB300 (sm_103a) MiniMax-M3 lightning-indexer
+ * library: causal block scoring of bf16 index queries against a paged index-K
+ * cache, followed by per-(head, query token) top-k block selection with
+ * forced init and local blocks.
+ *
+ * Sources of the operation (vLLM API pages):
+ *   vllm.models.minimax_m3.amd.ops.index_topk
+ *     - module docstring: index queries score each 128-token block of index
+ *       keys (max over the block), then the top-k blocks plus forced init /
+ *       local blocks are selected per query token; the KV page size equals the
+ *       sparse block size (128), so one sparse block is one page; the index-K
+ *       cache is [num_blocks, 128, head_dim], one key vector per token shared
+ *       by every index head.
+ *     - minimax_m3_index_decode: fused decode scoring + top-k; ids are
+ *       0-indexed logical block ids padded with -1, [heads, total_q, topk];
+ *       caller-owned `out` and a completion counter that must be zero before
+ *       the first launch and that every completed launch resets.
+ *     - minimax_m3_index_score: score [heads, total_q, max_block], each entry
+ *       the max over a 128-token index-K block.
+ *     - minimax_m3_index_topk: top-k from a precomputed score tensor.
+ *   vllm.models.minimax_m3.amd.ops.indexer_context_parallel,
+ *     check_context_score_inputs / indexer_context_scores: input layout rules
+ *     (bf16 [tokens, heads, 128] queries with unit d stride, contiguous
+ *     non-empty [pages, 128, 128] cache, int32 tables with unit inner stride),
+ *     rows = requests * query_len, table at least cdiv(max_seq_len, 128)
+ *     wide, max_seq_len a capture-stable bound, sm_scale applied to scores.
+ *   vllm.models.minimax_m3.amd.ops.indexer_cp_exchange, module docstring:
+ *     forced init/local blocks are pinned and never dropped; block ids must
+ *     stay below 0xFFFF (local_topk_keys).
+ *   vllm.models.minimax_m3.amd.indexer_nvfp4, module docstring: an NVFP4 key
+ *     element is e4m3_rn_satfinite(e2m1 * scale).
+ *
+ * Conventions shared by every call
+ *   - D = 128 and the block (page) size is 128 tokens; both are fixed.
+ *   - Request i has query_len query tokens, rows i*query_len .. +query_len-1;
+ *     query j sits at position pos = seq_lens[i] - query_len + j and sees key
+ *     tokens 0..pos.  Its own block is c = pos / 128; blocks 0..c are visible.
+ *     A prefill of one request is query_len == seq_len.
+ *   - score[h, row, b] = sm_scale * max over visible tokens t of block b of
+ *     sum_d q[row, h, d] * k[t, d]   (fp32; natural units).
+ *   - Forced blocks of a row: 0..init_blocks-1 and c-local_blocks+1..c,
+ *     clipped to 0..c.  They take top-k slots.  The other visible blocks are
+ *     ranked by (score desc, id asc); the best topk - |forced| join them.
+ *     Output ids are ascending, then -1 up to topk.
+ *   - Every pointer is a device pointer unless its comment says otherwise.
+ *     The library never allocates or frees device memory, so every address
+ *     stays stable for CUDA graph capture.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous and never synchronise, except mm3idx_get_device_error.
+ *   - Calls return MM3IDX_OK (0) or a negative MM3IDX_ERR_* code and launch
+ *     nothing on error.  rows == 0 is a successful no-op.
+ *   - Problems found only by the GPU (a page id outside [0, num_pages),
+ *     seq_len > max_seq_len, seq_len < query_len, a bounded wait that ran
+ *     out) set bits of a device status word instead of trapping; the affected
+ *     rows are computed as if the bad page held no visible tokens, lengths
+ *     are clamped to max_seq_len, and rows with pos < 0 see no blocks.
+ */
+#ifndef MM3IDX_H
+#define MM3IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define MM3IDX_OK                    0
+#define MM3IDX_ERR_INVALID_ARGUMENT (-1)  /* null pointer or negative size     */
+#define MM3IDX_ERR_Q_LAYOUT         (-2)  /* q not 16-byte aligned, strides not multiples of 8 elements */
+#define MM3IDX_ERR_CACHE_LAYOUT     (-3)  /* num_pages < 1, too many pages, or misaligned cache */
+#define MM3IDX_ERR_TABLE_LAYOUT     (-4)  /* table_width < cdiv(max_seq_len,128) or table_stride < table_width */
+#define MM3IDX_ERR_TOO_MANY_BLOCKS  (-5)  /* cdiv(max_seq_len,128) >= 0xFFFF   */
+#define MM3IDX_ERR_QUERY_LEN        (-6)  /* query_len < 1 or max_seq_len < query_len */
+#define MM3IDX_ERR_TOPK             (-7)  /* topk outside 1..MM3IDX_MAX_TOPK, init/local < 0, init+local > topk */
+#define MM3IDX_ERR_OUT_LAYOUT       (-8)  /* output strides overlap or width too small */
+#define MM3IDX_ERR_WORKSPACE        (-9)  /* workspace too small or not 256-byte aligned */
+#define MM3IDX_ERR_UNSUPPORTED      (-10) /* shape this entry point does not serve (see its comment) */
+#define MM3IDX_ERR_CUDA             (-11) /* a CUDA runtime / driver call failed */
+
+/* bits of the device status word (mm3idx_get_device_error) */
+#define MM3IDX_DEV_BAD_PAGE      1  /* a block table entry outside [0, num_pages) was read */
+#define MM3IDX_DEV_SEQ_TOO_LONG  2  /* seq_lens[i] > max_seq_len (clamped)  */
+#define MM3IDX_DEV_SEQ_TOO_SHORT 4  /* seq_lens[i] < query_len              */
+#define MM3IDX_DEV_TIMEOUT       8  /* an on-chip pipeline wait gave up; outputs of that launch are invalid */
+
+#define MM3IDX_MAX_TOPK            32  /* largest topk served                  */
+#define MM3IDX_MAX_DECODE_ROWS     32  /* heads * query_len limit of the fused decode kernel */
+
+/* workspace kinds for mm3idx_workspace_bytes */
+#define MM3IDX_OP_DECODE   1
+#define MM3IDX_OP_PREFILL  2
+
+/* The problem every scoring call reads.  Host struct; the pointers in it are
+ * device pointers. */
+typedef struct mm3idx_problem {
+    const void    *idx_q;          /* bf16 [rows, heads, 128], d stride 1, 16-byte aligned */
+    int64_t        q_token_stride; /* elements between consecutive rows (multiple of 8)   */
+    int64_t        q_head_stride;  /* elements between consecutive heads (multiple of 8)  */
+    int32_t        heads;          /* index heads, >= 1; all heads share the keys         */
+    const void    *index_cache;    /* bf16 [num_pages, 128, 128] contiguous, 16-byte aligned;
+                                      for the NVFP4 entry point: uint8 codes [num_pages, 128, 64],
+                                      element 2e in the low nibble, 2e+1 in the high nibble */
+    const void    *index_scales;   /* NVFP4 only: uint8 e4m3 [num_pages, 128, 8], scale g covers
+                                      d in [16g, 16g+16); must be NULL for bf16 calls       */
+    int32_t        num_pages;      /* pages in the cache, >= 1                              */
+    const int32_t *block_table;    /* int32 [num_reqs, table_stride]; logical block -> page */
+    int64_t        table_stride;   /* elements between table rows, >= table_width           */
+    int32_t        table_width;    /* readable columns, >= cdiv(max_seq_len, 128)           */
+    const int32_t *seq_lens;       /* int32 [num_reqs]                                      */
+    int32_t        num_reqs;       /* requests, >= 0                                        */
+    int32_t        query_len;      /* query tokens per request, >= 1                        */
+    int32_t        max_seq_len;    /* capture-stable bound on seq_lens (pass max_model_len) */
+    float          sm_scale;       /* multiplies every score                                */
+} mm3idx_problem_t;
+
+/*
+ * mm3idx_score -- block scores to HBM (index_topk, minimax_m3_index_score;
+ * indexer_context_parallel, indexer_context_scores for the sm_scale factor).
+ *
+ * out: fp32, element [h, row, b] at out[h*out_head_stride + row*out_row_stride + b]
+ * for b < cdiv(max_seq_len, 128).  Visible blocks get their score; blocks past
+ * the row's own block get -inf.  Columns at or beyond cdiv(max_seq_len,128)
+ * are not touched.  Requires out_row_stride >= cdiv(max_seq_len,128) and
+ * out_head_stride >= rows * out_row_stride.  Rows with heads*query_len <= 32
+ * run on the streaming decode kernel, others on the tensor-core prefill
+ * kernel.  bf16 cache only.
+ */
+int mm3idx_score(const mm3idx_problem_t *p, float *out, int64_t out_head_stride,
+                 int64_t out_row_stride, void *stream);
+
+/*
+ * mm3idx_topk -- top-k selection from a score tensor (index_topk,
+ * minimax_m3_index_topk).  score: fp32 [heads, rows, >= visible blocks] with
+ * the given strides; only each row's visible blocks 0..c are read.  out: int32,
+ * element [h, row, k] at out[h*out_head_stride + row*out_row_stride + k],
+ * k < topk.  seq_lens/num_reqs/query_len/max_seq_len follow the problem
+ * conventions (c comes from the row's position).
+ */
+int mm3idx_topk(const float *score, int64_t score_head_stride,
+                int64_t score_row_stride, int32_t heads,
+                const int32_t *seq_lens, int32_t num_reqs, int32_t query_len,
+                int32_t max_seq_len, int32_t topk, int32_t init_blocks,
+                int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                int64_t out_row_stride, void *stream);
+
+/*
+ * mm3idx_workspace_bytes -- device workspace the fused calls need.
+ * op = MM3IDX_OP_DECODE: per-request completion counters plus partial top-k
+ * candidate lists (depends on the current device's SM count).
+ * op = MM3IDX_OP_PREFILL: the fp32 score scratch [heads, rows, roundup(cdiv(max_seq_len,128), 4)].
+ * Writes the size to *bytes.  Reads the current device's attributes; no
+ * allocation.
+ */
+int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs,
+                           int32_t query_len, int32_t max_seq_len,
+                           int32_t topk, size_t *bytes);
+
+/*
+ * mm3idx_decode -- fused decode: block scores and top-k in one persistent
+ * kernel; the fp32 score row never goes to HBM (index_topk,
+ * minimax_m3_index_decode).  Requires heads * query_len <= 32.
+ *
+ * out: int32 [h, row, k] at out[h*out_head_stride + row*out_row_stride + k].
+ * workspace: >= mm3idx_workspace_bytes(MM3IDX_OP_DECODE, ...) bytes, 256-byte
+ * aligned, zero-filled by the caller once before its first use (the
+ * completion counters must start at zero); every completed launch leaves the
+ * counters at zero again.  Launches that share a workspace must not overlap.
+ */
+int mm3idx_decode(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
+                  int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                  int64_t out_row_stride, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * mm3idx_decode_nvfp4 -- mm3idx_decode over NVFP4 index-K pages
+ * (indexer_nvfp4 module docstring): p->index_cache holds the e2m1 codes and
+ * p->index_scales the e4m3 scales (layouts in mm3idx_problem_t).  Each key
+ * element is e4m3_rn_satfinite(e2m1 * scale), exact in bf16, scored against
+ * the bf16 query like the bf16 path.  Same workspace rules as mm3idx_decode.
+ */
+int mm3idx_decode_nvfp4(const mm3idx_problem_t *p, int32_t topk,
+                        int32_t init_blocks, int32_t local_blocks, int32_t *out,
+                        int64_t out_head_stride, int64_t out_row_stride,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mm3idx_prefill -- prefill scoring on the tensor cores followed by the
+ * selector (index_topk, minimax_m3_index_score then minimax_m3_index_topk).
+ * The fp32 scores go to the workspace (size from
+ * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL, ...), 256-byte aligned, no
+ * initialisation needed).  out as in mm3idx_decode.  Any heads/query_len.
+ */
+int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
+                   int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                   int64_t out_row_stride, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * mm3idx_get_device_error -- synchronises `stream`, then reads and clears the
+ * device status word of the current device (MM3IDX_DEV_* bits) into *code.
+ */
+int mm3idx_get_device_error(void *stream, int32_t *code);
+
+/* Human-readable text of a status code (static storage). */
+const char *mm3idx_status_string(int status);
+
+/* Library version, for the binding's sanity check. */
+int32_t mm3idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM3IDX_H */

@@ -1,0 +1,276 @@
+"""GB300 (sm_103a) MiniMax-M3 lightning-indexer: causal block scoring of bf16
+index queries against a paged index-K cache, and top-k block selection with
+forced init/local blocks.
+
+This module is the thin Python binding of ``libmm3idx.so`` (C ABI in
+``include/mm3idx.h``).  It only marshals torch tensors into pointers, strides
+and the current CUDA stream; every step of the computation runs in the
+library's CUDA kernels.  Importing it fails loudly when the library has not
+been built: there is no CPU or PyTorch fallback.
+
+Entry points (names after the vLLM MiniMax-M3 ``index_topk`` page):
+
+* :func:`score`        -- fp32 block scores [heads, rows, cdiv(max_seq_len,128)]
+* :func:`topk`         -- ids from a score tensor
+* :func:`decode`       -- fused score + top-k for short query runs
+* :func:`decode_nvfp4` -- the same over NVFP4 index-K pages
+* :func:`prefill`      -- tensor-core scores + selector for long query runs
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libmm3idx.so")
+
+OK = 0
+OP_DECODE = 1
+OP_PREFILL = 2
+MAX_TOPK = 32
+MAX_DECODE_ROWS = 32
+DEV_BAD_PAGE, DEV_SEQ_TOO_LONG, DEV_SEQ_TOO_SHORT, DEV_TIMEOUT = 1, 2, 4, 8
+
+
+class Mm3idxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``mm3idx_problem_t``."""
+    _fields_ = [
+        ("idx_q", ctypes.c_void_p),
+        ("q_token_stride", ctypes.c_int64),
+        ("q_head_stride", ctypes.c_int64),
+        ("heads", ctypes.c_int32),
+        ("index_cache", ctypes.c_void_p),
+        ("index_scales", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p),
+        ("table_stride", ctypes.c_int64),
+        ("table_width", ctypes.c_int32),
+        ("seq_lens", ctypes.c_void_p),
+        ("num_reqs", ctypes.c_int32),
+        ("query_len", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float),
+    ]
+
+
+SYMBOLS = {
+    "mm3idx_version": (ctypes.c_int32, []),
+    "mm3idx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mm3idx_workspace_bytes": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "mm3idx_score": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.c_void_p]),
+    "mm3idx_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "mm3idx_decode": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "mm3idx_decode_nvfp4": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.c_void_p]),
+    "mm3idx_prefill": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "mm3idx_get_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+}
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it first "
+            "(python -m sparse_attention_block_paged_gb300.build); there is no fallback")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SYMBOLS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+LIB_PATH = _LIB_PATH
+
+
+def status_string(status: int) -> str:
+    return lib.mm3idx_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise Mm3idxError(status, what)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cdiv(a, b):
+    return (a + b - 1) // b
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale,
+             index_scales=None, nvfp4=False):
+    """Layout checks of check_context_score_inputs, then the C struct."""
+    _need(idx_q.ndim == 3 and idx_q.shape[2] == 128 and idx_q.dtype == torch.bfloat16
+          and idx_q.stride(2) == 1, "index queries must be BF16 [tokens,heads,128] with contiguous D")
+    if nvfp4:
+        _need(index_cache.dtype == torch.uint8 and index_cache.ndim == 3
+              and tuple(index_cache.shape[1:]) == (128, 64) and index_cache.is_contiguous(),
+              "NVFP4 codes must be contiguous uint8 [pages,128,64]")
+        _need(index_scales is not None and index_scales.dtype == torch.uint8
+              and tuple(index_scales.shape) == (index_cache.shape[0], 128, 8)
+              and index_scales.is_contiguous(), "NVFP4 scales must be contiguous uint8 [pages,128,8]")
+    else:
+        _need(index_cache.ndim == 3 and tuple(index_cache.shape[1:]) == (128, 128)
+              and index_cache.is_contiguous() and index_cache.shape[0] >= 1,
+              "index cache must be contiguous non-empty [pages,128,128]")
+        _need(index_cache.dtype == torch.bfloat16, "index cache must be bf16")
+    _need(block_table.ndim == 2 and block_table.stride(1) == 1 and block_table.dtype == torch.int32
+          and seq_lens.ndim == 1 and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous(),
+          "block table and lengths must be int32 with unit stride")
+    dev = idx_q.device
+    _need(dev.type == "cuda" and all(t.device == dev for t in (index_cache, block_table, seq_lens))
+          and (index_scales is None or index_scales.device == dev),
+          "all score inputs must be on the same GPU")
+    num_reqs = seq_lens.shape[0]
+    _need(idx_q.shape[0] == num_reqs * query_len, "rows != batch * query_len")
+    _need(block_table.shape[0] == num_reqs, "block table must have one row per request")
+    p = Problem()
+    p.idx_q = idx_q.data_ptr()
+    p.q_token_stride = idx_q.stride(0)
+    p.q_head_stride = idx_q.stride(1)
+    p.heads = idx_q.shape[1]
+    p.index_cache = index_cache.data_ptr()
+    p.index_scales = index_scales.data_ptr() if index_scales is not None else None
+    p.num_pages = index_cache.shape[0]
+    p.block_table = block_table.data_ptr()
+    p.table_stride = block_table.stride(0) if num_reqs > 1 else max(block_table.shape[1], 1)
+    p.table_width = block_table.shape[1]
+    p.seq_lens = seq_lens.data_ptr()
+    p.num_reqs = num_reqs
+    p.query_len = query_len
+    p.max_seq_len = max_seq_len
+    p.sm_scale = sm_scale
+    return p
+
+
+def workspace_bytes(op: int, heads: int, num_reqs: int, query_len: int, max_seq_len: int,
+                    topk: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.mm3idx_workspace_bytes(op, heads, num_reqs, query_len, max_seq_len, topk,
+                                      ctypes.byref(n)), "mm3idx_workspace_bytes")
+    return n.value
+
+
+def new_workspace(op, heads, num_reqs, query_len, max_seq_len, topk, device=None):
+    """A zero-filled workspace (uint8, 256-byte aligned by the caching allocator)."""
+    n = workspace_bytes(op, heads, num_reqs, query_len, max_seq_len, topk)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def score(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, sm_scale,
+          out=None, stream=None):
+    """fp32 [heads, rows, cdiv(max_seq_len,128)] block scores (-inf past each
+    row's own block); written into ``out[:, :rows, :width]`` when given."""
+    p = _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale)
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    width = _cdiv(max_seq_len, 128)
+    if out is None:
+        out = torch.empty((heads, rows, width), dtype=torch.float32, device=idx_q.device)
+    _need(out.dtype == torch.float32 and out.ndim == 3 and out.shape[0] == heads
+          and out.shape[1] >= rows and out.shape[2] >= width and out.stride(2) == 1,
+          "out must be fp32 [heads, >=rows, >=cdiv(max_seq_len,128)] with unit inner stride")
+    _check(lib.mm3idx_score(ctypes.byref(p), out.data_ptr(), out.stride(0), out.stride(1),
+                            _stream(stream)), "mm3idx_score")
+    return out[:, :rows, :width]
+
+
+def _ids_out(out, heads, rows, topk, device):
+    if out is None:
+        out = torch.empty((heads, rows, topk), dtype=torch.int32, device=device)
+    _need(out.dtype == torch.int32 and out.ndim == 3 and out.shape[0] == heads
+          and out.shape[1] >= rows and out.shape[2] == topk and out.stride(2) == 1,
+          "out must be int32 [heads, >=rows, topk] with unit inner stride")
+    return out
+
+
+def topk(score_t, seq_lens, *, query_len, max_seq_len, topk, init_blocks, local_blocks,
+         out=None, stream=None):
+    """int32 [heads, rows, topk] ids (ascending, -1 pad) from a score tensor."""
+    _need(score_t.dtype == torch.float32 and score_t.ndim == 3 and score_t.stride(2) == 1,
+          "score must be fp32 [heads, rows, blocks] with unit inner stride")
+    heads, rows = score_t.shape[0], seq_lens.shape[0] * query_len
+    _need(score_t.shape[1] >= rows and score_t.shape[2] >= _cdiv(max_seq_len, 128),
+          "score narrower than the rows or cdiv(max_seq_len,128)")
+    out = _ids_out(out, heads, rows, topk, score_t.device)
+    _check(lib.mm3idx_topk(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,
+                           seq_lens.data_ptr(), seq_lens.shape[0], query_len, max_seq_len, topk,
+                           init_blocks, local_blocks, out.data_ptr(), out.stride(0), out.stride(1),
+                           _stream(stream)), "mm3idx_topk")
+    return out[:, :rows, :]
+
+
+def _fused(fn, name, op, idx_q, cache, block_table, seq_lens, scales, nvfp4, query_len,
+           max_seq_len, topk, init_blocks, local_blocks, sm_scale, out, workspace, stream):
+    p = _problem(idx_q, cache, block_table, seq_lens, query_len, max_seq_len, sm_scale,
+                 index_scales=scales, nvfp4=nvfp4)
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    out = _ids_out(out, heads, rows, topk, idx_q.device)
+    if workspace is None:
+        workspace = new_workspace(op, heads, seq_lens.shape[0], query_len, max_seq_len, topk,
+                                  idx_q.device)
+    _check(fn(ctypes.byref(p), topk, init_blocks, local_blocks, out.data_ptr(), out.stride(0),
+              out.stride(1), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+              _stream(stream)), name)
+    return out[:, :rows, :]
+
+
+def decode(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
+           init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
+    """Fused decode score + top-k (heads * query_len <= 32).  ``workspace`` must
+    come from :func:`new_workspace` (zeroed once, reused across calls)."""
+    return _fused(lib.mm3idx_decode, "mm3idx_decode", OP_DECODE, idx_q, index_cache, block_table,
+                  seq_lens, None, False, query_len, max_seq_len, topk, init_blocks, local_blocks,
+                  sm_scale, out, workspace, stream)
+
+
+def decode_nvfp4(idx_q, codes, scales, block_table, seq_lens, *, query_len, max_seq_len, topk,
+                 init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
+    """:func:`decode` over NVFP4 pages (codes uint8 [pages,128,64], scales
+    uint8 e4m3 [pages,128,8])."""
+    return _fused(lib.mm3idx_decode_nvfp4, "mm3idx_decode_nvfp4", OP_DECODE, idx_q, codes,
+                  block_table, seq_lens, scales, True, query_len, max_seq_len, topk, init_blocks,
+                  local_blocks, sm_scale, out, workspace, stream)
+
+
+def prefill(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
+            init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
+    """Tensor-core prefill scores (to the workspace) followed by the selector."""
+    return _fused(lib.mm3idx_prefill, "mm3idx_prefill", OP_PREFILL, idx_q, index_cache,
+                  block_table, seq_lens, None, False, query_len, max_seq_len, topk, init_blocks,
+                  local_blocks, sm_scale, out, workspace, stream)
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream, read and clear the device status word."""
+    v = ctypes.c_int32(0)
+    _check(lib.mm3idx_get_device_error(_stream(stream), ctypes.byref(v)), "mm3idx_get_device_error")
+    return v.value

@@ -1,0 +1,434 @@
+// api.cu -- the extern "C" boundary declared in include/mm3idx.h: argument
+// validation (the layout rules of the vLLM MiniMax-M3 pages, mapped to status
+// codes instead of ValueError), TMA tensor-map encoding, grid sizing and
+// kernel dispatch.  No device memory is allocated or freed here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mm3idx.h"
+#include "internal.h"
+
+using namespace mm3idx;
+
+namespace {
+
+constexpr int32_t kVersion = 1;
+constexpr int kMaxDevices = 64;
+
+// Device status word (MM3IDX_DEV_* bits), one per device context.
+__device__ int32_t g_status_word;
+
+struct DeviceInfo {
+  int sms = 0;
+  int32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MM3IDX_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return MM3IDX_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MM3IDX_ERR_CUDA;
+    d.status = static_cast<int32_t*>(p);
+    d.sms = sms;
+  }
+  *out = &d;
+  return MM3IDX_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [pages*128, 128] bf16 rows, 64-column boxes of 128 rows, 128-byte swizzle.
+int make_kmap(const mm3idx_problem_t* p, CUtensorMap* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return MM3IDX_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
+                              static_cast<cuuint64_t>(p->num_pages) * kBlock};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->index_cache), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MM3IDX_OK : MM3IDX_ERR_CACHE_LAYOUT;
+}
+
+// [rows, heads, 128] bf16 queries, boxes of 64 columns x 1 head x 128 rows.
+int make_qmap(const mm3idx_problem_t* p, CUtensorMap* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return MM3IDX_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p->heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->q_head_stride) * 2,
+                                 static_cast<cuuint64_t>(p->q_token_stride) * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->idx_q), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MM3IDX_OK : MM3IDX_ERR_Q_LAYOUT;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Layout rules of check_context_score_inputs / indexer_context_scores and
+// minimax_m3_index_decode, as status codes.
+int check_problem(const mm3idx_problem_t* p, bool nvfp4) {
+  if (!p) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (p->heads < 1 || p->num_reqs < 0) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (p->query_len < 1 || p->max_seq_len < p->query_len) return MM3IDX_ERR_QUERY_LEN;
+  if (static_cast<int64_t>(p->num_reqs) * p->query_len >= INT_MAX) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (!(p->sm_scale > 0.0f) || !std::isfinite(p->sm_scale)) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (cdiv(p->max_seq_len, kBlock) >= 0xFFFF) return MM3IDX_ERR_TOO_MANY_BLOCKS;
+  if (p->num_reqs == 0) return MM3IDX_OK;
+  if (!p->idx_q || !p->index_cache || !p->block_table || !p->seq_lens)
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (!aligned16(p->idx_q) || p->q_token_stride % 8 != 0 || p->q_head_stride % 8 != 0 ||
+      p->q_token_stride <= 0 || (p->heads > 1 && p->q_head_stride <= 0))
+    return MM3IDX_ERR_Q_LAYOUT;
+  if (p->num_pages < 1 || p->num_pages > INT_MAX / kBlock || !aligned16(p->index_cache))
+    return MM3IDX_ERR_CACHE_LAYOUT;
+  if (nvfp4 != (p->index_scales != nullptr)) return MM3IDX_ERR_CACHE_LAYOUT;
+  if (nvfp4 && !aligned16(p->index_scales)) return MM3IDX_ERR_CACHE_LAYOUT;
+  if (p->table_width < cdiv(p->max_seq_len, kBlock) || p->table_stride < p->table_width)
+    return MM3IDX_ERR_TABLE_LAYOUT;
+  return MM3IDX_OK;
+}
+
+int check_topk(int32_t topk, int32_t init_blocks, int32_t local_blocks) {
+  if (topk < 1 || topk > MM3IDX_MAX_TOPK || init_blocks < 0 || local_blocks < 0 ||
+      static_cast<int64_t>(init_blocks) + local_blocks > topk)
+    return MM3IDX_ERR_TOPK;
+  return MM3IDX_OK;
+}
+
+// Row-major [heads, rows, width] with the given strides must not overlap.
+bool out_ok(int64_t head_stride, int64_t row_stride, int32_t heads, int64_t rows, int64_t width) {
+  if (row_stride < width) return false;
+  if (heads > 1 && head_stride < rows * row_stride) return false;
+  return true;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MM3IDX_OK : MM3IDX_ERR_CUDA; }
+
+size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len, int32_t topk) {
+  const int R = heads * query_len;
+  const size_t counters = (static_cast<size_t>(num_reqs) * 4 + 255) / 256 * 256;
+  const size_t slots = static_cast<size_t>(sms) * decode_ctas_per_sm() + num_reqs;
+  return counters + slots * decode_nr(R) * decode_tk(topk) * 8;
+}
+
+size_t prefill_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len, int32_t max_seq_len) {
+  const int64_t w = (cdiv(max_seq_len, kBlock) + 3) / 4 * 4;
+  return static_cast<size_t>(heads) * num_reqs * query_len * w * 4;
+}
+
+DecodeArgs decode_args(const mm3idx_problem_t* p, int* status) {
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(p->idx_q);
+  a.q_tok = p->q_token_stride;
+  a.q_head = p->q_head_stride;
+  a.heads = p->heads;
+  a.rows_per_req = p->heads * p->query_len;
+  a.table = p->block_table;
+  a.table_stride = p->table_stride;
+  a.seq_lens = p->seq_lens;
+  a.num_reqs = p->num_reqs;
+  a.query_len = p->query_len;
+  a.max_seq_len = p->max_seq_len;
+  a.num_pages = p->num_pages;
+  a.sm_scale = p->sm_scale;
+  a.status = status;
+  return a;
+}
+
+int decode_grid(const mm3idx_problem_t* p, int sms) {
+  const int64_t bound = static_cast<int64_t>(p->num_reqs) * cdiv(p->max_seq_len, kBlock);
+  int64_t g = static_cast<int64_t>(sms) * decode_ctas_per_sm();
+  if (bound < g) g = bound;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init_blocks,
+               int32_t local_blocks, int32_t* out, int64_t out_head_stride, int64_t out_row_stride,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(p, nvfp4);
+  if (rc) return rc;
+  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
+  if (rows == 0) return MM3IDX_OK;
+  if (p->heads * static_cast<int64_t>(p->query_len) > MM3IDX_MAX_DECODE_ROWS)
+    return MM3IDX_ERR_UNSUPPORTED;
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const size_t need = decode_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len, topk);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MM3IDX_ERR_WORKSPACE;
+  DecodeArgs a = decode_args(p, dev->status);
+  a.mode = kModeSelect;
+  a.topk = topk;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.ids = out;
+  a.i_head = out_head_stride;
+  a.i_row = out_row_stride;
+  a.counters = static_cast<int32_t*>(workspace);
+  a.partials = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) +
+                                           (static_cast<size_t>(p->num_reqs) * 4 + 255) / 256 * 256);
+  const int grid = decode_grid(p, dev->sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nvfp4) {
+    a.codes = static_cast<const uint8_t*>(p->index_cache);
+    a.scales = static_cast<const uint8_t*>(p->index_scales);
+    return cuda_status(launch_decode_nvfp4(a, grid, s));
+  }
+  CUtensorMap kmap;
+  if ((rc = make_kmap(p, &kmap))) return rc;
+  return cuda_status(launch_decode_bf16(kmap, a, grid, s));
+}
+
+int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, int64_t row_stride,
+                   int32_t fill_width, int sms, int32_t* status, cudaStream_t s) {
+  PrefillArgs a{};
+  a.heads = p->heads;
+  a.num_reqs = p->num_reqs;
+  a.query_len = p->query_len;
+  a.max_seq_len = p->max_seq_len;
+  a.num_pages = p->num_pages;
+  a.table = p->block_table;
+  a.table_stride = p->table_stride;
+  a.seq_lens = p->seq_lens;
+  a.sm_scale = p->sm_scale;
+  a.score = out;
+  a.s_head = head_stride;
+  a.s_row = row_stride;
+  a.fill_width = fill_width;
+  a.qtiles = static_cast<int32_t>(cdiv(p->query_len, 128));
+  const int64_t wprefix = static_cast<int64_t>(p->max_seq_len) - p->query_len;
+  int64_t uph = 0;
+  for (int qt = 0; qt < a.qtiles; ++qt) {
+    const int64_t last = wprefix + std::min<int64_t>(static_cast<int64_t>(qt) * 128 + 127, p->query_len - 1);
+    uph += (last >> 7) + 1;
+  }
+  a.units_per_head = uph;
+  a.total_units = uph * p->heads * p->num_reqs;
+  a.status = status;
+  int64_t grid = sms;
+  if (a.total_units < grid) grid = a.total_units;
+  if (grid < 1) return MM3IDX_OK;
+  CUtensorMap qmap, kmap;
+  int rc;
+  if ((rc = make_qmap(p, &qmap))) return rc;
+  if ((rc = make_kmap(p, &kmap))) return rc;
+  return cuda_status(launch_prefill(qmap, kmap, a, static_cast<int>(grid), s));
+}
+
+SelectArgs select_args(const float* score, int64_t sh, int64_t sr, int32_t heads,
+                       const int32_t* seq_lens, int32_t num_reqs, int32_t query_len,
+                       int32_t max_seq_len, int32_t topk, int32_t init_blocks,
+                       int32_t local_blocks, int32_t* out, int64_t oh, int64_t orow,
+                       int32_t* status) {
+  SelectArgs a{};
+  a.score = score;
+  a.s_head = sh;
+  a.s_row = sr;
+  a.heads = heads;
+  a.seq_lens = seq_lens;
+  a.num_reqs = num_reqs;
+  a.query_len = query_len;
+  a.max_seq_len = max_seq_len;
+  a.topk = topk;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.ids = out;
+  a.i_head = oh;
+  a.i_row = orow;
+  a.status = status;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mm3idx_version(void) { return kVersion; }
+
+const char* mm3idx_status_string(int status) {
+  switch (status) {
+    case MM3IDX_OK: return "ok";
+    case MM3IDX_ERR_INVALID_ARGUMENT: return "invalid argument (null pointer, negative size or non-positive sm_scale)";
+    case MM3IDX_ERR_Q_LAYOUT: return "index queries must be bf16 [tokens, heads, 128], 16-byte aligned, strides multiples of 8";
+    case MM3IDX_ERR_CACHE_LAYOUT: return "index cache must be contiguous, non-empty and 16-byte aligned";
+    case MM3IDX_ERR_TABLE_LAYOUT: return "block table narrower than cdiv(max_seq_len, 128) or stride < width";
+    case MM3IDX_ERR_TOO_MANY_BLOCKS: return "block ids must stay below 0xFFFF";
+    case MM3IDX_ERR_QUERY_LEN: return "query_len must be >= 1 and <= max_seq_len";
+    case MM3IDX_ERR_TOPK: return "topk must be 1..32 with 0 <= init, local and init + local <= topk";
+    case MM3IDX_ERR_OUT_LAYOUT: return "output buffer too small or strides overlap";
+    case MM3IDX_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case MM3IDX_ERR_UNSUPPORTED: return "shape not served by this entry point";
+    case MM3IDX_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t query_len,
+                           int32_t max_seq_len, int32_t topk, size_t* bytes) {
+  if (!bytes || heads < 1 || num_reqs < 0 || query_len < 1 || max_seq_len < 1)
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (op == MM3IDX_OP_DECODE) {
+    if (topk < 1 || topk > MM3IDX_MAX_TOPK) return MM3IDX_ERR_TOPK;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    *bytes = decode_ws_bytes(dev->sms, heads, num_reqs, query_len, topk);
+    return MM3IDX_OK;
+  }
+  if (op == MM3IDX_OP_PREFILL) {
+    *bytes = prefill_ws_bytes(heads, num_reqs, query_len, max_seq_len);
+    return MM3IDX_OK;
+  }
+  return MM3IDX_ERR_INVALID_ARGUMENT;
+}
+
+int mm3idx_score(const mm3idx_problem_t* p, float* out, int64_t out_head_stride,
+                 int64_t out_row_stride, void* stream) {
+  int rc = check_problem(p, false);
+  if (rc) return rc;
+  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
+  if (rows == 0) return MM3IDX_OK;
+  const int32_t width = static_cast<int32_t>(cdiv(p->max_seq_len, kBlock));
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, width))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (static_cast<int64_t>(p->heads) * p->query_len <= MM3IDX_MAX_DECODE_ROWS) {
+    DecodeArgs a = decode_args(p, dev->status);
+    a.mode = kModeScore;
+    a.topk = 1;
+    a.score = out;
+    a.s_head = out_head_stride;
+    a.s_row = out_row_stride;
+    a.fill_width = width;
+    CUtensorMap kmap;
+    if ((rc = make_kmap(p, &kmap))) return rc;
+    return cuda_status(launch_decode_bf16(kmap, a, decode_grid(p, dev->sms), s));
+  }
+  return prefill_scores(p, out, out_head_stride, out_row_stride, width, dev->sms, dev->status, s);
+}
+
+int mm3idx_topk(const float* score, int64_t score_head_stride, int64_t score_row_stride,
+                int32_t heads, const int32_t* seq_lens, int32_t num_reqs, int32_t query_len,
+                int32_t max_seq_len, int32_t topk, int32_t init_blocks, int32_t local_blocks,
+                int32_t* out, int64_t out_head_stride, int64_t out_row_stride, void* stream) {
+  if (heads < 1 || num_reqs < 0) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (query_len < 1 || max_seq_len < query_len) return MM3IDX_ERR_QUERY_LEN;
+  if (cdiv(max_seq_len, kBlock) >= 0xFFFF) return MM3IDX_ERR_TOO_MANY_BLOCKS;
+  int rc = check_topk(topk, init_blocks, local_blocks);
+  if (rc) return rc;
+  const int64_t rows = static_cast<int64_t>(num_reqs) * query_len;
+  if (rows == 0) return MM3IDX_OK;
+  if (!score || !seq_lens || !out) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (!out_ok(score_head_stride, score_row_stride, heads, rows, cdiv(max_seq_len, kBlock)) ||
+      !out_ok(out_head_stride, out_row_stride, heads, rows, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  SelectArgs a = select_args(score, score_head_stride, score_row_stride, heads, seq_lens, num_reqs,
+                             query_len, max_seq_len, topk, init_blocks, local_blocks, out,
+                             out_head_stride, out_row_stride, dev->status);
+  return cuda_status(launch_select(a, dev->sms, static_cast<cudaStream_t>(stream)));
+}
+
+int mm3idx_decode(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                  int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                  int64_t out_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
+                    out_row_stride, workspace, workspace_bytes, stream);
+}
+
+int mm3idx_decode_nvfp4(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                        int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                        int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  return run_decode(p, true, topk, init_blocks, local_blocks, out, out_head_stride,
+                    out_row_stride, workspace, workspace_bytes, stream);
+}
+
+int mm3idx_prefill(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                   int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                   int64_t out_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(p, false);
+  if (rc) return rc;
+  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
+  if (rows == 0) return MM3IDX_OK;
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  const size_t need = prefill_ws_bytes(p->heads, p->num_reqs, p->query_len, p->max_seq_len);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MM3IDX_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t w = (cdiv(p->max_seq_len, kBlock) + 3) / 4 * 4;
+  float* score = static_cast<float*>(workspace);
+  if ((rc = prefill_scores(p, score, rows * w, w, 0, dev->sms, dev->status, s))) return rc;
+  SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
+                             p->max_seq_len, topk, init_blocks, local_blocks, out, out_head_stride,
+                             out_row_stride, dev->status);
+  return cuda_status(launch_select(a, dev->sms, s));
+}
+
+int mm3idx_get_device_error(void* stream, int32_t* code) {
+  if (!code) return MM3IDX_ERR_INVALID_ARGUMENT;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MM3IDX_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MM3IDX_ERR_CUDA;
+  const int32_t zero = 0;
+  if (cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MM3IDX_ERR_CUDA;
+  *code = v;
+  return MM3IDX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,749 @@
+// decode.cu -- persistent, warp-specialised decode kernel: causal block
+// scoring of a few query rows per request against the paged index-K cache,
+// with either the fp32 scores written out (score mode) or a fused top-k
+// selector whose scores never leave the chip (select mode).
+//
+// What it computes follows the vLLM MiniMax-M3 "index_topk" page
+// (module docstring; minimax_m3_index_decode: fused decode score + adaptive
+// top-k, ids 0-indexed with -1 pad, completion counters that the last arriving
+// program resets) and "indexer_cp_exchange" (forced init/local blocks are
+// pinned, packed 64-bit candidate keys).  The design is ours:
+//
+//   * The work list is every (request, logical block) pair of the batch,
+//     flattened request-major.  Each CTA takes one contiguous, equal share, so
+//     ragged lengths cost no imbalance.  Shares are computed on the device
+//     from seq_lens (no host round trip; CUDA-graph safe).
+//   * warp 0   : producer.  Walks the block table, TMA-loads each 32 KB page
+//                (two 64-column boxes, 128-byte swizzle) into a ring of stages;
+//                writes each request's query rows into a swizzled Q tile.
+//                NVFP4: bulk-copies the 9 KB code+scale page into a raw ring.
+//   * warps 6-9: (NVFP4 only) dequantise raw pages into bf16 tiles in the same
+//                swizzled layout, via a per-scale-byte magnitude table.
+//   * warp 1   : one thread issues tcgen05.mma, M = 128 tokens of the page,
+//                N = 16 or 32 query rows, K = 128; fp32 accumulators in TMEM,
+//                four buffers.
+//   * warps 2-5: epilogue.  tcgen05.ld of the 128 x N accumulator, causal mask
+//                on the last block only, max over the 128 tokens by a
+//                transposing warp-shuffle reduction plus a 4-way shared-memory
+//                combine, scale, then per row either a store of the score or
+//                an insertion into a sorted top-k candidate list in shared
+//                memory.  A request split across CTAs merges its candidate
+//                lists in the last CTA to finish it (atomic arrival count),
+//                which re-pins the forced blocks, writes the ids and resets
+//                the counter.
+//
+// Every wait is bounded (ptx.cuh).  A wait that gives up raises an abort flag
+// shared by the CTA's roles and the MM3IDX_DEV_TIMEOUT status bit.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/mm3idx.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mm3idx {
+namespace {
+
+constexpr int kAccBufs = 4;
+constexpr int kTileBytes = kBlock * kD * 2;          // 32 KB bf16 page
+constexpr int kFp4CodeBytes = kBlock * kD / 2;       // 8 KB
+constexpr int kFp4ScaleBytes = kBlock * kD / 16;     // 1 KB
+constexpr int kFp4RawBytes = kFp4CodeBytes + kFp4ScaleBytes;
+
+template <bool FP4, int NR, int TK>
+struct Cfg {
+  static constexpr int kStages = FP4 ? 3 : 5;
+  static constexpr int kRawStages = FP4 ? 8 : 0;
+  static constexpr int kThreads = FP4 ? 320 : 192;
+  static constexpr int kQBytes = NR * kD * 2;
+  static constexpr int oA = 0;
+  static constexpr int oRaw = oA + kStages * kTileBytes;
+  static constexpr int oQ = oRaw + kRawStages * kFp4RawBytes;
+  static constexpr int oTab = oQ + 2 * kQBytes;
+  static constexpr int oList = oTab + (FP4 ? 256 * 16 : 0);
+  static constexpr int oRed = oList + TK * NR * 8;
+  static constexpr int oBar = oRed + 2 * 4 * 32 * 4;
+  static constexpr int kBars = 2 * kStages + 2 * kRawStages + 2 * kAccBufs + 4 + 1;
+  static constexpr int oMisc = oBar + kBars * 8;
+  static constexpr int kSmem = oMisc + 64 + 1024;
+  static_assert(oQ % 1024 == 0, "Q tile must be 1024-byte aligned");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+struct Misc {
+  long long lo, hi, total, p0;
+  int i0;
+  uint32_t tmem;
+  int abort;
+  int last;
+};
+
+__device__ __forceinline__ int req_len(const DecodeArgs& a, int i) {
+  const int s = __ldg(a.seq_lens + i);
+  return min(max(s, 0), a.max_seq_len);
+}
+
+__device__ __forceinline__ int req_blocks(const DecodeArgs& a, int i) {
+  return (req_len(a, i) + kBlock - 1) / kBlock;
+}
+
+// Walks this CTA's share [lo, hi) of the flattened (request, block) list and
+// yields one segment (request, blocks [b0, b1)) at a time.
+struct Walker {
+  int i;
+  long long P, lo, hi;
+  __device__ bool next(const DecodeArgs& a, int& req, int& b0, int& b1, int& nb,
+                       long long& preq) {
+    while (i < a.num_reqs && P < hi) {
+      const int n = req_blocks(a, i);
+      const long long s = P > lo ? P : lo;
+      const long long e = (P + n) < hi ? (P + n) : hi;
+      req = i;
+      preq = P;
+      nb = n;
+      P += n;
+      ++i;
+      if (e > s) {
+        b0 = static_cast<int>(s - preq);
+        b1 = static_cast<int>(e - preq);
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+// The CTA whose share holds flattened position x.
+__device__ __forceinline__ int cta_of(long long x, long long total, int grid) {
+  return static_cast<int>(((x + 1) * grid - 1) / total);
+}
+
+// Warp 0: total block count, this CTA's share and the first request in it.
+__device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
+  long long total = 0;
+  for (int b = 0; b < a.num_reqs; b += 32) {
+    const int i = b + lane;
+    if (i < a.num_reqs) {
+      if (blockIdx.x == 0) {
+        const int raw = __ldg(a.seq_lens + i);
+        int bits = 0;
+        if (raw > a.max_seq_len) bits |= MM3IDX_DEV_SEQ_TOO_LONG;
+        if (raw < a.query_len) bits |= MM3IDX_DEV_SEQ_TOO_SHORT;
+        if (bits) atomicOr(a.status, bits);
+      }
+      total += req_blocks(a, i);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long lo = total * c / G, hi = total * (c + 1) / G;
+  long long P = 0, p0 = total;
+  int i0 = a.num_reqs;
+  for (int b = 0; b < a.num_reqs; b += 32) {
+    const int i = b + lane;
+    const long long nb = i < a.num_reqs ? req_blocks(a, i) : 0;
+    long long incl = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > lo);
+    if (hit) {
+      const int k = __ffs(hit) - 1;
+      const long long ex = __shfl_sync(0xffffffffu, incl - nb, k);
+      i0 = b + k;
+      p0 = P + ex;
+      break;
+    }
+    P += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    m->lo = lo;
+    m->hi = hi;
+    m->total = total;
+    m->i0 = i0;
+    m->p0 = p0;
+  }
+}
+
+// Writes request `req`'s query rows (row n = query j, head h with
+// n = j*heads + h) into a K-major 128-byte-swizzled tile of NR rows; rows past
+// heads*query_len are zero.
+template <int NR>
+__device__ void load_q_tile(const DecodeArgs& a, int req, uint8_t* dst, int lane) {
+  const int R = a.rows_per_req;
+  for (int item = lane; item < NR * 16; item += 32) {
+    const int n = item >> 4, ch = item & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < R) {
+      const int j = n / a.heads, h = n - j * a.heads;
+      const uint16_t* src = a.q + (static_cast<int64_t>(req) * a.query_len + j) * a.q_tok +
+                            static_cast<int64_t>(h) * a.q_head + ch * 8;
+      v = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+    const int sub = ch >> 3, c = ch & 7;
+    uint8_t* p = dst + sub * (NR * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4);
+    *reinterpret_cast<uint4*>(p) = v;
+  }
+}
+
+// Max over the warp's 32 lanes of each of NR columns.  Returns, in each lane,
+// the max of column (lane >> 1) for NR = 16 or column lane for NR = 32.
+template <int W, int O, int NR>
+__device__ __forceinline__ void tmax_stage(float (&v)[NR], int lane) {
+  if constexpr (W > 1) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int k = 0; k < W / 2; ++k) {
+      const float send = up ? v[k] : v[k + W / 2];
+      const float keep = up ? v[k + W / 2] : v[k];
+      v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+    }
+    tmax_stage<W / 2, O / 2, NR>(v, lane);
+  }
+}
+
+template <int NR>
+__device__ __forceinline__ float transpose_max(float (&v)[NR], int lane) {
+  tmax_stage<NR, 16, NR>(v, lane);
+  float r = v[0];
+  if constexpr (NR == 16) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, 1));
+  return r;
+}
+
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Insert `key` into row `n`'s descending candidate list L[k*NR + n].
+template <int NR, int TK>
+__device__ __forceinline__ void list_insert(uint64_t* L, int n, uint64_t key, int& cnt,
+                                            uint64_t& thr) {
+  if (cnt == TK && key <= thr) return;
+  int p = cnt < TK ? cnt : TK - 1;
+  while (p > 0) {
+    const uint64_t prev = L[(p - 1) * NR + n];
+    if (prev >= key) break;
+    L[p * NR + n] = prev;
+    --p;
+  }
+  L[p * NR + n] = key;
+  if (cnt < TK) ++cnt;
+  thr = cnt == TK ? L[(TK - 1) * NR + n] : 0ull;
+}
+
+// Forced blocks, then the best candidates, in ascending id order, -1 padded.
+template <int NR>
+__device__ void finalize_row(const DecodeArgs& a, const uint64_t* L, int n, int cnt, int c,
+                             int32_t* out) {
+  const int topk = a.topk;
+  if (c < 0) {
+    for (int k = 0; k < topk; ++k) out[k] = -1;
+    return;
+  }
+  const int f_lo = min(a.init_blocks, c + 1);
+  const int l_lo = max(f_lo, c - a.local_blocks + 1);
+  const int nf = f_lo + (c + 1 - l_lo);
+  const int take = min(topk - nf, cnt);
+  int o = 0;
+  for (int b = 0; b < f_lo; ++b) out[o++] = b;
+  for (int x = 0; x < take; ++x) {
+    const int bx = key_block(L[x * NR + n]);
+    int r = 0;
+    for (int y = 0; y < take; ++y) r += key_block(L[y * NR + n]) < bx;
+    out[f_lo + r] = bx;
+  }
+  o = f_lo + take;
+  for (int b = l_lo; b <= c; ++b) out[o++] = b;
+  for (; o < topk; ++o) out[o] = -1;
+}
+
+// ----------------------------------------------------------- NVFP4 dequant
+
+// Per-scale-byte magnitude table: for scale byte s, the bf16 bits of
+// e4m3_rn_satfinite(m * e4m3(s)) for the eight e2m1 magnitudes
+// m = 0, .5, 1, 1.5, 2, 3, 4, 6, split into low bytes (words 0-1) and high
+// bytes (words 2-3) for byte-permute lookups.
+__device__ void build_fp4_table(uint4* tab, int tid, int nthreads) {
+  const float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  for (int s = tid; s < 256; s += nthreads) {
+    const __half_raw sh = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(s), __NV_E4M3);
+    const float sv = __half2float(__half(sh));
+    uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_fp8_storage_t e =
+          __nv_cvt_float_to_fp8(mags[k] * sv, __NV_SATFINITE, __NV_E4M3);
+      const __half_raw eh = __nv_cvt_fp8_to_halfraw(e, __NV_E4M3);
+      const float ev = __half2float(__half(eh));
+      const uint32_t bits = __float_as_uint(ev) >> 16;  // exact: <= 4 significant bits
+      lo[k >> 2] |= (bits & 0xFFu) << ((k & 3) * 8);
+      hi[k >> 2] |= ((bits >> 8) & 0xFFu) << ((k & 3) * 8);
+    }
+    tab[s] = make_uint4(lo[0], lo[1], hi[0], hi[1]);
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight e2m1 codes (nibble k = element k, sign in bit 3) -> four bf16x2 words.
+__device__ __forceinline__ void dequant8(uint32_t codes, const uint4& t, uint32_t (&o)[4]) {
+  const uint32_t sel0 = codes & 0x7777u;
+  const uint32_t sel1 = (codes >> 16) & 0x7777u;
+  const uint32_t lo0 = prmt(t.x, t.y, sel0), hi0 = prmt(t.z, t.w, sel0);
+  const uint32_t lo1 = prmt(t.x, t.y, sel1), hi1 = prmt(t.z, t.w, sel1);
+  const uint32_t sa = (codes << 4) & 0x80808080u;  // signs of elements 0, 2, 4, 6
+  const uint32_t sb = codes & 0x80808080u;         // signs of elements 1, 3, 5, 7
+  const uint32_t h0 = hi0 ^ prmt(sa, sb, 0x5140u);
+  const uint32_t h1 = hi1 ^ prmt(sa, sb, 0x7362u);
+  o[0] = prmt(lo0, h0, 0x5140u);
+  o[1] = prmt(lo0, h0, 0x7362u);
+  o[2] = prmt(lo1, h1, 0x5140u);
+  o[3] = prmt(lo1, h1, 0x7362u);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <bool FP4, int NR, int TK>
+__global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const DecodeArgs a) {
+  using C = Cfg<FP4, NR, TK>;
+  constexpr int S = C::kStages;
+  constexpr int RS = C::kRawStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = sm + C::oA;
+  uint8_t* sRaw = sm + C::oRaw;
+  uint8_t* sQ = sm + C::oQ;
+  uint4* sTab = reinterpret_cast<uint4*>(sm + C::oTab);
+  uint64_t* sList = reinterpret_cast<uint64_t*>(sm + C::oList);
+  float* sRed = reinterpret_cast<float*>(sm + C::oRed);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::oBar);
+  uint64_t* empty = full + S;
+  uint64_t* raw_full = empty + S;
+  uint64_t* raw_empty = raw_full + RS;
+  uint64_t* acc_full = raw_empty + RS;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* q_full = acc_empty + kAccBufs;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* done_bar = q_empty + 2;
+  Misc* misc = reinterpret_cast<Misc*>(sm + C::oMisc);
+  volatile int* abort_flag = &misc->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kTmemCols = (kAccBufs * NR) < 32 ? 32 : kAccBufs * NR;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], FP4 ? 4 : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int s = 0; s < kAccBufs; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(done_bar, 1);
+    misc->abort = 0;
+    misc->last = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    if (!FP4 && lane == 0) prefetch_tensormap(&kmap);
+    partition(a, misc, lane);
+  }
+  if (warp == 1) {
+    tmem_alloc(&misc->tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if constexpr (FP4) build_fp4_table(sTab, threadIdx.x, C::kThreads);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc->tmem;
+  const long long total = misc->total;
+  Walker walker{misc->i0, misc->p0, misc->lo, misc->hi};
+
+  int req, b0, b1, nb;
+  long long preq;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    int seg = 0;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+      const int slot = seg & 1;
+      if (seg >= 2) ok = warp_wait(&q_empty[slot], ((seg >> 1) - 1) & 1, abort_flag);
+      if (!ok) break;
+      load_q_tile<NR>(a, req, sQ + slot * C::kQBytes, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[slot]);
+      const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
+      for (int bc = b0; bc < b1 && ok; bc += 32) {
+        const int mine = bc + lane;
+        const int pg = mine < b1 ? __ldg(trow + mine) : 0;
+        const int nblk = min(32, b1 - bc);
+        for (int k = 0; k < nblk; ++k) {
+          const int page = __shfl_sync(0xffffffffu, pg, k);
+          const bool good = page >= 0 && page < a.num_pages;
+          if constexpr (!FP4) {
+            const uint32_t st = it % S, rnd = it / S;
+            if (rnd > 0) ok = warp_wait(&empty[st], (rnd - 1) & 1, abort_flag);
+            if (!ok) break;
+            if (lane == 0) {
+              if (good) {
+                mbar_arrive_expect_tx(&full[st], kTileBytes);
+                tma_load_2d(sA + st * kTileBytes, &kmap, &full[st], 0, page * kBlock, pol);
+                tma_load_2d(sA + st * kTileBytes + kTileBytes / 2, &kmap, &full[st], 64,
+                            page * kBlock, pol);
+              } else {
+                atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
+                mbar_arrive(&full[st]);
+              }
+            }
+          } else {
+            const uint32_t st = it % RS, rnd = it / RS;
+            if (rnd > 0) ok = warp_wait(&raw_empty[st], (rnd - 1) & 1, abort_flag);
+            if (!ok) break;
+            if (lane == 0) {
+              if (good) {
+                uint8_t* dst = sRaw + st * kFp4RawBytes;
+                mbar_arrive_expect_tx(&raw_full[st], kFp4RawBytes);
+                bulk_load(dst, a.codes + static_cast<int64_t>(page) * kFp4CodeBytes,
+                          kFp4CodeBytes, &raw_full[st], pol);
+                bulk_load(dst + kFp4CodeBytes,
+                          a.scales + static_cast<int64_t>(page) * kFp4ScaleBytes,
+                          kFp4ScaleBytes, &raw_full[st], pol);
+              } else {
+                atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
+                mbar_arrive(&raw_full[st]);
+              }
+            }
+          }
+          __syncwarp();
+          ++it;
+        }
+      }
+      ++seg;
+    }
+    // Let every copy this warp started land before the CTA can exit.
+    if (lane == 0) {
+      constexpr int ring = FP4 ? RS : S;
+      uint64_t* ring_full = FP4 ? raw_full : full;
+      const uint32_t pending = it < static_cast<uint32_t>(ring) ? it : ring;
+      for (uint32_t k = 0; k < pending; ++k) {
+        const uint32_t idx = it - 1 - k;
+        int dummy = 0;
+        mbar_wait(&ring_full[idx % ring], (idx / ring) & 1, &dummy);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NR);
+      int seg = 0;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+        const int slot = seg & 1;
+        ok = mbar_wait(&q_full[slot], (seg >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(sQ + slot * C::kQBytes);
+        for (int b = b0; b < b1; ++b) {
+          const uint32_t st = it % S, rnd = it / S;
+          ok = mbar_wait(&full[st], rnd & 1, abort_flag);
+          if (!ok) break;
+          const uint32_t ab = it % kAccBufs, ar = it / kAccBufs;
+          if (ar > 0) ok = mbar_wait(&acc_empty[ab], (ar - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t aaddr = smem_u32(sA + st * kTileBytes);
+          const uint32_t d = tmem_base + ab * NR;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = sdesc_kmajor_sw128(aaddr + (k >> 2) * (kTileBytes / 2) + (k & 3) * 32);
+            const uint64_t bd = sdesc_kmajor_sw128(qaddr + (k >> 2) * (NR * 128) + (k & 3) * 32);
+            mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[st]);
+          mma_commit(&acc_full[ab]);
+          ++it;
+        }
+        if (!ok) break;
+        mma_commit(&q_empty[slot]);
+        ++seg;
+      }
+      // Wait until every MMA issued above has finished before TMEM is freed.
+      mma_commit(done_bar);
+      int dummy = 0;
+      mbar_wait(done_bar, 0, &dummy);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------- epilogue
+    const int ep = threadIdx.x - 64;
+    const int quad = warp & 3;
+    const int R = a.rows_per_req;
+    const int my_j = ep < R ? ep / a.heads : 0;
+    const int my_h = ep < R ? ep - my_j * a.heads : 0;
+    const bool select = a.mode == kModeSelect;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+      const int seq = req_len(a, req);
+      const int base = seq - a.query_len;  // position of query 0
+      const int pos = base + my_j;
+      const int c = pos >= 0 ? (pos >> 7) : -1;
+      const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
+      const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
+      int cnt = 0;
+      uint64_t thr = 0;
+      for (int b = b0; b < b1; ++b) {
+        const uint32_t ab = it % kAccBufs, ar = it / kAccBufs;
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&acc_full[ab], ar & 1, abort_flag);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        const int par = it & 1;
+        if (got) {
+          tc_fence_after();
+          float v[NR];
+#pragma unroll
+          for (int c0 = 0; c0 < NR; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * NR + c0, r);
+            tmem_ld_wait16(r);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[c0 + k] = __uint_as_float(r[k]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+          if (b * kBlock + kBlock - 1 > base) {
+            // Last block(s): token t is visible to row n = j*heads + h iff
+            // t - base <= j, i.e. n >= (t - base) * heads.
+            const int trel = b * kBlock + quad * 32 + lane - base;
+            const int lim = trel <= 0 ? 0 : min(trel, a.query_len) * a.heads;
+#pragma unroll
+            for (int n = 0; n < NR; ++n)
+              if (n < lim) v[n] = -INFINITY;
+          }
+          const float cm = transpose_max<NR>(v, lane);
+          float* red = sRed + par * 128 + quad * 32;
+          if constexpr (NR == 16) {
+            if ((lane & 1) == 0) red[lane >> 1] = cm;
+          } else {
+            red[lane] = cm;
+          }
+        }
+        if (!bar_and(1, 128, got)) {
+          ok = false;
+          break;
+        }
+        if (ep < R) {
+          const float* red = sRed + par * 128;
+          const float m = fmaxf(fmaxf(red[ep], red[32 + ep]), fmaxf(red[64 + ep], red[96 + ep]));
+          const int page = __ldg(trow + b);
+          const float s = (page >= 0 && page < a.num_pages) ? m * a.sm_scale : -INFINITY;
+          if (!select) {
+            a.score[my_h * a.s_head + row * a.s_row + b] = s;
+          } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
+            list_insert<NR, TK>(sList, ep, make_key(s, b), cnt, thr);
+          }
+        }
+        ++it;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------- segment end
+      if (!select) {
+        if (b1 == nb && a.fill_width > nb) {
+          const int w = a.fill_width - nb;
+          for (int idx = ep; idx < R * w; idx += 128) {
+            const int n = idx / w, b = nb + (idx - n * w);
+            const int j = n / a.heads, h = n - j * a.heads;
+            a.score[h * a.s_head + (static_cast<int64_t>(req) * a.query_len + j) * a.s_row + b] =
+                -INFINITY;
+          }
+        }
+        continue;
+      }
+      const int first = cta_of(preq, total, gridDim.x);
+      const int last = cta_of(preq + nb - 1, total, gridDim.x);
+      int32_t* out = a.ids + my_h * a.i_head + row * a.i_row;
+      if (first == last) {
+        if (ep < R) finalize_row<NR>(a, sList, ep, cnt, c, out);
+        continue;
+      }
+      const int slot_stride = NR * TK;
+      if (ep < R) {
+        uint64_t* dst = a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + ep * TK;
+        for (int k = 0; k < TK; ++k) dst[k] = k < cnt ? sList[k * NR + ep] : 0ull;
+      }
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (ep == 0) {
+        const int old = atomicAdd(a.counters + req, 1);
+        const int is_last = old == last - first;
+        if (is_last) a.counters[req] = 0;
+        misc->last = is_last;
+      }
+      named_barrier_sync(1, 128);
+      if (misc->last) {
+        __threadfence();
+        if (ep < R) {
+          cnt = 0;
+          thr = 0;
+          for (int s = first; s <= last; ++s) {
+            const uint64_t* src = a.partials + (static_cast<int64_t>(s) + req) * slot_stride + ep * TK;
+            for (int k = 0; k < TK; ++k) {
+              const uint64_t key = __ldcg(src + k);
+              if (key == 0ull || (cnt == TK && key <= thr)) break;
+              list_insert<NR, TK>(sList, ep, key, cnt, thr);
+            }
+          }
+          finalize_row<NR>(a, sList, ep, cnt, c, out);
+        }
+      }
+    }
+    if (ok) {
+      // Requests with no blocks at all appear in no share: spread them over CTAs.
+      for (int i = blockIdx.x; i < a.num_reqs; i += gridDim.x) {
+        if (req_blocks(a, i) != 0) continue;
+        if (!select) {
+          const int w = a.fill_width;
+          for (int idx = ep; idx < R * w; idx += 128) {
+            const int n = idx / w, b = idx - n * w;
+            const int j = n / a.heads, h = n - j * a.heads;
+            a.score[h * a.s_head + (static_cast<int64_t>(i) * a.query_len + j) * a.s_row + b] =
+                -INFINITY;
+          }
+        } else {
+          for (int idx = ep; idx < R * a.topk; idx += 128) {
+            const int n = idx / a.topk, k = idx - n * a.topk;
+            const int j = n / a.heads, h = n - j * a.heads;
+            a.ids[h * a.i_head + (static_cast<int64_t>(i) * a.query_len + j) * a.i_row + k] = -1;
+          }
+        }
+      }
+    }
+  } else if constexpr (FP4) {
+    // ---------------------------------------------------- NVFP4 dequantiser
+    const int dq = threadIdx.x - 192;  // 0..127
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+      for (int b = b0; b < b1; ++b) {
+        const uint32_t rs = it % RS, rr = it / RS;
+        const uint32_t st = it % S, sr = it / S;
+        bool got = true;
+        if (lane == 0) {
+          got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
+          if (got && sr > 0) got = mbar_wait(&empty[st], (sr - 1) & 1, abort_flag);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        const uint8_t* codes = sRaw + rs * kFp4RawBytes;
+        const uint8_t* scales = codes + kFp4CodeBytes;
+        uint8_t* tile = sA + st * kTileBytes;
+#pragma unroll 2
+        for (int kk = 0; kk < 8; ++kk) {
+          const int item = kk * 128 + dq;
+          const int tok = item >> 3, g = item & 7;
+          const uint2 cw = *reinterpret_cast<const uint2*>(codes + tok * 64 + g * 8);
+          const uint4 t = sTab[scales[tok * 8 + g]];
+          uint32_t o0[4], o1[4];
+          dequant8(cw.x, t, o0);
+          dequant8(cw.y, t, o1);
+          uint8_t* rowp = tile + (g >> 2) * (kTileBytes / 2) + (tok >> 3) * 1024 + (tok & 7) * 128;
+          const int c0 = (g & 3) * 2;
+          *reinterpret_cast<uint4*>(rowp + ((c0 ^ (tok & 7)) << 4)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+          *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (tok & 7)) << 4)) =
+              make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full[st]);
+          mbar_arrive(&raw_empty[rs]);
+        }
+        ++it;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && misc->abort) atomicOr(a.status, MM3IDX_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool FP4, int NR, int TK>
+cudaError_t launch_t(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
+  using C = Cfg<FP4, NR, TK>;
+  static bool configured = false;  // per process; attribute is per device-function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP4, NR, TK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  decode_kernel<FP4, NR, TK><<<grid, C::kThreads, C::kSmem, s>>>(kmap, a);
+  return cudaGetLastError();
+}
+
+template <bool FP4>
+cudaError_t dispatch(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
+  const int nr = decode_nr(a.rows_per_req), tk = decode_tk(a.topk);
+  if (nr == 16 && tk == 16) return launch_t<FP4, 16, 16>(kmap, a, grid, s);
+  if (nr == 16) return launch_t<FP4, 16, 32>(kmap, a, grid, s);
+  if (tk == 16) return launch_t<FP4, 32, 16>(kmap, a, grid, s);
+  return launch_t<FP4, 32, 32>(kmap, a, grid, s);
+}
+
+}  // namespace
+
+int decode_ctas_per_sm() { return 1; }
+
+cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
+  return dispatch<false>(kmap, a, grid, s);
+}
+
+cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s) {
+  CUtensorMap unused{};
+  return dispatch<true>(unused, a, grid, s);
+}
+
+}  // namespace mm3idx

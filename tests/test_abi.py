@@ -1,0 +1,163 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/mm3idx.h declares, and rejects bad arguments with
+the documented status codes before touching the device."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import sparse_attention_block_paged_gb300 as mm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mm3idx.h")
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mm3idx_\w+)\s*\(", src, re.M)))
+
+
+def header_constants():
+    src = open(HEADER).read()
+    return {k: int(v) for k, v in re.findall(r"#define\s+(MM3IDX_\w+)\s+\(?(-?\d+)\)?", src)}
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared()
+    assert len(names) >= 9
+    lib = ctypes.CDLL(mm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(mm.SYMBOLS) == set(names)
+
+
+def test_constants_match_binding():
+    c = header_constants()
+    assert c["MM3IDX_OK"] == mm.OK
+    assert c["MM3IDX_OP_DECODE"] == mm.OP_DECODE and c["MM3IDX_OP_PREFILL"] == mm.OP_PREFILL
+    assert c["MM3IDX_MAX_TOPK"] == mm.MAX_TOPK
+    assert c["MM3IDX_MAX_DECODE_ROWS"] == mm.MAX_DECODE_ROWS
+    assert (c["MM3IDX_DEV_BAD_PAGE"], c["MM3IDX_DEV_SEQ_TOO_LONG"], c["MM3IDX_DEV_SEQ_TOO_SHORT"],
+            c["MM3IDX_DEV_TIMEOUT"]) == (mm.DEV_BAD_PAGE, mm.DEV_SEQ_TOO_LONG,
+                                         mm.DEV_SEQ_TOO_SHORT, mm.DEV_TIMEOUT)
+    assert mm.Problem.sm_scale.offset > mm.Problem.max_seq_len.offset
+    for k, v in c.items():
+        if k.startswith("MM3IDX_ERR_"):
+            assert mm.status_string(v) not in ("", "unknown status")
+
+
+# Fake, 256-byte aligned addresses: validation must reject the arguments
+# before any pointer is dereferenced or any CUDA call is made.
+FAKE = 0x7f0000000000
+
+
+def problem(**kw):
+    p = mm.Problem()
+    vals = dict(idx_q=FAKE, q_token_stride=128, q_head_stride=128, heads=1, index_cache=FAKE,
+                index_scales=None, num_pages=16, block_table=FAKE, table_stride=8, table_width=8,
+                seq_lens=FAKE, num_reqs=2, query_len=1, max_seq_len=1000, sm_scale=0.088)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(p, k, v)
+    return p
+
+
+def decode_status(p, topk=4, init=1, local=1, out=FAKE, ohs=1024, ors=4, ws=FAKE, wsb=1 << 20):
+    return mm.lib.mm3idx_decode(ctypes.byref(p), topk, init, local, out, ohs, ors, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(query_len=0), -6),
+    (dict(max_seq_len=0, query_len=1), -6),
+    (dict(heads=0), -1),
+    (dict(sm_scale=0.0), -1),
+    (dict(sm_scale=-1.0), -1),
+    (dict(sm_scale=float("inf")), -1),
+    (dict(max_seq_len=0xFFFF * 128), -5),
+    (dict(idx_q=FAKE + 8), -2),
+    (dict(q_token_stride=100), -2),
+    (dict(index_cache=FAKE + 4), -3),
+    (dict(num_pages=0), -3),
+    (dict(index_scales=FAKE), -3),
+    (dict(table_width=7), -4),
+    (dict(table_stride=6, table_width=8), -4),
+])
+def test_decode_rejects_bad_problems(kw, code):
+    assert decode_status(problem(**kw)) == code
+
+
+@pytest.mark.parametrize("topk,init,local,code", [
+    (0, 0, 0, -7), (33, 1, 1, -7), (4, 3, 2, -7), (4, -1, 1, -7), (4, 1, -1, -7)])
+def test_decode_rejects_bad_topk(topk, init, local, code):
+    assert decode_status(problem(), topk=topk, init=init, local=local) == code
+
+
+def test_decode_rejects_wide_rows_and_bad_outputs():
+    assert decode_status(problem(heads=8, query_len=5, q_token_stride=1024)) == -10
+    assert decode_status(problem(), ors=3) == -8
+    assert decode_status(problem(), out=None) == -8
+    assert decode_status(problem(heads=2, q_token_stride=256), ohs=4, ors=4) == -8
+
+
+def test_nvfp4_requires_scales():
+    p = problem()
+    assert mm.lib.mm3idx_decode_nvfp4(ctypes.byref(p), 4, 1, 1, FAKE, 1024, 4, FAKE, 1 << 20,
+                                      None) == -3
+
+
+def test_empty_batch_is_ok_without_device():
+    assert decode_status(problem(num_reqs=0)) == 0
+    p = problem(num_reqs=0)
+    assert mm.lib.mm3idx_score(ctypes.byref(p), FAKE, 1000, 8, None) == 0
+    assert mm.lib.mm3idx_prefill(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 20, None) == 0
+
+
+def test_topk_validation():
+    f = mm.lib.mm3idx_topk
+    assert f(FAKE, 1000, 8, 1, FAKE, 2, 1, 0, 4, 1, 1, FAKE, 100, 4, None) == -6
+    assert f(FAKE, 1000, 8, 1, FAKE, 2, 1, 1000, 4, 3, 2, FAKE, 100, 4, None) == -7
+    assert f(FAKE, 1000, 7, 1, FAKE, 2, 1, 1000, 4, 1, 1, FAKE, 100, 4, None) == -8
+    assert f(FAKE, 1000, 8, 1, FAKE, 0, 1, 1000, 4, 1, 1, FAKE, 100, 4, None) == 0
+
+
+def test_workspace_query_validation():
+    n = ctypes.c_size_t(0)
+    assert mm.lib.mm3idx_workspace_bytes(3, 1, 1, 1, 128, 4, ctypes.byref(n)) == -1
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_DECODE, 1, 1, 1, 128, 40, ctypes.byref(n)) == -7
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 16, ctypes.byref(n)) == 0
+    assert n.value == 2 * 3 * 300 * 8 * 4      # [heads, rows, roundup(cdiv(1000,128), 4)] fp32
+
+
+def test_binding_layout_errors():
+    import torch
+    q = torch.zeros((2, 1, 64), dtype=torch.bfloat16)
+    cache = torch.zeros((4, 128, 128), dtype=torch.bfloat16)
+    t = torch.zeros((2, 8), dtype=torch.int32)
+    lens = torch.zeros((2,), dtype=torch.int32)
+    with pytest.raises(ValueError, match="BF16"):
+        mm.decode(q, cache, t, lens, query_len=1, max_seq_len=512, topk=4, init_blocks=1,
+                  local_blocks=1, sm_scale=0.1)
+    q = torch.zeros((2, 1, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="same GPU"):
+        mm.decode(q, cache, t, lens, query_len=1, max_seq_len=512, topk=4, init_blocks=1,
+                  local_blocks=1, sm_scale=0.1)
+    with pytest.raises(ValueError, match="int32"):
+        mm.decode(q, cache, t.long(), lens, query_len=1, max_seq_len=512, topk=4, init_blocks=1,
+                  local_blocks=1, sm_scale=0.1)
+
+
+def test_workload_generator_layout():
+    import workloads as W
+    wl = W.make("tiny")
+    assert wl.num_pages == 16 and wl.width == 6
+    used = {int(p) for i, s in enumerate(wl.seq_lens) for p in wl.block_table[i, :-(-int(s) // 128)]}
+    assert len(used) == 3 + 6 and max(used) < 16
+    assert wl.block_table[0, 3] == wl.num_pages + 7
+    # tail slots of request 0's last page are poisoned
+    last = wl.block_table[0, 2]
+    assert np.all(wl.cache[last, 300 % 128:] == W.POISON_BF16)
+    again = W.make("tiny")
+    assert np.array_equal(again.cache, wl.cache) and np.array_equal(again.q, wl.q)

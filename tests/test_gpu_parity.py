@@ -1,0 +1,269 @@
+"""GPU parity: every CUDA entry point against the CPU oracle on the same seeded
+inputs.  Small cases span several tiles, CTA splits and ragged tails and are
+compared element by element; the named full-size workloads are compared on
+sampled rows the oracle computes one by one."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import check_ids, check_scores, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mm(cuda_device):
+    import sparse_attention_block_paged_gb300 as m
+    return m
+
+
+def run_decode(mm, wl, **kw):
+    d = to_device(wl)
+    args = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+                init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale)
+    args.update(kw)
+    if wl.kv_format == "bf16":
+        ids = mm.decode(d["q"], d["cache"], d["table"], d["lens"], **args)
+    else:
+        ids = mm.decode_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"], **args)
+    return ids.cpu().numpy()
+
+
+def run_scores(mm, wl):
+    d = to_device(wl)
+    s = mm.score(d["q"], d["cache"], d["table"], d["lens"], query_len=wl.query_len,
+                 max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale)
+    return s.cpu().numpy()
+
+
+def run_prefill(mm, wl):
+    d = to_device(wl)
+    ids = mm.prefill(d["q"], d["cache"], d["table"], d["lens"], query_len=wl.query_len,
+                     max_seq_len=wl.max_seq_len, topk=wl.topk, init_blocks=wl.init_blocks,
+                     local_blocks=wl.local_blocks, sm_scale=wl.sm_scale)
+    return ids.cpu().numpy()
+
+
+# ------------------------------------------------------------ tiny workload
+
+def test_tiny_decode_exact(mm):
+    wl = W.make("tiny")
+    s, want = oracle.problem(wl)
+    got = run_decode(mm, wl)
+    np.testing.assert_array_equal(got, want)
+    check_scores(run_scores(mm, wl), s, "tiny scores")
+    assert mm.get_device_error() == 0
+
+
+# --------------------------------------------------- small decode sweeps
+
+DECODE_CASES = [
+    # seed, reqs, qlen, heads, topk, init, local, min_len, max_len
+    (1, 3, 1, 1, 4, 1, 1, 1, 2000),
+    (2, 5, 4, 1, 16, 1, 2, 100, 5000),
+    (3, 4, 4, 4, 16, 1, 2, 129, 3000),
+    (4, 2, 3, 2, 8, 2, 2, 3, 900),
+    (5, 6, 2, 8, 32, 2, 3, 128, 4096),
+    (6, 1, 8, 4, 16, 0, 0, 5000, 9000),
+    (7, 9, 1, 1, 16, 1, 2, 16000, 40000),
+    (8, 2, 4, 1, 5, 1, 2, 128, 130),
+    (9, 3, 16, 2, 12, 3, 1, 200, 2600),
+    (10, 40, 4, 1, 16, 1, 2, 1, 700),
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: f"seed{c[0]}")
+def test_decode_matches_oracle(mm, case):
+    seed, reqs, qlen, heads, topk, init, local, lo, hi = case
+    wl = W.random_case(seed, num_reqs=reqs, query_len=qlen, heads=heads, topk=topk,
+                       init_blocks=init, local_blocks=local, min_len=lo, max_len=hi)
+    s, want = oracle.problem(wl)
+    got = run_decode(mm, wl)
+    check_ids(got, want, s, wl, where=f"decode seed{seed}")
+    check_scores(run_scores(mm, wl), s, f"scores seed{seed}")
+    assert mm.get_device_error() == 0
+
+
+def test_decode_reused_workspace_and_graph_replay(mm):
+    import torch
+    wl = W.random_case(31, num_reqs=6, query_len=4, heads=2, topk=16, init_blocks=1,
+                       local_blocks=2, min_len=3000, max_len=30000)
+    s, want = oracle.problem(wl)
+    d = to_device(wl)
+    ws = mm.new_workspace(mm.OP_DECODE, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len, wl.topk)
+    out = torch.full((wl.heads, wl.rows, wl.topk), -7, dtype=torch.int32, device="cuda")
+    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+              init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale,
+              out=out, workspace=ws)
+    for _ in range(3):
+        out.fill_(-7)
+        mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+        check_ids(out.cpu().numpy(), want, s, wl, where="reuse")
+    # counters are back at zero after every launch
+    assert int(ws[: 4 * wl.num_reqs].view(torch.int32).abs().sum()) == 0
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)   # warm up on this stream
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+    for _ in range(3):
+        out.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        check_ids(out.cpu().numpy(), want, s, wl, where="graph")
+
+
+# ---------------------------------------------------------- prefill
+
+PREFILL_CASES = [
+    # seed, seq_lens, query_len, heads, topk, init, local
+    (1, [700], 700, 1, 4, 1, 1),
+    (2, [300, 1000], 300, 2, 8, 1, 2),          # prefix 700 on request 1: unaligned tiles
+    (3, [1280], 1280, 1, 16, 1, 2),
+    (4, [2000, 2000, 777], 257, 1, 16, 2, 2),   # ragged last tile, different prefixes
+    (5, [4096], 1500, 4, 32, 1, 3),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=lambda c: f"seed{c[0]}")
+def test_prefill_matches_oracle(mm, case):
+    seed, seq, qlen, heads, topk, init, local = case
+    wl = W.build(f"prefill-{seed}", seed=seed, seq_lens=seq, query_len=qlen, heads=heads,
+                 topk=topk, init_blocks=init, local_blocks=local, max_seq_len=max(seq) + 64)
+    s, want = oracle.problem(wl)
+    check_scores(run_scores(mm, wl), s, f"prefill scores seed{seed}")
+    check_ids(run_prefill(mm, wl), want, s, wl, where=f"prefill seed{seed}")
+    assert mm.get_device_error() == 0
+
+
+def test_topk_selector_bit_exact_on_same_scores(mm):
+    """Given the same fp32 scores, selection must agree bit for bit."""
+    import torch
+    rng = np.random.default_rng(5)
+    seq = rng.integers(1, 9000, size=37).astype(np.int32)
+    qlen, heads, topk = 3, 2, 16
+    seq = np.maximum(seq, qlen)
+    msl = int(seq.max())
+    W_ = -(-msl // 128)
+    sc = rng.standard_normal((heads, len(seq) * qlen, W_)).astype(np.float32)
+    sc[:, :, ::7] = sc[:, :, 3:4]          # plenty of exact ties
+    want = oracle.select_problem(sc.astype(np.float64), seq, qlen, topk, 1, 2)
+    got = mm.topk(torch.from_numpy(sc).cuda(), torch.from_numpy(seq).cuda(), query_len=qlen,
+                  max_seq_len=msl, topk=topk, init_blocks=1, local_blocks=2)
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------ NVFP4
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_nvfp4_decode_matches_oracle(mm, seed):
+    wl = W.random_case(seed, num_reqs=5, query_len=4, heads=1, topk=16, init_blocks=1,
+                       local_blocks=2, min_len=500, max_len=20000, kv_format="nvfp4")
+    s, want = oracle.problem(wl)
+    got = run_decode(mm, wl)
+    check_ids(got, want, s, wl, where=f"nvfp4 seed{seed}")
+    assert mm.get_device_error() == 0
+
+
+def test_nvfp4_equals_bf16_path_on_dequantised_cache(mm):
+    """The NVFP4 kernel's dequantised keys are exact bf16 values, so scoring the
+    oracle-dequantised cache on the bf16 path must give the same ids."""
+    wl = W.random_case(9, num_reqs=4, query_len=4, heads=1, topk=16, init_blocks=1,
+                       local_blocks=2, min_len=2000, max_len=9000, kv_format="nvfp4")
+    got4 = run_decode(mm, wl)
+    import copy
+    bf = copy.copy(wl)
+    bf.kv_format = "bf16"
+    bf.cache = oracle.nvfp4_dequant_bf16(wl.codes, wl.scales)
+    got16 = run_decode(mm, bf)
+    np.testing.assert_array_equal(got4, got16)
+
+
+def test_nvfp4_extreme_scales(mm):
+    """Scales near the subnormal floor and near saturation (6 * 448)."""
+    wl = W.random_case(12, num_reqs=3, query_len=2, heads=1, topk=8, init_blocks=1,
+                       local_blocks=1, min_len=300, max_len=3000, kv_format="nvfp4")
+    rng = np.random.default_rng(3)
+    choices = np.array([0x01, 0x02, 0x07, 0x08, 0x09, 0x7E, 0x7D, 0x77, 0x38, 0xB8], dtype=np.uint8)
+    wl.scales[:] = rng.choice(choices, size=wl.scales.shape)
+    s, want = oracle.problem(wl)
+    got = run_decode(mm, wl)
+    check_ids(got, want, s, wl, where="nvfp4 extremes")
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_padding_and_no_forced_blocks(mm):
+    wl = W.random_case(40, num_reqs=4, query_len=2, heads=2, topk=32, init_blocks=0,
+                       local_blocks=0, min_len=2, max_len=3000)
+    s, want = oracle.problem(wl)
+    check_ids(run_decode(mm, wl), want, s, wl, where="pad")
+
+
+def test_empty_batch_is_noop(mm):
+    import torch
+    q = torch.zeros((0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros((1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    table = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    lens = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    ids = mm.decode(q, cache, table, lens, query_len=1, max_seq_len=512, topk=4, init_blocks=1,
+                    local_blocks=1, sm_scale=0.1)
+    assert ids.shape == (1, 0, 4)
+
+
+def test_device_status_for_bad_lengths_and_pages(mm):
+    wl = W.random_case(41, num_reqs=3, query_len=2, heads=1, topk=4, init_blocks=1,
+                       local_blocks=1, min_len=300, max_len=900)
+    wl.seq_lens[1] = 1                       # shorter than query_len
+    s, want = oracle.problem(wl)
+    got = run_decode(mm, wl)
+    assert mm.get_device_error() & mm.DEV_SEQ_TOO_SHORT
+    check_ids(got, want, s, wl, where="short")
+    bad = W.random_case(42, num_reqs=2, query_len=1, heads=1, topk=4, init_blocks=1,
+                        local_blocks=1, min_len=600, max_len=900)
+    bad.block_table[0, 1] = bad.num_pages + 3   # out of range page
+    run_decode(mm, bad)
+    assert mm.get_device_error() & mm.DEV_BAD_PAGE
+    assert mm.get_device_error() == 0           # read-and-clear
+
+
+# ------------------------------------------------- full-size named workloads
+
+def _sample_rows(wl, reqs):
+    return [i * wl.query_len + j for i in reqs for j in range(wl.query_len)]
+
+
+@pytest.mark.parametrize("key", ["spec_decode", "high_batch", "nvfp4_decode"])
+def test_full_size_decode_sampled(mm, key):
+    wl = W.make(key)
+    got = run_decode(mm, wl)
+    assert mm.get_device_error() == 0
+    rng = np.random.default_rng(0)
+    order = np.argsort(wl.seq_lens)
+    reqs = sorted(set([int(order[0]), int(order[-1])] +
+                      [int(x) for x in rng.choice(wl.num_reqs, size=4, replace=False)]))
+    sub = oracle.subset(wl, reqs)
+    s, want = oracle.problem(sub)
+    rows = _sample_rows(wl, reqs)
+    check_ids(got[:, rows], want, s, sub, where=key)
+
+
+def test_full_size_prefill_sampled(mm):
+    wl = W.make("prefill")
+    got = run_prefill(mm, wl)
+    assert mm.get_device_error() == 0
+    rows = sorted(set([0, 1, 127, 128, 129, 255, 256, 4095, 4096, 16384, 30001,
+                       wl.query_len - 129, wl.query_len - 128, wl.query_len - 1] +
+                      list(range(5, wl.query_len, 997))))
+    for r in rows:
+        s, want = oracle.row(wl, r, 0)
+        c = len(s) - 1
+        from helpers import check_ids_row
+        check_ids_row(got[0, r], want, s, c, wl.topk, wl.init_blocks, wl.local_blocks,
+                      where=f"prefill row {r}")

@@ -29,8 +29,10 @@ Recipes for the five named workloads are in ``WORKLOADS``; every draw comes from
 
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -42,10 +44,11 @@ POISON_SCALE = 0x7E           # e4m3 448.0
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even); return uint16 bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    """Round finite float32 values to bf16 (nearest, ties to even); return
+    uint16 bits.  (No finite float32 overflows the 32-bit sum below.)"""
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    u += np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1))
+    return (u >> 16).astype(np.uint16)
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -122,13 +125,29 @@ def _poison_tails_nvfp4(codes, scales, table, seq_lens):
             scales[p, s % BLOCK:, :] = POISON_SCALE
 
 
-def _normal_bf16(rng, shape, chunk=1 << 24):
-    """Standard normals rounded to bf16, drawn in chunks to bound host memory."""
+def _parallel_fill(seed_key, n_items, chunk, fn):
+    """Run fn(rng, lo, hi) over [0, n_items) in chunks on a thread pool.  Chunk
+    k always draws from child k of SeedSequence(seed_key), so the result does
+    not depend on thread scheduling."""
+    nchunks = max(1, (n_items + chunk - 1) // chunk)
+    kids = np.random.SeedSequence(seed_key).spawn(nchunks)
+
+    def work(k):
+        fn(np.random.default_rng(kids[k]), k * chunk, min(n_items, (k + 1) * chunk))
+
+    with cf.ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 4)) as ex:
+        list(ex.map(work, range(nchunks)))
+
+
+def _normal_bf16(seed_key, shape, chunk=1 << 22):
+    """Standard normals rounded to bf16."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        out[s:e] = bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+
+    def fill(rng, lo, hi):
+        out[lo:hi] = bf16_bits(rng.standard_normal(hi - lo, dtype=np.float32))
+
+    _parallel_fill(seed_key, n, chunk, fill)
     return out.reshape(shape)
 
 
@@ -150,21 +169,26 @@ def _e4m3_decode_table() -> np.ndarray:
         torch.float8_e4m3fn).to(torch.float32).numpy()
 
 
+_E4M3_TABLE = _e4m3_decode_table()
+_E2M1_MID = (_E2M1[1:] + _E2M1[:-1]) / 2
+
+
 def nvfp4_encode(x: np.ndarray):
     """Encode float32 keys ``[..., 128]`` as (codes ``[..., 64]``, scales ``[..., 8]``).
 
-    Per 16-element group: scale byte = e4m3(amax/6); code = nearest e2m1
-    magnitude of ``|x|/scale`` (clamped to 6) with the sign in bit 3.
+    Per 16-element group: scale byte = e4m3(amax/6); code = the e2m1
+    magnitude nearest to ``|x|/scale`` (clamped to 6; a value exactly half
+    way goes to the larger magnitude) with the sign in bit 3.
     """
     shape = x.shape
     g = x.reshape(-1, 16)
-    amax = np.abs(g).max(axis=1)
+    ag = np.abs(g)
+    amax = ag.max(axis=1)
     sb = _e4m3_scale_bytes(amax / 6.0)
-    sv = _e4m3_decode_table()[sb]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        r = np.where(sv[:, None] > 0, np.abs(g) / sv[:, None], 0.0)
-    mag = np.abs(r[..., None] - _E2M1).argmin(axis=-1).astype(np.uint8)
-    code = mag | np.where(g < 0, 8, 0).astype(np.uint8)
+    sv = _E4M3_TABLE[sb]
+    inv = np.where(sv > 0, 1.0 / np.where(sv > 0, sv, 1.0), 0.0).astype(np.float32)
+    mag = np.searchsorted(_E2M1_MID, ag * inv[:, None], side="right").astype(np.uint8)
+    code = mag | ((g < 0).astype(np.uint8) << 3)
     code = code.reshape(-1, 8, 2)
     packed = (code[..., 0] | (code[..., 1] << 4)).astype(np.uint8)
     codes = packed.reshape(*shape[:-1], 64)
@@ -176,8 +200,9 @@ def build(name, *, seed, seq_lens, query_len, heads, topk, init_blocks,
           local_blocks, max_seq_len, sm_scale=1.0 / math.sqrt(128.0),
           kv_format="bf16", block_offset_std=0.0, pool_pages=None,
           poison=True):
-    """Draw a workload with the given shape.  Order of draws: block table
-    permutation, keys (and block offsets), queries."""
+    """Draw a workload with the given shape.  default_rng(seed) draws the
+    block-table permutation and the block offsets; keys and queries come from
+    the child streams of SeedSequence([seed, 1]) and ([seed, 2])."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     table, pages = _deal_pages(rng, seq_lens, max_seq_len, pool_pages)
@@ -190,34 +215,36 @@ def build(name, *, seed, seq_lens, query_len, heads, topk, init_blocks,
         if block_offset_std:
             # One scalar offset per page; a page is one (request, logical
             # block), so this is the per-block offset of the recipe.
-            cache = np.empty((pages, BLOCK, D), dtype=np.uint16)
             offs = rng.normal(0.0, block_offset_std, size=pages).astype(np.float32)
-            step = 512
-            for p0 in range(0, pages, step):
-                p1 = min(pages, p0 + step)
-                k = rng.standard_normal((p1 - p0, BLOCK, D), dtype=np.float32)
-                k += offs[p0:p1, None, None]
-                cache[p0:p1] = bf16_bits(k)
+            cache = np.empty((pages, BLOCK, D), dtype=np.uint16)
+
+            def fill(r, lo, hi):
+                k = r.standard_normal((hi - lo, BLOCK, D), dtype=np.float32)
+                k += offs[lo:hi, None, None]
+                cache[lo:hi] = bf16_bits(k)
+
+            _parallel_fill([seed, 1], pages, 256, fill)
         else:
-            cache = _normal_bf16(rng, (pages, BLOCK, D))
+            cache = _normal_bf16([seed, 1], (pages, BLOCK, D))
         if poison:
             _poison_tails_bf16(cache, table, seq_lens)
         wl.cache = cache
     elif kv_format == "nvfp4":
         codes = np.empty((pages, BLOCK, D // 2), dtype=np.uint8)
         scales = np.empty((pages, BLOCK, D // 16), dtype=np.uint8)
-        step = 256
-        for p0 in range(0, pages, step):
-            p1 = min(pages, p0 + step)
-            k = rng.standard_normal((p1 - p0, BLOCK, D), dtype=np.float32)
-            codes[p0:p1], scales[p0:p1] = nvfp4_encode(k)
+
+        def fill(r, lo, hi):
+            k = r.standard_normal((hi - lo, BLOCK, D), dtype=np.float32)
+            codes[lo:hi], scales[lo:hi] = nvfp4_encode(k)
+
+        _parallel_fill([seed, 1], pages, 256, fill)
         if poison:
             _poison_tails_nvfp4(codes, scales, table, seq_lens)
         wl.codes, wl.scales = codes, scales
     else:
         raise ValueError(kv_format)
     tokens = len(seq_lens) * query_len
-    wl.q = _normal_bf16(rng, (tokens, heads, D))
+    wl.q = _normal_bf16([seed, 2], (tokens, heads, D))
     return wl
 
 
