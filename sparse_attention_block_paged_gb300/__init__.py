@@ -90,7 +90,7 @@ def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(
             f"{_LIB_PATH} is missing: build it first "
-            "(python -m sparse_attention_block_paged_gb300.build); there is no fallback")
+            "(python sparse_attention_block_paged_gb300/build.py); there is no fallback")
     lib = ctypes.CDLL(_LIB_PATH)
     for name, (res, args) in SYMBOLS.items():
         fn = getattr(lib, name)

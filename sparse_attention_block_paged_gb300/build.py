@@ -4,7 +4,7 @@ Each translation unit compiles in parallel; the shared library links the CUDA
 runtime statically and resolves the driver's tensor-map encoder at run time,
 so loading it needs no GPU and no libcuda.
 
-    python -m sparse_attention_block_paged_gb300.build
+    python sparse_attention_block_paged_gb300/build.py [-v]
 """
 
 from __future__ import annotations

@@ -118,6 +118,12 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int grid) {
   return static_cast<int>(((x + 1) * grid - 1) / total);
 }
 
+// Whether CTA c's share [total*c/grid, total*(c+1)/grid) is non-empty.  With
+// fewer blocks than CTAs some shares are empty; those CTAs see no segment.
+__device__ __forceinline__ bool share_nonempty(int c, long long total, int grid) {
+  return total * (c + 1) / grid > total * c / grid;
+}
+
 // Warp 0: total block count, this CTA's share and the first request in it.
 __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
   long long total = 0;
@@ -597,7 +603,9 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
       const int first = cta_of(preq, total, gridDim.x);
       const int last = cta_of(preq + nb - 1, total, gridDim.x);
       int32_t* out = a.ids + my_h * a.i_head + row * a.i_row;
-      if (first == last) {
+      int nseg = 0;
+      for (int cc = first; cc <= last; ++cc) nseg += share_nonempty(cc, total, gridDim.x);
+      if (nseg == 1) {
         if (ep < R) finalize_row<NR>(a, sList, ep, cnt, c, out);
         continue;
       }
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
       named_barrier_sync(1, 128);
       if (ep == 0) {
         const int old = atomicAdd(a.counters + req, 1);
-        const int is_last = old == last - first;
+        const int is_last = old == nseg - 1;
         if (is_last) a.counters[req] = 0;
         misc->last = is_last;
       }
@@ -621,6 +629,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
           cnt = 0;
           thr = 0;
           for (int s = first; s <= last; ++s) {
+            if (!share_nonempty(s, total, gridDim.x)) continue;
             const uint64_t* src = a.partials + (static_cast<int64_t>(s) + req) * slot_stride + ep * TK;
             for (int k = 0; k < TK; ++k) {
               const uint64_t key = __ldcg(src + k);
