@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark of the lightning-indexer hot path on one GB300 (or N replicas).
+
+One step = one fused decode (block scores + top-k) over the spec-decode batch:
+64 requests x 4 query tokens (positions seq_len-4..seq_len-1), seq_lens uniform
+in [4096, 32768], 1 index head, topk 16, init 1, local 2, pages shuffled in a
+pool 1.25x the need.  Inputs are resident in HBM; the L2 is flushed (a read of
+a 2x-L2 buffer) before every timed step and the flush is not timed.
+
+Printed: one JSON line with rows/s (value), the roofline of the decode kernel
+against the measured HBM copy bandwidth, the CPU oracle timed on host cores,
+an end-to-end figure through the public API with host buffers, clocks sampled
+during the run, and (under "extra") the other named workloads: high-batch
+decode, NVFP4 decode and causal prefill (tensor-core scorer + selector).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica of the batch (weak scaling);
+value is the rows of all ranks over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode score+top-k rows/s & HBM GB/s; prefill index TFLOP/s vs peak"
+HEADLINE = "spec_decode"
+BLOCK = 128
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="bound on the CPU oracle sample")
+    ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill"],
+                    help="run just this extra workload and print its result (for profiling)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+def kernel_sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "sparse_attention_block_paged_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_name, sources):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != kernel_sources_sha(sources):
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of clocks and throttle reasons while the GPU works."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.flush()
+        rows = [l.strip().split(", ") for l in open(self.f.name) if l.strip()]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows if len(r) >= 9 for k in range(4)
+                          if r[5 + k].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(sm)}
+
+
+def device_inputs(wl, torch, dev):
+    q = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    d = dict(q=q, table=torch.from_numpy(wl.block_table).to(dev),
+             lens=torch.from_numpy(wl.seq_lens).to(dev))
+    if wl.kv_format == "bf16":
+        d["cache"] = torch.from_numpy(wl.cache.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        d["codes"] = torch.from_numpy(wl.codes).to(dev)
+        d["scales"] = torch.from_numpy(wl.scales).to(dev)
+    return d
+
+
+def decode_bytes(wl):
+    """Algorithmic bytes of one fused decode: the visible keys of every request
+    (tokens 0..seq_len-1), the queries, the block-table entries and lengths
+    read, and the ids written."""
+    per_tok = 256 if wl.kv_format == "bf16" else 72
+    nb = (wl.seq_lens.astype(np.int64) + BLOCK - 1) // BLOCK
+    return int(wl.seq_lens.astype(np.int64).sum() * per_tok + wl.q.nbytes + nb.sum() * 4
+               + wl.seq_lens.nbytes + wl.heads * wl.rows * wl.topk * 4)
+
+
+def prefill_flops(wl):
+    """2 * 128 * (visible keys of every query row), token-level causal."""
+    pos = []
+    for s in wl.seq_lens.astype(np.int64):
+        start = s - wl.query_len
+        pos.append((s * (s + 1) - start * (start + 1)) // 2)   # sum of (p+1) over rows
+    return 2.0 * 128 * float(sum(pos)) * wl.heads
+
+
+def timed_steps(torch, fn, steps, warmup, flush, stream, min_warm_s=0.0):
+    """Per-step CUDA-event times (ms) of fn() on `stream`, L2 flushed (untimed)
+    before each step."""
+    for _ in range(warmup):
+        fn()
+    if min_warm_s > 0:
+        t0 = time.time()
+        while time.time() - t0 < min_warm_s:
+            flush()
+            fn()
+        torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+# ---------------------------------------------------------------- our arm
+
+def bench_decode(mm, torch, wl, steps, warmup, flush, stream, pk, min_warm_s=0.0):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = device_inputs(wl, torch, dev)
+    out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
+    ws = mm.new_workspace(mm.OP_DECODE, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len,
+                          wl.topk, dev)
+    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+              init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale,
+              out=out, workspace=ws, stream=stream)
+    if wl.kv_format == "bf16":
+        fn = lambda: mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)  # noqa: E731
+        sources = ["decode.cu", "ptx.cuh", "internal.h"]
+    else:
+        fn = lambda: mm.decode_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"], **kw)  # noqa: E731
+        sources = ["decode.cu", "ptx.cuh", "internal.h"]
+    with torch.cuda.stream(stream):
+        ms = timed_steps(torch, fn, steps, warmup, flush, stream, min_warm_s)
+    assert mm.get_device_error(stream) == 0, "device status word set"
+    t = statistics.mean(ms) * 1e-3
+    nbytes = decode_bytes(wl)
+    res = dict(value=wl.rows / t, unit="rows/s", ms_per_step=t * 1e3,
+               ms_median=statistics.median(ms), steps=steps,
+               roofline=dict(bound="hbm", achieved=nbytes / t / 1e9, peak=pk["hbm_gbs"],
+                             unit="GB/s", frac=nbytes / t / 1e9 / pk["hbm_gbs"],
+                             traffic=None, algorithmic_bytes=nbytes,
+                             peak_source=pk["source"] + " burst copy"))
+    return res, d, out, ws, kw, sources
+
+
+def bench_e2e(mm, torch, wl, d, out, ws, kw, steps, warmup, flush, stream):
+    """Same decode through the public API with host buffers: H2D of the step's
+    queries, block table and lengths from pinned memory, the call, D2H of ids."""
+    q_h = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_h = torch.from_numpy(wl.block_table).pin_memory()
+    l_h = torch.from_numpy(wl.seq_lens).pin_memory()
+    o_h = torch.empty(out.shape, dtype=torch.int32).pin_memory()
+
+    def fn():
+        d["q"].copy_(q_h, non_blocking=True)
+        d["table"].copy_(t_h, non_blocking=True)
+        d["lens"].copy_(l_h, non_blocking=True)
+        mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+        o_h.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        ms = timed_steps(torch, fn, steps, warmup, flush, stream)
+    t = statistics.mean(ms) * 1e-3
+    return dict(value=wl.rows / t, unit="rows/s",
+                h2d_bytes_per_step=int(q_h.nbytes + t_h.nbytes + l_h.nbytes),
+                d2h_bytes_per_step=int(o_h.nbytes))
+
+
+def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = device_inputs(wl, torch, dev)
+    out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
+    n = mm.workspace_bytes(mm.OP_PREFILL, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len,
+                           wl.topk)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+              init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale,
+              out=out, workspace=ws, stream=stream)
+    fn = lambda: mm.prefill(d["q"], d["cache"], d["table"], d["lens"], **kw)  # noqa: E731
+    with torch.cuda.stream(stream):
+        ms_all = timed_steps(torch, fn, steps, warmup, flush, stream)
+        w = (-(-wl.max_seq_len // BLOCK) + 3) // 4 * 4
+        sc = ws.view(torch.float32)[: wl.heads * wl.rows * w].view(wl.heads, wl.rows, w)
+        sel = lambda: mm.topk(sc, d["lens"], query_len=wl.query_len, max_seq_len=wl.max_seq_len,  # noqa: E731
+                              topk=wl.topk, init_blocks=wl.init_blocks,
+                              local_blocks=wl.local_blocks, out=out, stream=stream)
+        ms_sel = timed_steps(torch, sel, steps, warmup, flush, stream)
+    assert mm.get_device_error(stream) == 0, "device status word set"
+    t_all = statistics.mean(ms_all) * 1e-3
+    t_sel = statistics.mean(ms_sel) * 1e-3
+    t_score = max(t_all - t_sel, 1e-9)
+    fl = prefill_flops(wl)
+    return dict(value=fl / t_score / 1e12, unit="TFLOP/s (scorer)",
+                rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3, scorer_ms=t_score * 1e3,
+                selector_ms=t_sel * 1e3,
+                roofline=dict(bound="tensor", achieved=fl / t_score / 1e12, peak=pk["bf16_tflops"],
+                              unit="TFLOP/s", frac=fl / t_score / 1e12 / pk["bf16_tflops"],
+                              traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
+                                                       ["prefill.cu", "ptx.cuh", "internal.h"]),
+                              algorithmic_flops=fl,
+                              peak_source=pk["source"] + " cuBLAS bf16 burst"))
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle as it stands, single-threaded, on whole batches of the
+    workload until `seconds` of CPU time are spent (at least one request)."""
+    import oracle
+    rows = 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        sub = oracle.subset(wl, [i % wl.num_reqs])
+        oracle.problem(sub, want_scores=False)
+        rows += sub.rows
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return dict(value=rows / el, unit="rows/s", cores=1, kind="oracle",
+                sample=f"{i} requests ({rows} rows) of the {wl.name} workload, "
+                       f"request by request, {el:.1f} s on one host core")
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import sparse_attention_block_paged_gb300 as mm
+    import workloads as W
+
+    pk = peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream()
+    flush_buf = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        torch.amax(flush_buf, dim=0, out=flush_out)
+
+    if args.only:
+        w = W.make(args.only)
+        if args.only == "prefill":
+            r = bench_prefill(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
+        else:
+            r = bench_decode(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)[0]
+        r["workload"] = w.name
+        print(json.dumps(r), flush=True)
+        return
+
+    wl = W.make(HEADLINE)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    res, d, out, ws, kw, sources = bench_decode(mm, torch, wl, args.steps, max(args.warmup, 3),
+                                                flush, stream, pk, min_warm_s=1.5)
+    res["roofline"]["traffic"] = profiled_traffic("decode_spec_decode.md", sources)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t = res["ms_per_step"]
+    if world > 1:
+        tt = torch.tensor([t], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t = float(tt.item())
+    e2e = bench_e2e(mm, torch, wl, d, out, ws, kw, args.steps, max(args.warmup, 3), flush, stream)
+    extra = {}
+    if not args.no_extra and rank == 0:
+        for key in ("high_batch", "nvfp4_decode"):
+            w2 = W.make(key)
+            r2 = bench_decode(mm, torch, w2, max(20, args.steps // 4), 3, flush, stream, pk)[0]
+            r2["roofline"]["traffic"] = profiled_traffic(f"decode_{key}.md", sources)
+            r2["workload"] = w2.name
+            extra[key] = r2
+            del w2
+        w4 = W.make("prefill")
+        r4 = bench_prefill(mm, torch, w4, max(10, args.steps // 10), 3, flush, stream, pk)
+        r4["workload"] = w4.name
+        extra["prefill"] = r4
+    clk = clocks.stop()
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC,
+        "value": world * wl.rows / (t * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": t,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy draws, bf16 q/k ~ N(0,1))",
+        "config": {"workload": "spec-decode batch: 64 requests x query_len 4, seq_lens U[4096,32768], "
+                               "1 index head, topk 16, init 1, local 2, pool 1.25x need (shuffled)",
+                   "rows_per_step": wl.rows, "key_bytes_per_step": wl.key_bytes(),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before each timed step (read of a 2x-L2 buffer), flush not timed"},
+        "roofline": res["roofline"],
+        "cpu_baseline": cpu_baseline(wl, args.cpu_seconds),
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as it stands on the headline workload: each step is a
+    bounded sample (4 requests = 16 rows) of the spec-decode batch."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+    wl = W.make(HEADLINE)
+    per_step = 4
+
+    def step(k):
+        reqs = [(k * per_step + j) % wl.num_reqs for j in range(per_step)]
+        oracle.problem(oracle.subset(wl, reqs), want_scores=False)
+
+    for k in range(max(args.warmup, 3)):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    el = time.perf_counter() - t0
+    rows = args.steps * per_step * wl.query_len
+    value = rows / el
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy draws)",
+        "config": {"workload": "spec-decode batch: 64 requests x query_len 4, seq_lens U[4096,32768], "
+                               "1 index head, topk 16, init 1, local 2",
+                   "sample_per_step": f"{per_step} requests ({per_step * wl.query_len} rows)"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} requests per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
