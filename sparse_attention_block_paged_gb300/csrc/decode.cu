@@ -13,24 +13,25 @@
 //     flattened request-major.  Each CTA takes one contiguous, equal share, so
 //     ragged lengths cost no imbalance.  Shares are computed on the device
 //     from seq_lens (no host round trip; CUDA-graph safe).
-//   * warp 0   : producer.  Walks the block table, TMA-loads each 32 KB page
+//   * warp 2   : producer.  Walks the block table and TMA-loads each 32 KB page
 //                (two 64-column boxes, 128-byte swizzle) into a ring of stages;
 //                writes each request's query rows into a swizzled Q tile.
 //                NVFP4: bulk-copies the 9 KB code+scale page into a raw ring.
-//   * warps 6-9: (NVFP4 only) dequantise raw pages into bf16 tiles in the same
+//   * warps 5-8: (NVFP4 only) dequantise raw pages into bf16 tiles in the same
 //                swizzled layout, via a per-scale-byte magnitude table.
-//   * warp 1   : one thread issues tcgen05.mma, M = 128 tokens of the page,
-//                N = 16 or 32 query rows, K = 128; fp32 accumulators in TMEM,
-//                four buffers.
-//   * warps 2-5: epilogue.  tcgen05.ld of the 128 x N accumulator, causal mask
-//                on the last block only, max over the 128 tokens by a
-//                transposing warp-shuffle reduction plus a 4-way shared-memory
-//                combine, scale, then per row either a store of the score or
-//                an insertion into a sorted top-k candidate list in shared
-//                memory.  A request split across CTAs merges its candidate
-//                lists in the last CTA to finish it (atomic arrival count),
-//                which re-pins the forced blocks, writes the ids and resets
-//                the counter.
+//   * warp 1   : one thread issues tcgen05.mma with the query rows as A
+//                (M = 64 or 128, rows past heads*query_len unused) and the page
+//                as B (N = 128 tokens), K = 128; fp32 accumulators in TMEM,
+//                four 128-column buffers.  Query row n lands in TMEM lane n.
+//   * warps 0,4: epilogue, alternate blocks.  Lane n loads its row's 128
+//                token scores with tcgen05.ld, masks only the causal tail,
+//                takes the max with 3-input max, scales, and either stores the
+//                score or inserts the candidate key into a sorted per-warp,
+//                per-row list in shared memory.  At a request boundary the two
+//                lists merge; a request split across CTAs merges its lists in
+//                the last CTA to finish it (atomic arrival count), which
+//                re-pins the forced blocks, writes the ids and resets the
+//                counter.
 //
 // Every wait is bounded (ptx.cuh).  A wait that gives up raises an abort flag
 // shared by the CTA's roles and the MM3IDX_DEV_TIMEOUT status bit.
@@ -45,24 +46,28 @@ namespace mm3idx {
 namespace {
 
 constexpr int kAccBufs = 4;
+constexpr int kAccCols = 128;                        // one page of tokens
+constexpr uint32_t kTmemCols = kAccBufs * kAccCols;  // 512: the whole TMEM
 constexpr int kTileBytes = kBlock * kD * 2;          // 32 KB bf16 page
 constexpr int kFp4CodeBytes = kBlock * kD / 2;       // 8 KB
 constexpr int kFp4ScaleBytes = kBlock * kD / 16;     // 1 KB
 constexpr int kFp4RawBytes = kFp4CodeBytes + kFp4ScaleBytes;
+constexpr int kLanes = 32;                           // rows per list slot
+constexpr int kEpiA = 0, kMmaWarp = 1, kProdWarp = 2, kEpiB = 4, kDeqWarp0 = 5;
 
-template <bool FP4, int NR, int TK>
+template <bool FP4, int MQ, int TK>
 struct Cfg {
-  static constexpr int kStages = FP4 ? 3 : 5;
-  static constexpr int kRawStages = FP4 ? 8 : 0;
-  static constexpr int kThreads = FP4 ? 320 : 192;
-  static constexpr int kQBytes = NR * kD * 2;
+  static constexpr int kStages = FP4 ? (MQ == 64 ? 3 : 2) : (MQ == 64 ? 5 : 4);
+  static constexpr int kRawStages = FP4 ? (MQ == 64 ? 8 : 6) : 0;
+  static constexpr int kThreads = FP4 ? 288 : 160;
+  static constexpr int kQBytes = MQ * kD * 2;
   static constexpr int oA = 0;
   static constexpr int oRaw = oA + kStages * kTileBytes;
   static constexpr int oQ = oRaw + kRawStages * kFp4RawBytes;
   static constexpr int oTab = oQ + 2 * kQBytes;
   static constexpr int oList = oTab + (FP4 ? 256 * 16 : 0);
-  static constexpr int oRed = oList + TK * NR * 8;
-  static constexpr int oBar = oRed + 2 * 4 * 32 * 4;
+  static constexpr int oCnt = oList + 2 * TK * kLanes * 8;
+  static constexpr int oBar = oCnt + kLanes * 4;
   static constexpr int kBars = 2 * kStages + 2 * kRawStages + 2 * kAccBufs + 4 + 1;
   static constexpr int oMisc = oBar + kBars * 8;
   static constexpr int kSmem = oMisc + 64 + 1024;
@@ -75,7 +80,6 @@ struct Misc {
   int i0;
   uint32_t tmem;
   int abort;
-  int last;
 };
 
 __device__ __forceinline__ int req_len(const DecodeArgs& a, int i) {
@@ -124,7 +128,7 @@ __device__ __forceinline__ bool share_nonempty(int c, long long total, int grid)
   return total * (c + 1) / grid > total * c / grid;
 }
 
-// Warp 0: total block count, this CTA's share and the first request in it.
+// One warp: total block count, this CTA's share and the first request in it.
 __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
   long long total = 0;
   for (int b = 0; b < a.num_reqs; b += 32) {
@@ -175,47 +179,27 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
 }
 
 // Writes request `req`'s query rows (row n = query j, head h with
-// n = j*heads + h) into a K-major 128-byte-swizzled tile of NR rows; rows past
-// heads*query_len are zero.
-template <int NR>
+// n = j*heads + h) into a K-major 128-byte-swizzled tile of MQ rows.  Rows
+// past heads*query_len are left as they are: their accumulator lanes are
+// never read.
+template <int MQ>
 __device__ void load_q_tile(const DecodeArgs& a, int req, uint8_t* dst, int lane) {
   const int R = a.rows_per_req;
-  for (int item = lane; item < NR * 16; item += 32) {
+  for (int item = lane; item < R * 16; item += 32) {
     const int n = item >> 4, ch = item & 15;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < R) {
-      const int j = n / a.heads, h = n - j * a.heads;
-      const uint16_t* src = a.q + (static_cast<int64_t>(req) * a.query_len + j) * a.q_tok +
-                            static_cast<int64_t>(h) * a.q_head + ch * 8;
-      v = __ldg(reinterpret_cast<const uint4*>(src));
-    }
+    const int j = n / a.heads, h = n - j * a.heads;
+    const uint16_t* src = a.q + (static_cast<int64_t>(req) * a.query_len + j) * a.q_tok +
+                          static_cast<int64_t>(h) * a.q_head + ch * 8;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
     const int sub = ch >> 3, c = ch & 7;
-    uint8_t* p = dst + sub * (NR * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4);
+    uint8_t* p = dst + sub * (MQ * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4);
     *reinterpret_cast<uint4*>(p) = v;
   }
 }
 
-// Max over the warp's 32 lanes of each of NR columns.  Returns, in each lane,
-// the max of column (lane >> 1) for NR = 16 or column lane for NR = 32.
-template <int W, int O, int NR>
-__device__ __forceinline__ void tmax_stage(float (&v)[NR], int lane) {
-  if constexpr (W > 1) {
-    const bool up = (lane & O) != 0;
-#pragma unroll
-    for (int k = 0; k < W / 2; ++k) {
-      const float send = up ? v[k] : v[k + W / 2];
-      const float keep = up ? v[k + W / 2] : v[k];
-      v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
-    }
-    tmax_stage<W / 2, O / 2, NR>(v, lane);
-  }
-}
-
-template <int NR>
-__device__ __forceinline__ float transpose_max(float (&v)[NR], int lane) {
-  tmax_stage<NR, 16, NR>(v, lane);
-  float r = v[0];
-  if constexpr (NR == 16) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, 1));
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
@@ -232,25 +216,24 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
   return r != 0;
 }
 
-// Insert `key` into row `n`'s descending candidate list L[k*NR + n].
-template <int NR, int TK>
+// Insert `key` into row `n`'s descending candidate list L[k*kLanes + n].
+template <int TK>
 __device__ __forceinline__ void list_insert(uint64_t* L, int n, uint64_t key, int& cnt,
                                             uint64_t& thr) {
   if (cnt == TK && key <= thr) return;
   int p = cnt < TK ? cnt : TK - 1;
   while (p > 0) {
-    const uint64_t prev = L[(p - 1) * NR + n];
+    const uint64_t prev = L[(p - 1) * kLanes + n];
     if (prev >= key) break;
-    L[p * NR + n] = prev;
+    L[p * kLanes + n] = prev;
     --p;
   }
-  L[p * NR + n] = key;
+  L[p * kLanes + n] = key;
   if (cnt < TK) ++cnt;
-  thr = cnt == TK ? L[(TK - 1) * NR + n] : 0ull;
+  thr = cnt == TK ? L[(TK - 1) * kLanes + n] : 0ull;
 }
 
 // Forced blocks, then the best candidates, in ascending id order, -1 padded.
-template <int NR>
 __device__ void finalize_row(const DecodeArgs& a, const uint64_t* L, int n, int cnt, int c,
                              int32_t* out) {
   const int topk = a.topk;
@@ -265,14 +248,43 @@ __device__ void finalize_row(const DecodeArgs& a, const uint64_t* L, int n, int 
   int o = 0;
   for (int b = 0; b < f_lo; ++b) out[o++] = b;
   for (int x = 0; x < take; ++x) {
-    const int bx = key_block(L[x * NR + n]);
+    const int bx = key_block(L[x * kLanes + n]);
     int r = 0;
-    for (int y = 0; y < take; ++y) r += key_block(L[y * NR + n]) < bx;
+    for (int y = 0; y < take; ++y) r += key_block(L[y * kLanes + n]) < bx;
     out[f_lo + r] = bx;
   }
   o = f_lo + take;
   for (int b = l_lo; b <= c; ++b) out[o++] = b;
   for (; o < topk; ++o) out[o] = -1;
+}
+
+// Row max of one 128-column accumulator row (this lane's TMEM lane), with the
+// columns past `lim` left out when lim < 127.
+__device__ __forceinline__ float acc_row_max(uint32_t taddr, int lim) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int c0 = 0; c0 < kAccCols; c0 += 64) {
+    uint32_t v[32], w[32];
+    tmem_ld32(taddr + c0, v);
+    tmem_ld32(taddr + c0 + 32, w);
+    tmem_ld_wait32x2(v, w);
+    if (lim >= 127) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        m0 = fmax3(m0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+        m1 = fmax3(m1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
+        m0 = fmax3(m0, __uint_as_float(w[k]), __uint_as_float(w[k + 1]));
+        m1 = fmax3(m1, __uint_as_float(w[k + 2]), __uint_as_float(w[k + 3]));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
+        if (c0 + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(w[k]));
+      }
+    }
+  }
+  return fmaxf(m0, m1);
 }
 
 // ----------------------------------------------------------- NVFP4 dequant
@@ -325,10 +337,10 @@ __device__ __forceinline__ void dequant8(uint32_t codes, const uint4& t, uint32_
 
 // ------------------------------------------------------------------ kernel
 
-template <bool FP4, int NR, int TK>
-__global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
+template <bool FP4, int MQ, int TK>
+__global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const DecodeArgs a) {
-  using C = Cfg<FP4, NR, TK>;
+  using C = Cfg<FP4, MQ, TK>;
   constexpr int S = C::kStages;
   constexpr int RS = C::kRawStages;
   extern __shared__ uint8_t smem_raw[];
@@ -339,7 +351,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
   uint8_t* sQ = sm + C::oQ;
   uint4* sTab = reinterpret_cast<uint4*>(sm + C::oTab);
   uint64_t* sList = reinterpret_cast<uint64_t*>(sm + C::oList);
-  float* sRed = reinterpret_cast<float*>(sm + C::oRed);
+  int* sCnt = reinterpret_cast<int*>(sm + C::oCnt);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::oBar);
   uint64_t* empty = full + S;
   uint64_t* raw_full = empty + S;
@@ -353,7 +365,6 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
   volatile int* abort_flag = &misc->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kTmemCols = (kAccBufs * NR) < 32 ? 32 : kAccBufs * NR;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
@@ -374,14 +385,13 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
     }
     mbar_init(done_bar, 1);
     misc->abort = 0;
-    misc->last = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     if (!FP4 && lane == 0) prefetch_tensormap(&kmap);
     partition(a, misc, lane);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&misc->tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -396,7 +406,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
   int req, b0, b1, nb;
   long long preq;
 
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     int seg = 0;
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
       const int slot = seg & 1;
       if (seg >= 2) ok = warp_wait(&q_empty[slot], ((seg >> 1) - 1) & 1, abort_flag);
       if (!ok) break;
-      load_q_tile<NR>(a, req, sQ + slot * C::kQBytes, lane);
+      load_q_tile<MQ>(a, req, sQ + slot * C::kQBytes, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[slot]);
@@ -470,10 +480,10 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, NR);
+      constexpr uint32_t idesc = idesc_bf16_f32(MQ, kAccCols);
       int seg = 0;
       uint32_t it = 0;
       bool ok = true;
@@ -491,12 +501,13 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
           if (ar > 0) ok = mbar_wait(&acc_empty[ab], (ar - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t aaddr = smem_u32(sA + st * kTileBytes);
-          const uint32_t d = tmem_base + ab * NR;
+          const uint32_t kaddr = smem_u32(sA + st * kTileBytes);
+          const uint32_t d = tmem_base + ab * kAccCols;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_kmajor_sw128(aaddr + (k >> 2) * (kTileBytes / 2) + (k & 3) * 32);
-            const uint64_t bd = sdesc_kmajor_sw128(qaddr + (k >> 2) * (NR * 128) + (k & 3) * 32);
+            const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (MQ * 128) + (k & 3) * 32);
+            const uint64_t bd =
+                sdesc_kmajor_sw128(kaddr + (k >> 2) * (kTileBytes / 2) + (k & 3) * 32);
             mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
           }
           mma_commit(&empty[st]);
@@ -513,158 +524,143 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
       mbar_wait(done_bar, 0, &dummy);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp == kEpiA || warp == kEpiB) {
     // ------------------------------------------------------------- epilogue
-    const int ep = threadIdx.x - 64;
-    const int quad = warp & 3;
+    const int e = warp == kEpiA ? 0 : 1;
+    const int n = lane;  // query row (TMEM lane)
     const int R = a.rows_per_req;
-    const int my_j = ep < R ? ep / a.heads : 0;
-    const int my_h = ep < R ? ep - my_j * a.heads : 0;
+    const int my_j = n < R ? n / a.heads : 0;
+    const int my_h = n < R ? n - my_j * a.heads : 0;
     const bool select = a.mode == kModeSelect;
+    uint64_t* L = sList + e * TK * kLanes;
     uint32_t it = 0;
     bool ok = true;
-    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+    while (walker.next(a, req, b0, b1, nb, preq)) {
       const int seq = req_len(a, req);
-      const int base = seq - a.query_len;  // position of query 0
-      const int pos = base + my_j;
+      const int pos = seq - a.query_len + my_j;
       const int c = pos >= 0 ? (pos >> 7) : -1;
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
       int cnt = 0;
       uint64_t thr = 0;
-      for (int b = b0; b < b1; ++b) {
+      for (int b = b0; b < b1; ++b, ++it) {
+        if ((it & 1u) != static_cast<uint32_t>(e) || !ok) continue;
+        const int page = __ldg(trow + b);
         const uint32_t ab = it % kAccBufs, ar = it / kAccBufs;
         bool got = true;
         if (lane == 0) got = mbar_wait(&acc_full[ab], ar & 1, abort_flag);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        const int par = it & 1;
-        if (got) {
-          tc_fence_after();
-          float v[NR];
-#pragma unroll
-          for (int c0 = 0; c0 < NR; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * NR + c0, r);
-            tmem_ld_wait16(r);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[c0 + k] = __uint_as_float(r[k]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[ab]);
-          if (b * kBlock + kBlock - 1 > base) {
-            // Last block(s): token t is visible to row n = j*heads + h iff
-            // t - base <= j, i.e. n >= (t - base) * heads.
-            const int trel = b * kBlock + quad * 32 + lane - base;
-            const int lim = trel <= 0 ? 0 : min(trel, a.query_len) * a.heads;
-#pragma unroll
-            for (int n = 0; n < NR; ++n)
-              if (n < lim) v[n] = -INFINITY;
-          }
-          const float cm = transpose_max<NR>(v, lane);
-          float* red = sRed + par * 128 + quad * 32;
-          if constexpr (NR == 16) {
-            if ((lane & 1) == 0) red[lane >> 1] = cm;
-          } else {
-            red[lane] = cm;
-          }
-        }
-        if (!bar_and(1, 128, got)) {
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
-          break;
+          continue;
         }
-        if (ep < R) {
-          const float* red = sRed + par * 128;
-          const float m = fmaxf(fmaxf(red[ep], red[32 + ep]), fmaxf(red[64 + ep], red[96 + ep]));
-          const int page = __ldg(trow + b);
+        tc_fence_after();
+        const float m = acc_row_max(tmem_base + ab * kAccCols, pos - b * kBlock);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        if (n < R) {
           const float s = (page >= 0 && page < a.num_pages) ? m * a.sm_scale : -INFINITY;
           if (!select) {
             a.score[my_h * a.s_head + row * a.s_row + b] = s;
           } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
-            list_insert<NR, TK>(sList, ep, make_key(s, b), cnt, thr);
+            list_insert<TK>(L, n, make_key(s, b), cnt, thr);
           }
         }
-        ++it;
       }
-      if (!ok) break;
       // ---------------------------------------------------- segment end
+      if (e == 1) sCnt[n] = cnt;
+      if (!bar_and(1, 64, ok)) break;
       if (!select) {
-        if (b1 == nb && a.fill_width > nb) {
+        if (e == 0 && b1 == nb && a.fill_width > nb) {
           const int w = a.fill_width - nb;
-          for (int idx = ep; idx < R * w; idx += 128) {
-            const int n = idx / w, b = nb + (idx - n * w);
-            const int j = n / a.heads, h = n - j * a.heads;
-            a.score[h * a.s_head + (static_cast<int64_t>(req) * a.query_len + j) * a.s_row + b] =
+          for (int idx = lane; idx < R * w; idx += 32) {
+            const int rr = idx / w, bb = nb + (idx - rr * w);
+            const int j = rr / a.heads, h = rr - j * a.heads;
+            a.score[h * a.s_head + (static_cast<int64_t>(req) * a.query_len + j) * a.s_row + bb] =
                 -INFINITY;
           }
         }
         continue;
       }
-      const int first = cta_of(preq, total, gridDim.x);
-      const int last = cta_of(preq + nb - 1, total, gridDim.x);
-      int32_t* out = a.ids + my_h * a.i_head + row * a.i_row;
-      int nseg = 0;
-      for (int cc = first; cc <= last; ++cc) nseg += share_nonempty(cc, total, gridDim.x);
-      if (nseg == 1) {
-        if (ep < R) finalize_row<NR>(a, sList, ep, cnt, c, out);
-        continue;
-      }
-      const int slot_stride = NR * TK;
-      if (ep < R) {
-        uint64_t* dst = a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + ep * TK;
-        for (int k = 0; k < TK; ++k) dst[k] = k < cnt ? sList[k * NR + ep] : 0ull;
-      }
-      __threadfence();
-      named_barrier_sync(1, 128);
-      if (ep == 0) {
-        const int old = atomicAdd(a.counters + req, 1);
-        const int is_last = old == nseg - 1;
-        if (is_last) a.counters[req] = 0;
-        misc->last = is_last;
-      }
-      named_barrier_sync(1, 128);
-      if (misc->last) {
-        __threadfence();
-        if (ep < R) {
-          cnt = 0;
-          thr = 0;
-          for (int s = first; s <= last; ++s) {
-            if (!share_nonempty(s, total, gridDim.x)) continue;
-            const uint64_t* src = a.partials + (static_cast<int64_t>(s) + req) * slot_stride + ep * TK;
-            for (int k = 0; k < TK; ++k) {
-              const uint64_t key = __ldcg(src + k);
-              if (key == 0ull || (cnt == TK && key <= thr)) break;
-              list_insert<NR, TK>(sList, ep, key, cnt, thr);
+      if (e == 0) {
+        // Fold the other epilogue warp's list for this row into this one.
+        if (n < R) {
+          const uint64_t* L1 = sList + TK * kLanes;
+          const int c1 = sCnt[n];
+          for (int k = 0; k < c1; ++k) {
+            const uint64_t key = L1[k * kLanes + n];
+            if (cnt == TK && key <= thr) break;
+            list_insert<TK>(L, n, key, cnt, thr);
+          }
+        }
+        const int first = cta_of(preq, total, gridDim.x);
+        const int last = cta_of(preq + nb - 1, total, gridDim.x);
+        int32_t* out = a.ids + my_h * a.i_head + row * a.i_row;
+        int nseg = 0;
+        for (int cc = first; cc <= last; ++cc) nseg += share_nonempty(cc, total, gridDim.x);
+        if (nseg == 1) {
+          if (n < R) finalize_row(a, L, n, cnt, c, out);
+        } else {
+          const int slot_stride = kLanes * TK;
+          if (n < R) {
+            uint64_t* dst = a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK;
+            for (int k = 0; k < TK; ++k) dst[k] = k < cnt ? L[k * kLanes + n] : 0ull;
+          }
+          __threadfence();
+          __syncwarp();
+          int is_last = 0;
+          if (lane == 0) {
+            const int old = atomicAdd(a.counters + req, 1);
+            is_last = old == nseg - 1;
+            if (is_last) a.counters[req] = 0;
+          }
+          if (__shfl_sync(0xffffffffu, is_last, 0)) {
+            __threadfence();
+            if (n < R) {
+              cnt = 0;
+              thr = 0;
+              for (int s = first; s <= last; ++s) {
+                if (!share_nonempty(s, total, gridDim.x)) continue;
+                const uint64_t* src =
+                    a.partials + (static_cast<int64_t>(s) + req) * slot_stride + n * TK;
+                for (int k = 0; k < TK; ++k) {
+                  const uint64_t key = __ldcg(src + k);
+                  if (key == 0ull || (cnt == TK && key <= thr)) break;
+                  list_insert<TK>(L, n, key, cnt, thr);
+                }
+              }
+              finalize_row(a, L, n, cnt, c, out);
             }
           }
-          finalize_row<NR>(a, sList, ep, cnt, c, out);
         }
       }
+      // The other warp may reuse its list only after the fold above.
+      named_barrier_sync(1, 64);
     }
-    if (ok) {
+    if (ok && e == 0) {
       // Requests with no blocks at all appear in no share: spread them over CTAs.
       for (int i = blockIdx.x; i < a.num_reqs; i += gridDim.x) {
         if (req_blocks(a, i) != 0) continue;
         if (!select) {
           const int w = a.fill_width;
-          for (int idx = ep; idx < R * w; idx += 128) {
-            const int n = idx / w, b = idx - n * w;
-            const int j = n / a.heads, h = n - j * a.heads;
-            a.score[h * a.s_head + (static_cast<int64_t>(i) * a.query_len + j) * a.s_row + b] =
+          for (int idx = lane; idx < R * w; idx += 32) {
+            const int rr = idx / w, bb = idx - rr * w;
+            const int j = rr / a.heads, h = rr - j * a.heads;
+            a.score[h * a.s_head + (static_cast<int64_t>(i) * a.query_len + j) * a.s_row + bb] =
                 -INFINITY;
           }
         } else {
-          for (int idx = ep; idx < R * a.topk; idx += 128) {
-            const int n = idx / a.topk, k = idx - n * a.topk;
-            const int j = n / a.heads, h = n - j * a.heads;
+          for (int idx = lane; idx < R * a.topk; idx += 32) {
+            const int rr = idx / a.topk, k = idx - rr * a.topk;
+            const int j = rr / a.heads, h = rr - j * a.heads;
             a.ids[h * a.i_head + (static_cast<int64_t>(i) * a.query_len + j) * a.i_row + k] = -1;
           }
         }
       }
     }
-  } else if constexpr (FP4) {
+  } else if (FP4 && warp >= kDeqWarp0) {
     // ---------------------------------------------------- NVFP4 dequantiser
-    const int dq = threadIdx.x - 192;  // 0..127
+    const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..127
     uint32_t it = 0;
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
@@ -676,8 +672,7 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
           got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
           if (got && sr > 0) got = mbar_wait(&empty[st], (sr - 1) & 1, abort_flag);
         }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
@@ -713,33 +708,29 @@ __global__ void __launch_bounds__(Cfg<FP4, NR, TK>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && misc->abort) atomicOr(a.status, MM3IDX_DEV_TIMEOUT);
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <bool FP4, int NR, int TK>
+template <bool FP4, int MQ, int TK>
 cudaError_t launch_t(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
-  using C = Cfg<FP4, NR, TK>;
-  static bool configured = false;  // per process; attribute is per device-function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP4, NR, TK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  decode_kernel<FP4, NR, TK><<<grid, C::kThreads, C::kSmem, s>>>(kmap, a);
+  using C = Cfg<FP4, MQ, TK>;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP4, MQ, TK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<FP4, MQ, TK><<<grid, C::kThreads, C::kSmem, s>>>(kmap, a);
   return cudaGetLastError();
 }
 
 template <bool FP4>
 cudaError_t dispatch(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
-  const int nr = decode_nr(a.rows_per_req), tk = decode_tk(a.topk);
-  if (nr == 16 && tk == 16) return launch_t<FP4, 16, 16>(kmap, a, grid, s);
-  if (nr == 16) return launch_t<FP4, 16, 32>(kmap, a, grid, s);
-  if (tk == 16) return launch_t<FP4, 32, 16>(kmap, a, grid, s);
-  return launch_t<FP4, 32, 32>(kmap, a, grid, s);
+  const bool small = a.rows_per_req <= 16, tk16 = decode_tk(a.topk) == 16;
+  if (small && tk16) return launch_t<FP4, 64, 16>(kmap, a, grid, s);
+  if (small) return launch_t<FP4, 64, 32>(kmap, a, grid, s);
+  if (tk16) return launch_t<FP4, 128, 16>(kmap, a, grid, s);
+  return launch_t<FP4, 128, 32>(kmap, a, grid, s);
 }
 
 }  // namespace

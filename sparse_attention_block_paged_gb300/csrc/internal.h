@@ -39,7 +39,7 @@ struct DecodeArgs {
   // select mode
   int32_t* ids;
   int64_t i_head, i_row;
-  uint64_t* partials;         // [slots, nr_pad, tk] keys
+  uint64_t* partials;         // [slots, 32 rows, tk] keys
   int32_t* counters;          // [num_reqs]
   int32_t* status;            // device status word
 };
@@ -89,6 +89,5 @@ cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
 int decode_ctas_per_sm();
 // Keys per (slot, row) in the decode workspace for a given topk.
 inline int decode_tk(int topk) { return topk <= 16 ? 16 : 32; }
-inline int decode_nr(int rows_per_req) { return rows_per_req <= 16 ? 16 : 32; }
 
 }  // namespace mm3idx

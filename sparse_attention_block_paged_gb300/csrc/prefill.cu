@@ -17,11 +17,12 @@
 //                [tokens, heads, 128]) once per tile, and each key page (from
 //                a 2-D map over [pages*128, 128]) into a 4-stage ring.
 //   * warp 1   : one thread issues tcgen05.mma, M = 128 query rows,
-//                N = 128 key tokens, K = 128, into one of two 128-column fp32
-//                TMEM accumulators.
-//   * warps 2-5: epilogue: tcgen05.ld of the thread's query row (128 fp32
-//                columns), causal mask only on diagonal blocks, row max,
-//                scale, one fp32 store per (row, block).
+//                N = 128 key tokens, K = 128, into one of four 128-column fp32
+//                TMEM accumulators (all 512 columns).
+//   * warps 2-9: epilogue, two teams of four warps taking alternate units:
+//                tcgen05.ld of the thread's query row (128 fp32 columns),
+//                causal mask only on diagonal blocks, row max with 3-input
+//                max, scale, one fp32 store per (row, block).
 #include <cuda_runtime.h>
 
 #include "../../include/mm3idx.h"
@@ -32,9 +33,9 @@ namespace mm3idx {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kAcc = 2;
+constexpr int kAcc = 4;
 constexpr int kTile = 32768;  // 128 x 128 bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int oQ = 0;
 constexpr int oK = oQ + 2 * kTile;
 constexpr int oBar = oK + kStages * kTile;
@@ -93,43 +94,10 @@ __device__ __forceinline__ int clamp_len(const PrefillArgs& a, int i) {
   return min(max(__ldg(a.seq_lens + i), 0), a.max_seq_len);
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                 "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-
-__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -283,7 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue
-    const int quad = warp & 3;
+    // Two teams of four warps (one warp per TMEM lane quadrant) take
+    // alternate units, so two accumulators drain at once.
+    const int team = (warp - 2) >> 2;
+    const int quad = warp & 3;       // a warp may only read lanes 32*(warp%4)..+31
     const int r = quad * 32 + lane;  // query row within the tile
     uint32_t it = 0;
     bool ok = true;
@@ -296,52 +267,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* srow = a.score + head * a.s_head +
                     (static_cast<int64_t>(req) * a.query_len + qrow) * a.s_row;
       const bool active = U.b < tile_blocks(prefix, U.qt, a.query_len);
-      if (active) {
-        const uint32_t ab = it % kAcc, ar = it / kAcc;
+      const uint32_t mine = active ? it++ : 0u;
+      if (active && (mine & 1u) == static_cast<uint32_t>(team)) {
+        const uint32_t ab = mine % kAcc, ar = mine / kAcc;
         bool got = true;
         if (lane == 0) got = mbar_wait(&acc_full[ab], ar & 1, abort_flag);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        float best = -INFINITY;
-        if (got) {
-          tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * 128;
-          const int lim = pos - U.b * 128;  // columns 0..lim are visible
-          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c0, v);
-            tmem_ld_wait32(v);
-            if (lim >= 127) {
-#pragma unroll
-              for (int k = 0; k < 32; k += 4) {
-                m0 = fmaxf(m0, __uint_as_float(v[k]));
-                m1 = fmaxf(m1, __uint_as_float(v[k + 1]));
-                m2 = fmaxf(m2, __uint_as_float(v[k + 2]));
-                m3 = fmaxf(m3, __uint_as_float(v[k + 3]));
-              }
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k)
-                if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
-            }
-          }
-          best = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[ab]);
-        }
-        if (!bar_and(1, 128, got)) {
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
-        ++it;
-        if (row_ok && pos >= 0) srow[U.b] = best * a.sm_scale;
-      } else if (a.fill_width > 0 && row_ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * 128;
+        const int lim = pos - U.b * 128;  // columns 0..lim are visible
+        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint32_t v[32], w[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_ld32(taddr + c0 + 32, w);
+          tmem_ld_wait32x2(v, w);
+          if (lim >= 127) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+              m0 = fmax3(m0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
+              m0 = fmax3(m0, __uint_as_float(w[k]), __uint_as_float(w[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(w[k + 2]), __uint_as_float(w[k + 3]));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
+              if (c0 + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(w[k]));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        if (row_ok) srow[U.b] = fmaxf(m0, m1) * a.sm_scale;
+      } else if (!active && a.fill_width > 0 && row_ok && (U.u & 1) == team) {
         srow[U.b] = -INFINITY;
       }
       // The tile's last scheduled block: blocks past the worst-case schedule.
-      if (a.fill_width > 0 && row_ok && U.b == U.n - 1)
+      if (a.fill_width > 0 && row_ok && team == 0 && U.b == U.n - 1)
         for (int b = U.n; b < a.fill_width; ++b) srow[b] = -INFINITY;
     }
   }
