@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmm3idx.so")
 SOURCES = ["api.cu", "decode.cu", "prefill.cu", "select.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "warp_select.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

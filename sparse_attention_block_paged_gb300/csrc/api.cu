@@ -148,7 +148,7 @@ size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_l
   const size_t counters = (static_cast<size_t>(num_reqs) * 4 + 255) / 256 * 256;
   const size_t slots = static_cast<size_t>(sms) * decode_ctas_per_sm() + num_reqs;
   (void)R;
-  return counters + slots * 32 * decode_tk(topk) * 8;
+  return counters + slots * 32 * decode_tk(topk) * 8;  // [slot][32 rows][tk keys]
 }
 
 size_t prefill_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len, int32_t max_seq_len) {

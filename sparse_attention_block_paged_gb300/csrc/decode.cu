@@ -26,12 +26,16 @@
 //   * warps 0,4: epilogue, alternate blocks.  Lane n loads its row's 128
 //                token scores with tcgen05.ld, masks only the causal tail,
 //                takes the max with 3-input max, scales, and either stores the
-//                score or inserts the candidate key into a sorted per-warp,
-//                per-row list in shared memory.  At a request boundary the two
-//                lists merge; a request split across CTAs merges its lists in
-//                the last CTA to finish it (atomic arrival count), which
-//                re-pins the forced blocks, writes the ids and resets the
-//                counter.
+//                score or offers the candidate key to its row's sorted list,
+//                kept in registers.  At a request boundary both warps hand
+//                their lists to the merge warp through shared memory and go
+//                on streaming.
+//   * warp 3   : merge warp.  Folds the two lists of each row; a request
+//                split across CTAs merges its lists in the last CTA to finish
+//                it (atomic arrival count).  Writes the ids (forced blocks
+//                re-pinned, ascending, -1 pad) and resets the counter.  Each
+//                CTA walks its two boundary requests first so these merges
+//                overlap the streaming of its interior requests.
 //
 // Every wait is bounded (ptx.cuh).  A wait that gives up raises an abort flag
 // shared by the CTA's roles and the MM3IDX_DEV_TIMEOUT status bit.
@@ -41,6 +45,7 @@
 #include "../../include/mm3idx.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "warp_select.cuh"
 
 namespace mm3idx {
 namespace {
@@ -53,22 +58,21 @@ constexpr int kFp4CodeBytes = kBlock * kD / 2;       // 8 KB
 constexpr int kFp4ScaleBytes = kBlock * kD / 16;     // 1 KB
 constexpr int kFp4RawBytes = kFp4CodeBytes + kFp4ScaleBytes;
 constexpr int kLanes = 32;                           // rows per list slot
-constexpr int kEpiA = 0, kMmaWarp = 1, kProdWarp = 2, kEpiB = 4, kDeqWarp0 = 5;
+constexpr int kEpiA = 0, kMmaWarp = 1, kProdWarp = 2, kMergeWarp = 3, kEpiB = 4, kDeqWarp0 = 5;
 
 template <bool FP4, int MQ, int TK>
 struct Cfg {
   static constexpr int kStages = FP4 ? (MQ == 64 ? 3 : 2) : (MQ == 64 ? 5 : 4);
-  static constexpr int kRawStages = FP4 ? (MQ == 64 ? 8 : 6) : 0;
+  static constexpr int kRawStages = FP4 ? ((MQ == 64 && TK == 16) ? 8 : 6) : 0;
   static constexpr int kThreads = FP4 ? 288 : 160;
   static constexpr int kQBytes = MQ * kD * 2;
   static constexpr int oA = 0;
   static constexpr int oRaw = oA + kStages * kTileBytes;
   static constexpr int oQ = oRaw + kRawStages * kFp4RawBytes;
   static constexpr int oTab = oQ + 2 * kQBytes;
-  static constexpr int oList = oTab + (FP4 ? 256 * 16 : 0);
-  static constexpr int oCnt = oList + 2 * TK * kLanes * 8;
-  static constexpr int oBar = oCnt + kLanes * 4;
-  static constexpr int kBars = 2 * kStages + 2 * kRawStages + 2 * kAccBufs + 4 + 1;
+  static constexpr int oHand = oTab + (FP4 ? 256 * 16 : 0);  // [2 slots][2 warps][TK][32]
+  static constexpr int oBar = oHand + 2 * 2 * TK * kLanes * 8;
+  static constexpr int kBars = 2 * kStages + 2 * kRawStages + 2 * kAccBufs + 4 + 4 + 1;
   static constexpr int oMisc = oBar + kBars * 8;
   static constexpr int kSmem = oMisc + 64 + 1024;
   static_assert(oQ % 1024 == 0, "Q tile must be 1024-byte aligned");
@@ -76,8 +80,8 @@ struct Cfg {
 };
 
 struct Misc {
-  long long lo, hi, total, p0;
-  int i0;
+  long long lo, hi, total, p0, pl;
+  int i0, il;
   uint32_t tmem;
   int abort;
 };
@@ -92,26 +96,50 @@ __device__ __forceinline__ int req_blocks(const DecodeArgs& a, int i) {
 }
 
 // Walks this CTA's share [lo, hi) of the flattened (request, block) list and
-// yields one segment (request, blocks [b0, b1)) at a time.
+// yields one segment (request, blocks [b0, b1)) at a time.  The two boundary
+// segments come first -- the share's first request (whose earlier blocks
+// belong to the previous CTA) and its last request (whose later blocks belong
+// to the next CTA) -- so that the requests split across CTAs complete early
+// and their cross-CTA merges overlap the streaming of the interior requests,
+// which are whole and need no merge.
 struct Walker {
-  int i;
-  long long P, lo, hi;
+  int i0, il;             // first and last request of the share
+  long long p0, pl;       // their first flattened positions
+  long long lo, hi;
+  int stage = 0, i = 0;   // 0: first, 1: last, 2: interior requests
+  long long P = 0;
+  __device__ bool emit(const DecodeArgs& a, int r, long long pr, int& req, int& b0, int& b1,
+                       int& nb, long long& preq) const {
+    const int n = req_blocks(a, r);
+    const long long s = pr > lo ? pr : lo;
+    const long long e = (pr + n) < hi ? (pr + n) : hi;
+    if (e <= s) return false;
+    req = r;
+    preq = pr;
+    nb = n;
+    b0 = static_cast<int>(s - pr);
+    b1 = static_cast<int>(e - pr);
+    return true;
+  }
   __device__ bool next(const DecodeArgs& a, int& req, int& b0, int& b1, int& nb,
                        long long& preq) {
-    while (i < a.num_reqs && P < hi) {
-      const int n = req_blocks(a, i);
-      const long long s = P > lo ? P : lo;
-      const long long e = (P + n) < hi ? (P + n) : hi;
-      req = i;
-      preq = P;
-      nb = n;
-      P += n;
+    if (lo >= hi) return false;
+    if (stage == 0) {
+      stage = 1;
+      if (emit(a, i0, p0, req, b0, b1, nb, preq)) return true;
+    }
+    if (stage == 1) {
+      stage = 2;
+      i = i0 + 1;
+      P = p0 + req_blocks(a, i0);
+      if (il != i0 && emit(a, il, pl, req, b0, b1, nb, preq)) return true;
+    }
+    while (i < il) {
+      const int r = i;
+      const long long pr = P;
+      P += req_blocks(a, r);
       ++i;
-      if (e > s) {
-        b0 = static_cast<int>(s - preq);
-        b1 = static_cast<int>(e - preq);
-        return true;
-      }
+      if (emit(a, r, pr, req, b0, b1, nb, preq)) return true;
     }
     return false;
   }
@@ -120,12 +148,6 @@ struct Walker {
 // The CTA whose share holds flattened position x.
 __device__ __forceinline__ int cta_of(long long x, long long total, int grid) {
   return static_cast<int>(((x + 1) * grid - 1) / total);
-}
-
-// Whether CTA c's share [total*c/grid, total*(c+1)/grid) is non-empty.  With
-// fewer blocks than CTAs some shares are empty; those CTAs see no segment.
-__device__ __forceinline__ bool share_nonempty(int c, long long total, int grid) {
-  return total * (c + 1) / grid > total * c / grid;
 }
 
 // One warp: total block count, this CTA's share and the first request in it.
@@ -148,9 +170,11 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   const long long G = gridDim.x, c = blockIdx.x;
   const long long lo = total * c / G, hi = total * (c + 1) / G;
-  long long P = 0, p0 = total;
-  int i0 = a.num_reqs;
-  for (int b = 0; b < a.num_reqs; b += 32) {
+  // First request with blocks at or past lo (i0) and at or past hi - 1 (il).
+  long long P = 0, p0 = total, pl = total;
+  int i0 = a.num_reqs, il = a.num_reqs;
+  bool need0 = true;
+  for (int b = 0; b < a.num_reqs && hi > lo; b += 32) {
     const int i = b + lane;
     const long long nb = i < a.num_reqs ? req_blocks(a, i) : 0;
     long long incl = nb;
@@ -159,12 +183,20 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
       const long long y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > lo);
-    if (hit) {
-      const int k = __ffs(hit) - 1;
-      const long long ex = __shfl_sync(0xffffffffu, incl - nb, k);
-      i0 = b + k;
-      p0 = P + ex;
+    if (need0) {
+      const unsigned hit = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > lo);
+      if (hit) {
+        const int k = __ffs(hit) - 1;
+        i0 = b + k;
+        p0 = P + __shfl_sync(0xffffffffu, incl - nb, k);
+        need0 = false;
+      }
+    }
+    const unsigned hitl = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > hi - 1);
+    if (hitl) {
+      const int k = __ffs(hitl) - 1;
+      il = b + k;
+      pl = P + __shfl_sync(0xffffffffu, incl - nb, k);
       break;
     }
     P += __shfl_sync(0xffffffffu, incl, 31);
@@ -175,6 +207,8 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
     m->total = total;
     m->i0 = i0;
     m->p0 = p0;
+    m->il = il;
+    m->pl = pl;
   }
 }
 
@@ -203,60 +237,35 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
-// Insert `key` into row `n`'s descending candidate list L[k*kLanes + n].
+// A row's best candidate keys, descending, held in registers (0 = empty).
+// Insertion is a branchless compare-and-swap cascade with static indices.
 template <int TK>
-__device__ __forceinline__ void list_insert(uint64_t* L, int n, uint64_t key, int& cnt,
-                                            uint64_t& thr) {
-  if (cnt == TK && key <= thr) return;
-  int p = cnt < TK ? cnt : TK - 1;
-  while (p > 0) {
-    const uint64_t prev = L[(p - 1) * kLanes + n];
-    if (prev >= key) break;
-    L[p * kLanes + n] = prev;
-    --p;
+struct RegList {
+  uint64_t v[TK];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) v[k] = 0ull;
   }
-  L[p * kLanes + n] = key;
-  if (cnt < TK) ++cnt;
-  thr = cnt == TK ? L[(TK - 1) * kLanes + n] : 0ull;
-}
-
-// Forced blocks, then the best candidates, in ascending id order, -1 padded.
-__device__ void finalize_row(const DecodeArgs& a, const uint64_t* L, int n, int cnt, int c,
-                             int32_t* out) {
-  const int topk = a.topk;
-  if (c < 0) {
-    for (int k = 0; k < topk; ++k) out[k] = -1;
-    return;
+  // Keys at or below this cannot enter.
+  __device__ __forceinline__ uint64_t floor() const { return v[TK - 1]; }
+  __device__ __forceinline__ void insert(uint64_t key) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) {
+      const uint64_t cur = v[k];
+      const bool gt = key > cur;
+      v[k] = gt ? key : cur;
+      key = gt ? cur : key;
+    }
   }
-  const int f_lo = min(a.init_blocks, c + 1);
-  const int l_lo = max(f_lo, c - a.local_blocks + 1);
-  const int nf = f_lo + (c + 1 - l_lo);
-  const int take = min(topk - nf, cnt);
-  int o = 0;
-  for (int b = 0; b < f_lo; ++b) out[o++] = b;
-  for (int x = 0; x < take; ++x) {
-    const int bx = key_block(L[x * kLanes + n]);
-    int r = 0;
-    for (int y = 0; y < take; ++y) r += key_block(L[y * kLanes + n]) < bx;
-    out[f_lo + r] = bx;
+  __device__ __forceinline__ void offer(uint64_t key) {
+    if (key > floor()) insert(key);
   }
-  o = f_lo + take;
-  for (int b = l_lo; b <= c; ++b) out[o++] = b;
-  for (; o < topk; ++o) out[o] = -1;
-}
+  // Row-major store to a [k][kLanes] shared-memory table at column n.
+  __device__ __forceinline__ void store_cols(uint64_t* t, int n) const {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) t[k * kLanes + n] = v[k];
+  }
+};
 
 // Row max of one 128-column accumulator row (this lane's TMEM lane), with the
 // columns past `lim` left out when lim < 127.
@@ -350,8 +359,7 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   uint8_t* sRaw = sm + C::oRaw;
   uint8_t* sQ = sm + C::oQ;
   uint4* sTab = reinterpret_cast<uint4*>(sm + C::oTab);
-  uint64_t* sList = reinterpret_cast<uint64_t*>(sm + C::oList);
-  int* sCnt = reinterpret_cast<int*>(sm + C::oCnt);
+  uint64_t* sHand = reinterpret_cast<uint64_t*>(sm + C::oHand);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::oBar);
   uint64_t* empty = full + S;
   uint64_t* raw_full = empty + S;
@@ -360,7 +368,9 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* q_full = acc_empty + kAccBufs;
   uint64_t* q_empty = q_full + 2;
-  uint64_t* done_bar = q_empty + 2;
+  uint64_t* h_full = q_empty + 2;     // both epilogue warps handed a request's lists over
+  uint64_t* h_empty = h_full + 2;     // the merge warp is done with a hand-over slot
+  uint64_t* done_bar = h_empty + 2;
   Misc* misc = reinterpret_cast<Misc*>(sm + C::oMisc);
   volatile int* abort_flag = &misc->abort;
 
@@ -382,6 +392,8 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
+      mbar_init(&h_full[s], 2);
+      mbar_init(&h_empty[s], 1);
     }
     mbar_init(done_bar, 1);
     misc->abort = 0;
@@ -401,7 +413,7 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem;
   const long long total = misc->total;
-  Walker walker{misc->i0, misc->p0, misc->lo, misc->hi};
+  Walker walker{misc->i0, misc->il, misc->p0, misc->pl, misc->lo, misc->hi};
 
   int req, b0, b1, nb;
   long long preq;
@@ -532,26 +544,24 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     const int my_j = n < R ? n / a.heads : 0;
     const int my_h = n < R ? n - my_j * a.heads : 0;
     const bool select = a.mode == kModeSelect;
-    uint64_t* L = sList + e * TK * kLanes;
+    RegList<TK> list;
     uint32_t it = 0;
+    int seg = 0;
     bool ok = true;
-    while (walker.next(a, req, b0, b1, nb, preq)) {
+    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
       const int seq = req_len(a, req);
       const int pos = seq - a.query_len + my_j;
       const int c = pos >= 0 ? (pos >> 7) : -1;
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
-      int cnt = 0;
-      uint64_t thr = 0;
+      list.clear();
       for (int b = b0; b < b1; ++b, ++it) {
-        if ((it & 1u) != static_cast<uint32_t>(e) || !ok) continue;
+        if ((it & 1u) != static_cast<uint32_t>(e)) continue;
         const int page = __ldg(trow + b);
         const uint32_t ab = it % kAccBufs, ar = it / kAccBufs;
-        bool got = true;
-        if (lane == 0) got = mbar_wait(&acc_full[ab], ar & 1, abort_flag);
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
+        if (!warp_wait(&acc_full[ab], ar & 1, abort_flag)) {
           ok = false;
-          continue;
+          break;
         }
         tc_fence_after();
         const float m = acc_row_max(tmem_base + ab * kAccCols, pos - b * kBlock);
@@ -563,81 +573,150 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
           if (!select) {
             a.score[my_h * a.s_head + row * a.s_row + b] = s;
           } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
-            list_insert<TK>(L, n, make_key(s, b), cnt, thr);
+            list.offer(make_key(s, b));
           }
         }
       }
-      // ---------------------------------------------------- segment end
-      if (e == 1) sCnt[n] = cnt;
-      if (!bar_and(1, 64, ok)) break;
-      if (!select) {
-        if (e == 0 && b1 == nb && a.fill_width > nb) {
-          const int w = a.fill_width - nb;
-          for (int idx = lane; idx < R * w; idx += 32) {
-            const int rr = idx / w, bb = nb + (idx - rr * w);
-            const int j = rr / a.heads, h = rr - j * a.heads;
-            a.score[h * a.s_head + (static_cast<int64_t>(req) * a.query_len + j) * a.s_row + bb] =
-                -INFINITY;
-          }
+      if (!ok) break;
+      if (select) {
+        // Hand this request's lists to the merge warp and keep streaming.
+        const int hs = seg & 1;
+        if (seg >= 2 && !warp_wait(&h_empty[hs], ((seg >> 1) - 1) & 1, abort_flag)) break;
+        if (n < R) list.store_cols(sHand + (hs * 2 + e) * TK * kLanes, n);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&h_full[hs]);
+      } else if (e == 0 && b1 == nb && a.fill_width > nb) {
+        const int w = a.fill_width - nb;
+        for (int idx = lane; idx < R * w; idx += 32) {
+          const int rr = idx / w, bb = nb + (idx - rr * w);
+          const int j = rr / a.heads, h = rr - j * a.heads;
+          a.score[h * a.s_head + (static_cast<int64_t>(req) * a.query_len + j) * a.s_row + bb] =
+              -INFINITY;
         }
-        continue;
       }
-      if (e == 0) {
-        // Fold the other epilogue warp's list for this row into this one.
+      ++seg;
+    }
+  } else if (warp == kMergeWarp) {
+    // ------------------------------------------------------------ merge warp
+    // Per request (in the walker's order): fold the two epilogue warps'
+    // lists row by row (lane n owns row n).  A request held by one CTA is
+    // written here; otherwise each row's list goes to this CTA's partial slot
+    // and the last CTA to finish the request folds all slots the same way
+    // (each slot's list is sorted, so a key at or below the running floor
+    // ends it).  With total >= grid every share is non-empty, so the
+    // request's CTAs are first..last; with fewer blocks than CTAs every
+    // non-empty share is a single block, so block k sits in cta_of(preq + k).
+    // Rows are written by the whole warp, one row at a time.
+    const int n = lane;
+    const int R = a.rows_per_req;
+    const bool select = a.mode == kModeSelect;
+    int seg = 0;
+    bool ok = true;
+    while (select && ok && walker.next(a, req, b0, b1, nb, preq)) {
+      const int hs = seg & 1;
+      if (!warp_wait(&h_full[hs], (seg >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint64_t* H0 = sHand + (hs * 2 + 0) * TK * kLanes;
+      const uint64_t* H1 = sHand + (hs * 2 + 1) * TK * kLanes;
+      RegList<TK> list;
+      list.clear();
+      if (n < R) {
+#pragma unroll
+        for (int k = 0; k < TK; ++k) list.v[k] = H0[k * kLanes + n];
+        for (int k = 0; k < TK; ++k) {
+          const uint64_t key = H1[k * kLanes + n];
+          if (key <= list.floor()) break;
+          list.insert(key);
+        }
+      }
+      const int first = cta_of(preq, total, gridDim.x);
+      const int last = cta_of(preq + nb - 1, total, gridDim.x);
+      const bool dense = total >= gridDim.x;
+      const int nseg = dense ? last - first + 1 : nb;
+      bool write_rows = nseg == 1;
+      if (!write_rows) {
+        const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
         if (n < R) {
-          const uint64_t* L1 = sList + TK * kLanes;
-          const int c1 = sCnt[n];
-          for (int k = 0; k < c1; ++k) {
-            const uint64_t key = L1[k * kLanes + n];
-            if (cnt == TK && key <= thr) break;
-            list_insert<TK>(L, n, key, cnt, thr);
-          }
+          ulonglong2* dst = reinterpret_cast<ulonglong2*>(
+              a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
+#pragma unroll
+          for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
         }
-        const int first = cta_of(preq, total, gridDim.x);
-        const int last = cta_of(preq + nb - 1, total, gridDim.x);
-        int32_t* out = a.ids + my_h * a.i_head + row * a.i_row;
-        int nseg = 0;
-        for (int cc = first; cc <= last; ++cc) nseg += share_nonempty(cc, total, gridDim.x);
-        if (nseg == 1) {
-          if (n < R) finalize_row(a, L, n, cnt, c, out);
-        } else {
-          const int slot_stride = kLanes * TK;
-          if (n < R) {
-            uint64_t* dst = a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK;
-            for (int k = 0; k < TK; ++k) dst[k] = k < cnt ? L[k * kLanes + n] : 0ull;
-          }
-          __threadfence();
-          __syncwarp();
-          int is_last = 0;
-          if (lane == 0) {
-            const int old = atomicAdd(a.counters + req, 1);
-            is_last = old == nseg - 1;
-            if (is_last) a.counters[req] = 0;
-          }
-          if (__shfl_sync(0xffffffffu, is_last, 0)) {
-            __threadfence();
+        // One round trip publishes the slot and tells whether this CTA is the
+        // last of the request (the warp barrier orders the lanes' stores
+        // before lane 0's release).
+        __syncwarp();
+        int is_last = 0;
+        if (lane == 0) {
+          const int old = atomic_add_acq_rel_gpu(a.counters + req, 1);
+          is_last = old == nseg - 1;
+          if (is_last) a.counters[req] = 0;
+        }
+        write_rows = __shfl_sync(0xffffffffu, is_last, 0) != 0;
+        if (write_rows) {
+          // Stage every slot's rows 0..R-1 (contiguous in a slot) in shared
+          // memory with one burst of independent 16-byte loads per batch,
+          // then fold them lane by lane.
+          ulonglong2* stage = reinterpret_cast<ulonglong2*>(H0);  // H0 and H1 are adjacent
+          constexpr int kU = TK / 2;                       // units per lane per burst
+          const int units = R * TK / 2;                    // 16-byte units per slot (<= 32 * kU)
+          const int per_batch = (32 * kU) / units;         // slots per burst; fits in H0+H1
+          list.clear();
+          for (int j0 = 0; j0 < nseg; j0 += per_batch) {
+            const int nj = min(per_batch, nseg - j0);
+            ulonglong2 v[kU];
+#pragma unroll
+            for (int t = 0; t < kU; ++t) {
+              const int u = lane + 32 * t;
+              v[t] = make_ulonglong2(0ull, 0ull);
+              if (u < nj * units) {
+                const int j = j0 + u / units;
+                const int cj = dense ? first + j : cta_of(preq + j, total, gridDim.x);
+                v[t] = __ldcg(reinterpret_cast<const ulonglong2*>(
+                                  a.partials + (static_cast<int64_t>(cj) + req) * slot_stride) +
+                              (u % units));
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int t = 0; t < kU; ++t)
+              if (lane + 32 * t < nj * units) stage[lane + 32 * t] = v[t];
+            __syncwarp();
             if (n < R) {
-              cnt = 0;
-              thr = 0;
-              for (int s = first; s <= last; ++s) {
-                if (!share_nonempty(s, total, gridDim.x)) continue;
-                const uint64_t* src =
-                    a.partials + (static_cast<int64_t>(s) + req) * slot_stride + n * TK;
+              for (int j = 0; j < nj; ++j) {
+                const uint64_t* src = reinterpret_cast<const uint64_t*>(stage) + (j * R + n) * TK;
                 for (int k = 0; k < TK; ++k) {
-                  const uint64_t key = __ldcg(src + k);
-                  if (key == 0ull || (cnt == TK && key <= thr)) break;
-                  list_insert<TK>(L, n, key, cnt, thr);
+                  const uint64_t key = src[k];
+                  if (key <= list.floor()) break;
+                  list.insert(key);
                 }
               }
-              finalize_row(a, L, n, cnt, c, out);
             }
+            __syncwarp();
           }
         }
       }
-      // The other warp may reuse its list only after the fold above.
-      named_barrier_sync(1, 64);
+      if (write_rows) {
+        if (n < R) list.store_cols(H0, n);
+        __syncwarp();
+        const int qpos0 = req_len(a, req) - a.query_len;  // position of query 0
+        for (int rr = 0; rr < R; ++rr) {
+          const int j = rr / a.heads, h = rr - j * a.heads;
+          const int pr = qpos0 + j;
+          const int cr = pr >= 0 ? (pr >> 7) : -1;
+          const uint64_t mine = lane < TK ? H0[lane * kLanes + rr] : 0ull;
+          warp_write_row(cr, a.init_blocks, a.local_blocks, a.topk, mine,
+                         a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row,
+                         lane);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&h_empty[hs]);
+      ++seg;
     }
-    if (ok && e == 0) {
+    if (ok) {
       // Requests with no blocks at all appear in no share: spread them over CTAs.
       for (int i = blockIdx.x; i < a.num_reqs; i += gridDim.x) {
         if (req_blocks(a, i) != 0) continue;
@@ -658,49 +737,51 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
         }
       }
     }
-  } else if (FP4 && warp >= kDeqWarp0) {
+  } else if constexpr (FP4) {
     // ---------------------------------------------------- NVFP4 dequantiser
-    const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..127
-    uint32_t it = 0;
-    bool ok = true;
-    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      for (int b = b0; b < b1; ++b) {
-        const uint32_t rs = it % RS, rr = it / RS;
-        const uint32_t st = it % S, sr = it / S;
-        bool got = true;
-        if (lane == 0) {
-          got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
-          if (got && sr > 0) got = mbar_wait(&empty[st], (sr - 1) & 1, abort_flag);
+    if (warp >= kDeqWarp0) {  // warp 3 has no role
+      const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..127 (warps 5..8)
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && walker.next(a, req, b0, b1, nb, preq)) {
+        for (int b = b0; b < b1; ++b) {
+          const uint32_t rs = it % RS, rr = it / RS;
+          const uint32_t st = it % S, sr = it / S;
+          bool got = true;
+          if (lane == 0) {
+            got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
+            if (got && sr > 0) got = mbar_wait(&empty[st], (sr - 1) & 1, abort_flag);
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* codes = sRaw + rs * kFp4RawBytes;
+          const uint8_t* scales = codes + kFp4CodeBytes;
+          uint8_t* tile = sA + st * kTileBytes;
+  #pragma unroll 2
+          for (int kk = 0; kk < 8; ++kk) {
+            const int item = kk * 128 + dq;
+            const int tok = item >> 3, g = item & 7;
+            const uint2 cw = *reinterpret_cast<const uint2*>(codes + tok * 64 + g * 8);
+            const uint4 t = sTab[scales[tok * 8 + g]];
+            uint32_t o0[4], o1[4];
+            dequant8(cw.x, t, o0);
+            dequant8(cw.y, t, o1);
+            uint8_t* rowp = tile + (g >> 2) * (kTileBytes / 2) + (tok >> 3) * 1024 + (tok & 7) * 128;
+            const int c0 = (g & 3) * 2;
+            *reinterpret_cast<uint4*>(rowp + ((c0 ^ (tok & 7)) << 4)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (tok & 7)) << 4)) =
+                make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&full[st]);
+            mbar_arrive(&raw_empty[rs]);
+          }
+          ++it;
         }
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* codes = sRaw + rs * kFp4RawBytes;
-        const uint8_t* scales = codes + kFp4CodeBytes;
-        uint8_t* tile = sA + st * kTileBytes;
-#pragma unroll 2
-        for (int kk = 0; kk < 8; ++kk) {
-          const int item = kk * 128 + dq;
-          const int tok = item >> 3, g = item & 7;
-          const uint2 cw = *reinterpret_cast<const uint2*>(codes + tok * 64 + g * 8);
-          const uint4 t = sTab[scales[tok * 8 + g]];
-          uint32_t o0[4], o1[4];
-          dequant8(cw.x, t, o0);
-          dequant8(cw.y, t, o1);
-          uint8_t* rowp = tile + (g >> 2) * (kTileBytes / 2) + (tok >> 3) * 1024 + (tok & 7) * 128;
-          const int c0 = (g & 3) * 2;
-          *reinterpret_cast<uint4*>(rowp + ((c0 ^ (tok & 7)) << 4)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-          *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (tok & 7)) << 4)) =
-              make_uint4(o1[0], o1[1], o1[2], o1[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&full[st]);
-          mbar_arrive(&raw_empty[rs]);
-        }
-        ++it;
       }
     }
   }

@@ -16,9 +16,12 @@
 //                boxes, 128-byte swizzle, from a 3-D map over
 //                [tokens, heads, 128]) once per tile, and each key page (from
 //                a 2-D map over [pages*128, 128]) into a 4-stage ring.
-//   * warp 1   : one thread issues tcgen05.mma, M = 128 query rows,
-//                N = 128 key tokens, K = 128, into one of four 128-column fp32
-//                TMEM accumulators (all 512 columns).
+//   * warp 1   : one thread copies each query tile into TMEM once
+//                (tcgen05.cp) and issues tcgen05.mma with A (M = 128 query
+//                rows) read from TMEM and B (N = 128 key tokens) from shared
+//                memory, K = 128, into one of three 128-column fp32 TMEM
+//                accumulators.  Reading only B from shared memory keeps the
+//                operand traffic well inside shared-memory bandwidth.
 //   * warps 2-9: epilogue, two teams of four warps taking alternate units:
 //                tcgen05.ld of the thread's query row (128 fp32 columns),
 //                causal mask only on diagonal blocks, row max with 3-input
@@ -32,17 +35,22 @@
 namespace mm3idx {
 namespace {
 
+// The query tile is the MMA's A operand.  It is TMA-loaded into shared
+// memory and, when kQInTmem, copied once per tile into TMEM (two 64-column
+// buffers) so that every MMA reads only the key page from shared memory.
+constexpr bool kQInTmem = true;
 constexpr int kStages = 4;
-constexpr int kAcc = 4;
+constexpr int kAcc = kQInTmem ? 3 : 4;
+constexpr uint32_t kAccCol0 = kQInTmem ? 128 : 0;  // first accumulator column
 constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kThreads = 320;
 constexpr int oQ = 0;
 constexpr int oK = oQ + 2 * kTile;
 constexpr int oBar = oK + kStages * kTile;
-constexpr int kBars = 2 * kStages + 2 * kAcc + 4 + 1;
+constexpr int kBars = 2 * kStages + 2 * kAcc + 6 + 1;
 constexpr int oMisc = oBar + kBars * 8;
 constexpr int kSmem = oMisc + 64 + 1024;
-constexpr uint32_t kTmemCols = kAcc * 128;
+constexpr uint32_t kTmemCols = 512;
 
 struct Misc {
   uint32_t tmem;
@@ -114,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + kAcc;
   uint64_t* q_full = acc_empty + kAcc;
   uint64_t* q_empty = q_full + 2;
-  uint64_t* done_bar = q_empty + 2;
+  uint64_t* qtm_free = q_empty + 2;   // TMEM query buffer free again
+  uint64_t* done_bar = qtm_free + 2;
   Misc* misc = reinterpret_cast<Misc*>(sm + oMisc);
   volatile int* abort_flag = &misc->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
+      mbar_init(&qtm_free[s], 1);
     }
     mbar_init(done_bar, 1);
     misc->abort = 0;
@@ -209,19 +219,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cur_rh = -1, cur_qt = -1;
       uint32_t tq = 0, it = 0;
       bool ok = true;
-      uint32_t qaddr = 0;
+      uint32_t qaddr = 0, qtm = 0;
       for (; ok && U.valid(); U.advance(a)) {
         const int req = U.rh / a.heads;
         const int prefix = clamp_len(a, req) - a.query_len;
         if (U.b >= tile_blocks(prefix, U.qt, a.query_len)) continue;
         if (U.rh != cur_rh || U.qt != cur_qt) {
-          if (tq > 0) mma_commit(&q_empty[(tq - 1) & 1]);
+          if (tq > 0) mma_commit(kQInTmem ? &qtm_free[(tq - 1) & 1] : &q_empty[(tq - 1) & 1]);
           cur_rh = U.rh;
           cur_qt = U.qt;
           const int qs = tq & 1;
           ok = mbar_wait(&q_full[qs], (tq >> 1) & 1, abort_flag);
           if (!ok) break;
           qaddr = smem_u32(sQ + qs * kTile);
+          if constexpr (kQInTmem) {
+            // The MMAs of tile tq-2 read this TMEM buffer; let them finish.
+            if (tq >= 2) ok = mbar_wait(&qtm_free[qs], ((tq >> 1) - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            qtm = tmem_base + qs * 64;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tmem_cp_128x256b(qtm + k * 8,
+                               sdesc_kmajor_sw128(qaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32));
+            mma_commit(&q_empty[qs]);   // the shared-memory tile is free once copied
+          }
           ++tq;
         }
         const uint32_t st = it % kStages, rnd = it / kStages;
@@ -232,18 +254,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t kaddr = smem_u32(sK + st * kTile);
-        const uint32_t d = tmem_base + ab * 128;
+        const uint32_t d = tmem_base + kAccCol0 + ab * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32);
           const uint64_t bd = sdesc_kmajor_sw128(kaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32);
-          mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+          if constexpr (kQInTmem) {
+            mma_bf16_ts(d, qtm + k * 8, bd, idesc, k > 0 ? 1u : 0u);
+          } else {
+            const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32);
+            mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
         }
         mma_commit(&empty[st]);
         mma_commit(&acc_full[ab]);
         ++it;
       }
-      if (ok && tq > 0) mma_commit(&q_empty[(tq - 1) & 1]);
+      if (ok && tq > 0 && !kQInTmem) mma_commit(&q_empty[(tq - 1) & 1]);
       mma_commit(done_bar);
       int dummy = 0;
       mbar_wait(done_bar, 0, &dummy);
@@ -277,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * 128;
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol0 + ab * 128;
         const int lim = pos - U.b * 128;  // columns 0..lim are visible
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll

@@ -199,6 +199,24 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16 bf16) is read from TMEM, lane m
+// holding row m as 8 columns of packed bf16 pairs.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 128-row x 256-bit block described by an shared-memory matrix
+// descriptor into TMEM lanes 0..127, 8 columns starting at taddr.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -262,6 +280,15 @@ __device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld_wait32x2(uint32_t (&r)[32], uint32_t (&w)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r) : : "memory");
   asm volatile("" : MM3IDX_PLUS32(w) : : "memory");
+}
+
+// Fetch-and-add with acquire-release semantics at GPU scope: orders this
+// thread's earlier writes (and those it has observed) before the add, and the
+// writes released by earlier adds before this thread's later reads.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 // --------------------------------------------------------------- misc helpers

@@ -17,19 +17,13 @@
 #include "../../include/mm3idx.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "warp_select.cuh"
 
 namespace mm3idx {
 namespace {
 
 constexpr int kPerLane = 8;
 constexpr int kWarpsPerBlock = 8;
-
-__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
-  const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(k >> 32));
-  const uint32_t lo = __reduce_max_sync(
-      0xffffffffu, static_cast<uint32_t>(k >> 32) == hi ? static_cast<uint32_t>(k) : 0u);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) select_kernel(const SelectArgs a) {
   const int lane = threadIdx.x & 31;
@@ -47,65 +41,27 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) select_kernel(const Selec
     const int c = pos >= 0 ? (pos >> 7) : -1;
     int32_t* out = a.ids + h * a.i_head + row * a.i_row;
     const int topk = a.topk;
-    if (c < 0) {
-      for (int k = lane; k < topk; k += 32) out[k] = -1;
-      continue;
-    }
-    const int f_lo = min(a.init_blocks, c + 1);
-    const int l_lo = max(f_lo, c - a.local_blocks + 1);
-    const int nf = f_lo + (c + 1 - l_lo);
-    const int m = topk - nf;
-    const int ncand = l_lo - f_lo;
-    if (ncand <= m) {
-      for (int k = lane; k < topk; k += 32) out[k] = k <= c ? k : -1;
-      continue;
-    }
-    const float* srow = a.score + h * a.s_head + row * a.s_row;
+    const Forced F(c, a.init_blocks, a.local_blocks);
+    const int m = topk - F.nf;
     uint64_t mine = 0;  // lane r < m holds the r-th best key so far
-    uint64_t thr = 0;   // m-th best so far, 0 while fewer than m are known
-    for (int base = f_lo; base < l_lo; base += 32 * kPerLane) {
-      uint64_t k[kPerLane];
-      bool any = false;
+    if (c >= 0 && F.l_lo - F.f_lo > m) {
+      const float* srow = a.score + h * a.s_head + row * a.s_row;
+      uint64_t thr = 0;
+      for (int base = F.f_lo; base < F.l_lo; base += 32 * kPerLane) {
+        uint64_t k[kPerLane];
 #pragma unroll
-      for (int p = 0; p < kPerLane; ++p) {
-        const int idx = base + p * 32 + lane;
-        k[p] = 0;
-        if (idx < l_lo) {
-          const uint64_t key = make_key(__ldg(srow + idx), idx);
-          if (key > thr) k[p] = key;
+        for (int p = 0; p < kPerLane; ++p) {
+          const int idx = base + p * 32 + lane;
+          k[p] = idx < F.l_lo ? make_key(__ldg(srow + idx), idx) : 0ull;
         }
-        any |= k[p] != 0;
+        warp_topm_merge<kPerLane>(k, m, mine, thr, lane);
       }
-      if (!__any_sync(0xffffffffu, any)) continue;
-      bool list_taken = false;
-      uint64_t next = 0;
-      for (int r = 0; r < m; ++r) {
-        uint64_t best = list_taken ? 0ull : mine;
-#pragma unroll
-        for (int p = 0; p < kPerLane; ++p) best = k[p] > best ? k[p] : best;
-        const uint64_t win = warp_max_key(best);
-        if (win == 0) break;
-        if (lane == r) next = win;
-        if (best == win) {
-          if (!list_taken && mine == win) {
-            list_taken = true;
-          } else {
-#pragma unroll
-            for (int p = 0; p < kPerLane; ++p)
-              if (k[p] == win) k[p] = 0;
-          }
-        }
-      }
-      mine = next;
-      thr = __shfl_sync(0xffffffffu, mine, m - 1);
+    } else if (c >= 0) {
+      // At most m candidates: take them all (any order; the writer sorts).
+      const int idx = F.f_lo + lane;
+      mine = (lane < m && idx < F.l_lo) ? make_key(0.f, idx) : 0ull;
     }
-    // Output: forced blocks around the picks, picks in ascending id order.
-    const int bx = lane < m ? key_block(mine) : 0x7fffffff;
-    int rank = 0;
-    for (int q = 0; q < m; ++q) rank += __shfl_sync(0xffffffffu, bx, q) < bx;
-    if (lane < m) out[f_lo + rank] = bx;
-    for (int b = lane; b < f_lo; b += 32) out[b] = b;
-    for (int b = l_lo + lane; b <= c; b += 32) out[f_lo + m + (b - l_lo)] = b;
+    warp_write_row(c, a.init_blocks, a.local_blocks, topk, mine, out, lane);
   }
 }
 
