@@ -148,8 +148,9 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
 
 /*
  * mm3idx_workspace_bytes -- device workspace the fused calls need.
- * op = MM3IDX_OP_DECODE: per-request completion counters plus partial top-k
- * candidate lists (depends on the current device's SM count).
+ * op = MM3IDX_OP_DECODE: request start offsets plus the partial top-k
+ * candidate lists of requests split across CTAs (depends on the current
+ * device's SM count).
  * op = MM3IDX_OP_PREFILL: the fp32 score scratch [heads, rows, roundup(cdiv(max_seq_len,128), 4)].
  * Writes the size to *bytes.  Reads the current device's attributes; no
  * allocation.
@@ -159,15 +160,17 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs,
                            int32_t topk, size_t *bytes);
 
 /*
- * mm3idx_decode -- fused decode: block scores and top-k in one persistent
- * kernel; the fp32 score row never goes to HBM (index_topk,
+ * mm3idx_decode -- fused decode: block scores and top-k selection in one
+ * persistent kernel; the fp32 score row never goes to HBM (index_topk,
  * minimax_m3_index_decode).  Requires heads * query_len <= 32.
  *
  * out: int32 [h, row, k] at out[h*out_head_stride + row*out_row_stride + k].
  * workspace: >= mm3idx_workspace_bytes(MM3IDX_OP_DECODE, ...) bytes, 256-byte
- * aligned, zero-filled by the caller once before its first use (the
- * completion counters must start at zero); every completed launch leaves the
- * counters at zero again.  Launches that share a workspace must not overlap.
+ * aligned; no initialisation needed and no state is kept in it between
+ * calls.  Requests longer than one CTA's share of the batch leave at most
+ * topk candidate keys per row per CTA there, which a second, small kernel
+ * (a programmatic dependent launch on the same stream) merges.  Launches
+ * that share a workspace must not overlap.
  */
 int mm3idx_decode(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
                   int32_t local_blocks, int32_t *out, int64_t out_head_stride,

@@ -181,9 +181,10 @@ def workspace_bytes(op: int, heads: int, num_reqs: int, query_len: int, max_seq_
 
 
 def new_workspace(op, heads, num_reqs, query_len, max_seq_len, topk, device=None):
-    """A zero-filled workspace (uint8, 256-byte aligned by the caching allocator)."""
+    """A workspace for :func:`decode` / :func:`prefill` (uint8, 256-byte
+    aligned by the caching allocator; needs no initialisation)."""
     n = workspace_bytes(op, heads, num_reqs, query_len, max_seq_len, topk)
-    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def score(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, sm_scale,
@@ -245,8 +246,8 @@ def _fused(fn, name, op, idx_q, cache, block_table, seq_lens, scales, nvfp4, que
 
 def decode(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
            init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
-    """Fused decode score + top-k (heads * query_len <= 32).  ``workspace`` must
-    come from :func:`new_workspace` (zeroed once, reused across calls)."""
+    """Fused decode score + top-k (heads * query_len <= 32).  ``workspace``
+    (from :func:`new_workspace`) may be reused across calls."""
     return _fused(lib.mm3idx_decode, "mm3idx_decode", OP_DECODE, idx_q, index_cache, block_table,
                   seq_lens, None, False, query_len, max_seq_len, topk, init_blocks, local_blocks,
                   sm_scale, out, workspace, stream)

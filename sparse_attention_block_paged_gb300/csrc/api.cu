@@ -143,12 +143,17 @@ bool out_ok(int64_t head_stride, int64_t row_stride, int32_t heads, int64_t rows
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MM3IDX_OK : MM3IDX_ERR_CUDA; }
 
+// Decode workspace: [total blocks: 256 B][request starts: num_reqs x 8 B,
+// 256-aligned][partial lists: (grid + num_reqs) slots x 32 rows x tk keys].
+size_t decode_ws_head(int32_t num_reqs) {
+  return 256 + (static_cast<size_t>(num_reqs) * 8 + 255) / 256 * 256;
+}
+
 size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len, int32_t topk) {
-  const int R = heads * query_len;
-  const size_t counters = (static_cast<size_t>(num_reqs) * 4 + 255) / 256 * 256;
+  (void)heads;
+  (void)query_len;
   const size_t slots = static_cast<size_t>(sms) * decode_ctas_per_sm() + num_reqs;
-  (void)R;
-  return counters + slots * 32 * decode_tk(topk) * 8;  // [slot][32 rows][tk keys]
+  return decode_ws_head(num_reqs) + slots * 32 * decode_tk(topk) * 8;
 }
 
 size_t prefill_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len, int32_t max_seq_len) {
@@ -207,19 +212,24 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   a.ids = out;
   a.i_head = out_head_stride;
   a.i_row = out_row_stride;
-  a.counters = static_cast<int32_t*>(workspace);
-  a.partials = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) +
-                                           (static_cast<size_t>(p->num_reqs) * 4 + 255) / 256 * 256);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.total_blocks = reinterpret_cast<long long*>(ws);
+  a.req_start = reinterpret_cast<long long*>(ws + 256);
+  a.partials = reinterpret_cast<uint64_t*>(ws + decode_ws_head(p->num_reqs));
   const int grid = decode_grid(p, dev->sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
   if (nvfp4) {
     a.codes = static_cast<const uint8_t*>(p->index_cache);
     a.scales = static_cast<const uint8_t*>(p->index_scales);
-    return cuda_status(launch_decode_nvfp4(a, grid, s));
+    e = launch_decode_nvfp4(a, grid, s);
+  } else {
+    CUtensorMap kmap;
+    if ((rc = make_kmap(p, &kmap))) return rc;
+    e = launch_decode_bf16(kmap, a, grid, s);
   }
-  CUtensorMap kmap;
-  if ((rc = make_kmap(p, &kmap))) return rc;
-  return cuda_status(launch_decode_bf16(kmap, a, grid, s));
+  if (e != cudaSuccess) return MM3IDX_ERR_CUDA;
+  return cuda_status(launch_decode_merge(a, grid, s));
 }
 
 int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, int64_t row_stride,

@@ -5,8 +5,8 @@
 //
 // What it computes follows the vLLM MiniMax-M3 "index_topk" page
 // (module docstring; minimax_m3_index_decode: fused decode score + adaptive
-// top-k, ids 0-indexed with -1 pad, completion counters that the last arriving
-// program resets) and "indexer_cp_exchange" (forced init/local blocks are
+// top-k with a final merge of per-chunk partial top-k lists, ids 0-indexed
+// with -1 pad) and "indexer_cp_exchange" (forced init/local blocks are
 // pinned, packed 64-bit candidate keys).  The design is ours:
 //
 //   * The work list is every (request, logical block) pair of the batch,
@@ -30,12 +30,12 @@
 //                kept in registers.  At a request boundary both warps hand
 //                their lists to the merge warp through shared memory and go
 //                on streaming.
-//   * warp 3   : merge warp.  Folds the two lists of each row; a request
-//                split across CTAs merges its lists in the last CTA to finish
-//                it (atomic arrival count).  Writes the ids (forced blocks
-//                re-pinned, ascending, -1 pad) and resets the counter.  Each
-//                CTA walks its two boundary requests first so these merges
-//                overlap the streaming of its interior requests.
+//   * warp 3   : merge warp.  Folds the two lists of each row and writes the
+//                ids of requests held by one CTA (forced blocks re-pinned,
+//                ascending, -1 pad); for a request split across CTAs it
+//                publishes the lists, and a small merge kernel -- launched as
+//                a programmatic dependent launch, so its start overlaps this
+//                grid -- merges every split request once this grid is done.
 //
 // Every wait is bounded (ptx.cuh).  A wait that gives up raises an abort flag
 // shared by the CTA's roles and the MM3IDX_DEV_TIMEOUT status bit.
@@ -193,6 +193,11 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
       }
     }
     const unsigned hitl = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > hi - 1);
+    // Record where each request this share touches starts (several CTAs may
+    // write the same value); the merge kernel reads it.
+    const int il_here = hitl ? b + __ffs(hitl) - 1 : a.num_reqs;
+    if (a.req_start && !need0 && i >= i0 && i <= il_here && i < a.num_reqs)
+      a.req_start[i] = P + incl - nb;
     if (hitl) {
       const int k = __ffs(hitl) - 1;
       il = b + k;
@@ -202,6 +207,7 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
     P += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) {
+    if (a.total_blocks && blockIdx.x == 0) *a.total_blocks = total;
     m->lo = lo;
     m->hi = hi;
     m->total = total;
@@ -260,12 +266,77 @@ struct RegList {
   __device__ __forceinline__ void offer(uint64_t key) {
     if (key > floor()) insert(key);
   }
+  // Replace the list by the best TK keys of itself and `b` (b sorted
+  // descending): the elementwise max of the list and reversed b holds exactly
+  // those keys as a bitonic sequence, which a bitonic sort orders again.
+  __device__ __forceinline__ void merge_sorted(const uint64_t (&b)[TK]) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) v[k] = v[k] > b[TK - 1 - k] ? v[k] : b[TK - 1 - k];
+#pragma unroll
+    for (int half = TK / 2; half > 0; half >>= 1) {
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        if ((k & half) == 0) {
+          const uint64_t x = v[k], y = v[k + half];
+          v[k] = x > y ? x : y;
+          v[k + half] = x > y ? y : x;
+        }
+      }
+    }
+  }
   // Row-major store to a [k][kLanes] shared-memory table at column n.
   __device__ __forceinline__ void store_cols(uint64_t* t, int n) const {
 #pragma unroll
     for (int k = 0; k < TK; ++k) t[k * kLanes + n] = v[k];
   }
 };
+
+// One thread writes one output row from its candidate list (keys sorted
+// descending, 0 = none): forced blocks [0, f_lo) and [l_lo, c] around the best
+// topk - |forced| picks, picks in ascending id order, then -1.
+template <int TK>
+__device__ __forceinline__ void write_row_lane(const uint64_t (&v)[TK], int c, int init_blocks,
+                                               int local_blocks, int topk, int32_t* out) {
+  if (c < 0) {
+    for (int k = 0; k < topk; ++k) out[k] = -1;
+    return;
+  }
+  const Forced F(c, init_blocks, local_blocks);
+  const int m = topk - F.nf;
+  int id[TK];
+  int npick = 0;
+#pragma unroll
+  for (int k = 0; k < TK; ++k) {
+    const bool take = k < m && v[k] != 0ull;
+    id[k] = take ? key_block(v[k]) : 0x7fffffff;
+    npick += take;
+  }
+  // Bitonic sort of the ids, ascending (absent picks sort to the end).
+#pragma unroll
+  for (int size = 2; size <= TK; size <<= 1) {
+#pragma unroll
+    for (int stride = size / 2; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        const int l = k ^ stride;
+        if (l > k) {
+          const bool up = (k & size) == 0;
+          const int x = id[k], y = id[l];
+          id[k] = (x < y) == up ? x : y;
+          id[l] = (x < y) == up ? y : x;
+        }
+      }
+    }
+  }
+  int o = 0;
+  for (int b = 0; b < F.f_lo; ++b) out[o++] = b;
+#pragma unroll
+  for (int k = 0; k < TK; ++k)
+    if (k < npick) out[o + k] = id[k];
+  o += npick;
+  for (int b = F.l_lo; b <= c; ++b) out[o++] = b;
+  for (; o < topk; ++o) out[o] = -1;
+}
 
 // Row max of one 128-column accumulator row (this lane's TMEM lane), with the
 // columns past `lim` left out when lim < 127.
@@ -375,6 +446,8 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   volatile int* abort_flag = &misc->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The merge kernel may be scheduled now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -428,10 +501,17 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
       const int slot = seg & 1;
       if (seg >= 2) ok = warp_wait(&q_empty[slot], ((seg >> 1) - 1) & 1, abort_flag);
       if (!ok) break;
-      load_q_tile<MQ>(a, req, sQ + slot * C::kQBytes, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[slot]);
+      // The query tile is written just before the first wait that could
+      // block (stages are only freed by MMAs, which need the tile), so page
+      // loads into free stages are already in flight meanwhile.
+      bool q_pending = true;
+      auto put_q = [&]() {
+        load_q_tile<MQ>(a, req, sQ + slot * C::kQBytes, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[slot]);
+        q_pending = false;
+      };
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
       for (int bc = b0; bc < b1 && ok; bc += 32) {
         const int mine = bc + lane;
@@ -442,6 +522,7 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
           const bool good = page >= 0 && page < a.num_pages;
           if constexpr (!FP4) {
             const uint32_t st = it % S, rnd = it / S;
+            if (rnd > 0 && q_pending) put_q();
             if (rnd > 0) ok = warp_wait(&empty[st], (rnd - 1) & 1, abort_flag);
             if (!ok) break;
             if (lane == 0) {
@@ -457,6 +538,7 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
             }
           } else {
             const uint32_t st = it % RS, rnd = it / RS;
+            if (rnd > 0 && q_pending) put_q();
             if (rnd > 0) ok = warp_wait(&raw_empty[st], (rnd - 1) & 1, abort_flag);
             if (!ok) break;
             if (lane == 0) {
@@ -478,6 +560,7 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
           ++it;
         }
       }
+      if (q_pending) put_q();
       ++seg;
     }
     // Let every copy this warp started land before the CTA can exit.
@@ -600,13 +683,11 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     // ------------------------------------------------------------ merge warp
     // Per request (in the walker's order): fold the two epilogue warps'
     // lists row by row (lane n owns row n).  A request held by one CTA is
-    // written here; otherwise each row's list goes to this CTA's partial slot
-    // and the last CTA to finish the request folds all slots the same way
-    // (each slot's list is sorted, so a key at or below the running floor
-    // ends it).  With total >= grid every share is non-empty, so the
-    // request's CTAs are first..last; with fewer blocks than CTAs every
-    // non-empty share is a single block, so block k sits in cta_of(preq + k).
-    // Rows are written by the whole warp, one row at a time.
+    // written here, one row at a time by the whole warp; otherwise each row's
+    // list goes to this CTA's partial slot for the merge kernel.  With
+    // total >= grid every share is non-empty, so the request's CTAs are
+    // first..last; with fewer blocks than CTAs every non-empty share is a
+    // single block, so block k sits in cta_of(preq + k).
     const int n = lane;
     const int R = a.rows_per_req;
     const bool select = a.mode == kModeSelect;
@@ -623,94 +704,36 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
       RegList<TK> list;
       list.clear();
       if (n < R) {
+        uint64_t other[TK];
 #pragma unroll
-        for (int k = 0; k < TK; ++k) list.v[k] = H0[k * kLanes + n];
         for (int k = 0; k < TK; ++k) {
-          const uint64_t key = H1[k * kLanes + n];
-          if (key <= list.floor()) break;
-          list.insert(key);
+          list.v[k] = H0[k * kLanes + n];
+          other[k] = H1[k * kLanes + n];
         }
+        list.merge_sorted(other);
       }
       const int first = cta_of(preq, total, gridDim.x);
       const int last = cta_of(preq + nb - 1, total, gridDim.x);
       const bool dense = total >= gridDim.x;
       const int nseg = dense ? last - first + 1 : nb;
-      bool write_rows = nseg == 1;
-      if (!write_rows) {
+      const bool write_rows = nseg == 1;
+      if (!write_rows && n < R) {
+        // Split request: publish this CTA's lists; the merge kernel folds
+        // the request's slots after this grid completes.
         const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
-        if (n < R) {
-          ulonglong2* dst = reinterpret_cast<ulonglong2*>(
-              a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
+        ulonglong2* dst = reinterpret_cast<ulonglong2*>(
+            a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
 #pragma unroll
-          for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
-        }
-        // One round trip publishes the slot and tells whether this CTA is the
-        // last of the request (the warp barrier orders the lanes' stores
-        // before lane 0's release).
-        __syncwarp();
-        int is_last = 0;
-        if (lane == 0) {
-          const int old = atomic_add_acq_rel_gpu(a.counters + req, 1);
-          is_last = old == nseg - 1;
-          if (is_last) a.counters[req] = 0;
-        }
-        write_rows = __shfl_sync(0xffffffffu, is_last, 0) != 0;
-        if (write_rows) {
-          // Stage every slot's rows 0..R-1 (contiguous in a slot) in shared
-          // memory with one burst of independent 16-byte loads per batch,
-          // then fold them lane by lane.
-          ulonglong2* stage = reinterpret_cast<ulonglong2*>(H0);  // H0 and H1 are adjacent
-          constexpr int kU = TK / 2;                       // units per lane per burst
-          const int units = R * TK / 2;                    // 16-byte units per slot (<= 32 * kU)
-          const int per_batch = (32 * kU) / units;         // slots per burst; fits in H0+H1
-          list.clear();
-          for (int j0 = 0; j0 < nseg; j0 += per_batch) {
-            const int nj = min(per_batch, nseg - j0);
-            ulonglong2 v[kU];
-#pragma unroll
-            for (int t = 0; t < kU; ++t) {
-              const int u = lane + 32 * t;
-              v[t] = make_ulonglong2(0ull, 0ull);
-              if (u < nj * units) {
-                const int j = j0 + u / units;
-                const int cj = dense ? first + j : cta_of(preq + j, total, gridDim.x);
-                v[t] = __ldcg(reinterpret_cast<const ulonglong2*>(
-                                  a.partials + (static_cast<int64_t>(cj) + req) * slot_stride) +
-                              (u % units));
-              }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int t = 0; t < kU; ++t)
-              if (lane + 32 * t < nj * units) stage[lane + 32 * t] = v[t];
-            __syncwarp();
-            if (n < R) {
-              for (int j = 0; j < nj; ++j) {
-                const uint64_t* src = reinterpret_cast<const uint64_t*>(stage) + (j * R + n) * TK;
-                for (int k = 0; k < TK; ++k) {
-                  const uint64_t key = src[k];
-                  if (key <= list.floor()) break;
-                  list.insert(key);
-                }
-              }
-            }
-            __syncwarp();
-          }
-        }
+        for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
       }
-      if (write_rows) {
-        if (n < R) list.store_cols(H0, n);
-        __syncwarp();
-        const int qpos0 = req_len(a, req) - a.query_len;  // position of query 0
-        for (int rr = 0; rr < R; ++rr) {
-          const int j = rr / a.heads, h = rr - j * a.heads;
-          const int pr = qpos0 + j;
-          const int cr = pr >= 0 ? (pr >> 7) : -1;
-          const uint64_t mine = lane < TK ? H0[lane * kLanes + rr] : 0ull;
-          warp_write_row(cr, a.init_blocks, a.local_blocks, a.topk, mine,
-                         a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row,
-                         lane);
-        }
+      if (write_rows && n < R) {
+        // Lane n writes row n: forced blocks, the best picks in ascending id
+        // order (a sorting network over the TK candidate ids), then -1.
+        const int j = n / a.heads, h = n - j * a.heads;
+        const int pr = req_len(a, req) - a.query_len + j;
+        const int cr = pr >= 0 ? (pr >> 7) : -1;
+        int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
+        write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&h_empty[hs]);
@@ -795,6 +818,58 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   }
 }
 
+// One warp per request split across decode CTAs, lane n owning query row n:
+// the row's partial lists (one per CTA holding part of the request, each its
+// best TK candidate keys, sorted) are merged in registers -- the next slot's
+// keys load while the current one merges -- and the lane writes the row.
+// Requests held by one CTA were written by the decode kernel.
+template <int TK>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a, int grid) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int req = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (req >= a.num_reqs || lane >= a.rows_per_req) return;
+  const int nb = req_blocks(a, req);
+  if (nb == 0) return;
+  const long long total = __ldcg(a.total_blocks);
+  const long long preq = __ldcg(a.req_start + req);
+  const int first = cta_of(preq, total, grid);
+  const int last = cta_of(preq + nb - 1, total, grid);
+  const bool dense = total >= grid;
+  const int nseg = dense ? last - first + 1 : nb;
+  if (nseg == 1) return;
+  const int n = lane;
+  const int j = n / a.heads, h = n - j * a.heads;
+  const int pr = req_len(a, req) - a.query_len + j;
+  const int cr = pr >= 0 ? (pr >> 7) : -1;
+  const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
+  auto load_slot = [&](int js, uint64_t (&k)[TK]) {
+    const int cj = dense ? first + js : cta_of(preq + js, total, grid);
+    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
+        a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + n * TK);
+#pragma unroll
+    for (int u = 0; u < TK / 2; ++u) {
+      const ulonglong2 x = __ldcg(src + u);
+      k[2 * u] = x.x;
+      k[2 * u + 1] = x.y;
+    }
+  };
+  RegList<TK> list;
+  uint64_t cur[TK], nxt[TK];
+  load_slot(0, cur);
+  load_slot(1, nxt);
+#pragma unroll
+  for (int k = 0; k < TK; ++k) list.v[k] = cur[k];
+  for (int js = 1; js < nseg; ++js) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) cur[k] = nxt[k];
+    if (js + 1 < nseg) load_slot(js + 1, nxt);   // in flight while this slot merges
+    list.merge_sorted(cur);
+  }
+  write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk,
+                     a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row);
+}
+
 template <bool FP4, int MQ, int TK>
 cudaError_t launch_t(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
   using C = Cfg<FP4, MQ, TK>;
@@ -817,6 +892,22 @@ cudaError_t dispatch(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cud
 }  // namespace
 
 int decode_ctas_per_sm() { return 1; }
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, int decode_grid, cudaStream_t s) {
+  const unsigned blocks = static_cast<unsigned>((a.num_reqs + 7) / 8);
+  if (blocks == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (decode_tk(a.topk) == 16) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<16>, a, decode_grid);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<32>, a, decode_grid);
+}
 
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
   return dispatch<false>(kmap, a, grid, s);

@@ -103,8 +103,11 @@ def test_decode_reused_workspace_and_graph_replay(mm):
         out.fill_(-7)
         mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
         check_ids(out.cpu().numpy(), want, s, wl, where="reuse")
-    # counters are back at zero after every launch
-    assert int(ws[: 4 * wl.num_reqs].view(torch.int32).abs().sum()) == 0
+    # stale contents of the workspace do not matter
+    ws.fill_(0xA5)
+    out.fill_(-7)
+    mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+    check_ids(out.cpu().numpy(), want, s, wl, where="dirty workspace")
     g = torch.cuda.CUDAGraph()
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
