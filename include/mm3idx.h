@@ -207,6 +207,34 @@ int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
  */
 int mm3idx_get_device_error(void *stream, int32_t *code);
 
+/*
+ * mm3idx_decode_static -- mm3idx_decode without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot give the library device memory: code that has no allocator at
+ * hand or is not allowed to allocate at the point of the call (for example a
+ * plug-in whose host framework plans every device buffer in advance, or a C
+ * caller that only holds the input and output pointers).  The scratch the
+ * decode needs lives instead in one array inside this library, of
+ * MM3IDX_STATIC_SCRATCH_BYTES, which every GPU that loads the library keeps
+ * until the process exits.  Nothing is allocated or freed by this call.
+ *
+ * Arguments and results are those of mm3idx_decode (bf16 cache).  A problem
+ * whose decode workspace (mm3idx_workspace_bytes with MM3IDX_OP_DECODE)
+ * exceeds MM3IDX_STATIC_SCRATCH_BYTES is rejected with
+ * MM3IDX_ERR_STATIC_SCRATCH.  The first call on a device looks up the
+ * array's device address (once per device, with that device current); make
+ * that first call before any stream capture.  All calls share the one array
+ * and it keeps the previous call's contents (the decode needs none of them
+ * cleared); calls whose executions overlap on the GPU race on it, so issue
+ * them in one stream or otherwise order them.
+ */
+#define MM3IDX_STATIC_SCRATCH_BYTES (8u << 20)  /* 8 MiB */
+#define MM3IDX_ERR_STATIC_SCRATCH   (-12)       /* problem needs more scratch than the static array */
+int mm3idx_decode_static(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
+                         int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                         int64_t out_row_stride, void *stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *mm3idx_status_string(int status);
 

@@ -32,6 +32,7 @@ OP_DECODE = 1
 OP_PREFILL = 2
 MAX_TOPK = 32
 MAX_DECODE_ROWS = 32
+STATIC_SCRATCH_BYTES = 8 << 20
 DEV_BAD_PAGE, DEV_SEQ_TOO_LONG, DEV_SEQ_TOO_SHORT, DEV_TIMEOUT = 1, 2, 4, 8
 
 
@@ -83,6 +84,9 @@ SYMBOLS = {
                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "mm3idx_get_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    "mm3idx_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
 }
 
 
@@ -268,6 +272,20 @@ def prefill(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len
     return _fused(lib.mm3idx_prefill, "mm3idx_prefill", OP_PREFILL, idx_q, index_cache,
                   block_table, seq_lens, None, False, query_len, max_seq_len, topk, init_blocks,
                   local_blocks, sm_scale, out, workspace, stream)
+
+
+def decode_static(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
+                  init_blocks, local_blocks, sm_scale, out=None, stream=None):
+    """:func:`decode` for callers that cannot provide a workspace: the library
+    uses its own fixed device array (STATIC_SCRATCH_BYTES), shared by every
+    call, so calls that overlap on the GPU must not be issued."""
+    p = _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale)
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    out = _ids_out(out, heads, rows, topk, idx_q.device)
+    _check(lib.mm3idx_decode_static(ctypes.byref(p), topk, init_blocks, local_blocks,
+                                    out.data_ptr(), out.stride(0), out.stride(1), _stream(stream)),
+           "mm3idx_decode_static")
+    return out[:, :rows, :]
 
 
 def get_device_error(stream=None) -> int:

@@ -100,6 +100,26 @@ int make_qmap(const mm3idx_problem_t* p, CUtensorMap* m) {
   return r == CUDA_SUCCESS ? MM3IDX_OK : MM3IDX_ERR_Q_LAYOUT;
 }
 
+// Scratch of mm3idx_decode_static: one array per device context, kept until
+// the process exits.  Host code may not use the symbol itself as a device
+// address; its address is looked up once per device with that device current.
+static __device__ __align__(256) uint8_t g_static_scratch[MM3IDX_STATIC_SCRATCH_BYTES];
+void* g_static_scratch_ptr[kMaxDevices];
+std::mutex g_static_mu;
+
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MM3IDX_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return MM3IDX_ERR_CUDA;
+    g_static_scratch_ptr[dev] = ptr;
+  }
+  *out = g_static_scratch_ptr[dev];
+  return MM3IDX_OK;
+}
+
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -312,6 +332,8 @@ const char* mm3idx_status_string(int status) {
     case MM3IDX_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
     case MM3IDX_ERR_UNSUPPORTED: return "shape not served by this entry point";
     case MM3IDX_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case MM3IDX_ERR_STATIC_SCRATCH:
+      return "problem needs more decode scratch than the library's static array (MM3IDX_STATIC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }
@@ -423,6 +445,24 @@ int mm3idx_prefill(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
                              p->max_seq_len, topk, init_blocks, local_blocks, out, out_head_stride,
                              out_row_stride, dev->status);
   return cuda_status(launch_select(a, dev->sms, s));
+}
+
+int mm3idx_decode_static(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                         int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                         int64_t out_row_stride, void* stream) {
+  int rc = check_problem(p, false);
+  if (rc) return rc;
+  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  if (static_cast<int64_t>(p->num_reqs) * p->query_len == 0) return MM3IDX_OK;
+  void* scratch = nullptr;
+  if ((rc = static_scratch(&scratch))) return rc;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  if (decode_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len, topk) >
+      MM3IDX_STATIC_SCRATCH_BYTES)
+    return MM3IDX_ERR_STATIC_SCRATCH;
+  return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
+                    out_row_stride, scratch, MM3IDX_STATIC_SCRATCH_BYTES, stream);
 }
 
 int mm3idx_get_device_error(void* stream, int32_t* code) {
