@@ -10,21 +10,22 @@
  *       keys (max over the block), then the top-k blocks plus forced init /
  *       local blocks are selected per query token; the KV page size equals the
  *       sparse block size (128), so one sparse block is one page; the index-K
- *       cache is [num_blocks, 128, head_dim], one key vector per token shared
- *       by every index head.
+ *       cache is [num_blocks, 128, head_dim] and each token has a single key
+ *       that all index heads read.
  *     - minimax_m3_index_decode: fused decode scoring + top-k; ids are
- *       0-indexed logical block ids padded with -1, [heads, total_q, topk];
- *       caller-owned `out` and a completion counter that must be zero before
- *       the first launch and that every completed launch resets.
+ *       logical block ids counted from 0, unused slots -1, [heads, total_q, topk];
+ *       caller-owned `out` for graph capture, and per-query partial top-k
+ *       lists merged in a final step.
  *     - minimax_m3_index_score: score [heads, total_q, max_block], each entry
- *       the max over a 128-token index-K block.
+ *       the largest token score inside a 128-token block.
  *     - minimax_m3_index_topk: top-k from a precomputed score tensor.
  *   vllm.models.minimax_m3.amd.ops.indexer_context_parallel,
  *     check_context_score_inputs / indexer_context_scores: input layout rules
  *     (bf16 [tokens, heads, 128] queries with unit d stride, contiguous
  *     non-empty [pages, 128, 128] cache, int32 tables with unit inner stride),
  *     rows = requests * query_len, table at least cdiv(max_seq_len, 128)
- *     wide, max_seq_len a capture-stable bound, sm_scale applied to scores.
+ *     wide, max_seq_len a bound that stays fixed across graph replays, sm_scale
+ *     applied to scores.
  *   vllm.models.minimax_m3.amd.ops.indexer_cp_exchange, module docstring:
  *     forced init/local blocks are pinned and never dropped; block ids must
  *     stay below 0xFFFF (local_topk_keys).
@@ -112,7 +113,7 @@ typedef struct mm3idx_problem {
     const int32_t *seq_lens;       /* int32 [num_reqs]                                      */
     int32_t        num_reqs;       /* requests, >= 0                                        */
     int32_t        query_len;      /* query tokens per request, >= 1                        */
-    int32_t        max_seq_len;    /* capture-stable bound on seq_lens (pass max_model_len) */
+    int32_t        max_seq_len;    /* bound on seq_lens fixed across graph replays (e.g. the model's max length) */
     float          sm_scale;       /* multiplies every score                                */
 } mm3idx_problem_t;
 

@@ -12,12 +12,12 @@
  *     queries score each 128-token block of index keys, taking the max over
  *     the block, then the top-k blocks plus forced init/local blocks are
  *     selected per query token; one page is one sparse block; the index-K
- *     cache is [num_blocks, 128, head_dim] with one key vector per token,
- *     shared by all index heads.
+ *     cache is [num_blocks, 128, head_dim] and each token has a single key
+ *     that all index heads read.
  *   - same page, minimax_m3_index_score docstring: the score of a visible
  *     sparse block is the max over its index-K tokens.
- *   - same page, minimax_m3_index_decode docstring: ids are 0-indexed logical
- *     block ids, padded with -1, laid out [heads, total_q, topk].
+ *   - same page, minimax_m3_index_decode docstring: ids are logical block ids
+ *     counted from 0, unused slots -1, laid out [heads, total_q, topk].
  *   - vllm.models.minimax_m3.amd.ops.indexer_cp_exchange, module docstring:
  *     forced init/local blocks are pinned so they can never be dropped.
  *   - vllm.models.minimax_m3.amd.ops.indexer_context_parallel,

@@ -3,12 +3,12 @@
 // Computes score[h, row, b] = sm_scale * max over the visible tokens of block
 // b of q[row, h] . k[token] (vLLM MiniMax-M3 "index_topk" page,
 // minimax_m3_index_score: per-token index scores for each visible sparse
-// block, the max over a 128-token index-K block, causal through the request's
+// block, i.e. the largest token score inside the block, causal through the request's
 // prefix).  The design is ours:
 //
 //   * A unit is (request, head, 128-row query tile, key block).  Units are
 //     enumerated from host-known sizes, assuming every request is
-//     max_seq_len long (a capture-stable bound); units past a request's real
+//     max_seq_len long (a bound fixed across graph replays); units past a request's real
 //     causal range do no math.  Each CTA of a persistent grid takes one
 //     contiguous, equal share of the units, so the causal triangle is spread
 //     evenly over the SMs.

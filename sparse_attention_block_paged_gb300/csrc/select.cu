@@ -3,7 +3,7 @@
 //
 // Follows the vLLM MiniMax-M3 "index_topk" page, minimax_m3_index_topk
 // (top-k from a precomputed score tensor, forced init/local blocks kept,
-// output [heads, total_q, topk] of 0-indexed block ids with -1 pad) and the
+// output [heads, total_q, topk] of logical block ids counted from 0, -1 pad) and the
 // "indexer_cp_exchange" page (packed 64-bit (score, id) keys, ids < 0xFFFF).
 //
 // Per row: forced blocks F = [0, f_lo) and [l_lo, c]; candidates are the

@@ -13,7 +13,7 @@ docstring and `minimax_m3_index_decode` argument comments):
   ``tokens = num_reqs * query_len``; query ``j`` of request ``i`` sits at
   position ``seq_len[i] - query_len + j``.
 * ``cache``  uint16 bf16 bits ``[pages, 128, 128]``: one page is one 128-token
-  sparse block, one shared key vector per token.
+  sparse block; every index head reads the same key for a token.
 * ``codes``/``scales`` (NVFP4 variant) uint8 ``[pages, 128, 64]`` with element
   ``2e`` in the low nibble and ``2e+1`` in the high nibble, and uint8
   ``[pages, 128, 8]`` e4m3 scale bytes, scale ``g`` covering ``d`` in
