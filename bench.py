@@ -41,6 +41,10 @@ METRIC = "decode score+top-k rows/s & HBM GB/s; prefill index TFLOP/s vs peak"
 HEADLINE = "spec_decode"
 BLOCK = 128
 L2_BYTES = 129 * 1024 * 1024
+# kernel sources whose hash a committed ncu summary must match for its
+# dram traffic to be reported
+DECODE_SOURCES = ["decode.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
+PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "internal.h"]
 
 
 def parse_args():
@@ -198,10 +202,10 @@ def bench_decode(mm, torch, wl, steps, warmup, flush, stream, pk, min_warm_s=0.0
               out=out, workspace=ws, stream=stream)
     if wl.kv_format == "bf16":
         fn = lambda: mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)  # noqa: E731
-        sources = ["decode.cu", "ptx.cuh", "internal.h"]
+        sources = DECODE_SOURCES
     else:
         fn = lambda: mm.decode_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"], **kw)  # noqa: E731
-        sources = ["decode.cu", "ptx.cuh", "internal.h"]
+        sources = DECODE_SOURCES
     with torch.cuda.stream(stream):
         ms = timed_steps(torch, fn, steps, warmup, flush, stream, min_warm_s)
     assert mm.get_device_error(stream) == 0, "device status word set"
@@ -269,7 +273,7 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                 roofline=dict(bound="tensor", achieved=fl / t_score / 1e12, peak=pk["bf16_tflops"],
                               unit="TFLOP/s", frac=fl / t_score / 1e12 / pk["bf16_tflops"],
                               traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
-                                                       ["prefill.cu", "ptx.cuh", "internal.h"]),
+                                                       PREFILL_SOURCES),
                               algorithmic_flops=fl,
                               peak_source=pk["source"] + " cuBLAS bf16 burst"))
 
