@@ -269,12 +269,7 @@ int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, i
   a.s_row = row_stride;
   a.fill_width = fill_width;
   a.qtiles = static_cast<int32_t>(cdiv(p->query_len, 128));
-  const int64_t wprefix = static_cast<int64_t>(p->max_seq_len) - p->query_len;
-  int64_t uph = 0;
-  for (int qt = 0; qt < a.qtiles; ++qt) {
-    const int64_t last = wprefix + std::min<int64_t>(static_cast<int64_t>(qt) * 128 + 127, p->query_len - 1);
-    uph += (last >> 7) + 1;
-  }
+  const int64_t uph = prefill_units_per_head(p->query_len, p->max_seq_len);
   a.units_per_head = uph;
   a.total_units = uph * p->heads * p->num_reqs;
   a.status = status;

@@ -59,7 +59,7 @@ struct PrefillArgs {
   int64_t s_head, s_row;
   int32_t fill_width;         // 0: leave invisible blocks untouched; else write -inf up to it
   int32_t qtiles;             // cdiv(query_len, 128)
-  int64_t units_per_head;     // worst-case (tile, block) units of one (request, head)
+  int64_t units_per_head;     // prefill_units_per_head(query_len, max_seq_len)
   int64_t total_units;
   int32_t status_dummy;
   int32_t* status;
@@ -88,6 +88,9 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, int decode_grid, cudaStream
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
+// Work units of the prefill scorer for one (request, head), counted for a
+// request of max_seq_len tokens (the unit is defined in prefill.cu).
+int64_t prefill_units_per_head(int32_t query_len, int32_t max_seq_len);
 
 // Grid sizing of the decode kernel (persistent; one CTA per SM).
 int decode_ctas_per_sm();

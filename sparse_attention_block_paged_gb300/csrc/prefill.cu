@@ -3,59 +3,84 @@
 // Computes score[h, row, b] = sm_scale * max over the visible tokens of block
 // b of q[row, h] . k[token] (vLLM MiniMax-M3 "index_topk" page,
 // minimax_m3_index_score: per-token index scores for each visible sparse
-// block, i.e. the largest token score inside the block, causal through the request's
-// prefix).  The design is ours:
+// block, i.e. the largest token score inside the block, causal through the
+// request's prefix).  The design is ours:
 //
-//   * A unit is (request, head, 128-row query tile, key block).  Units are
-//     enumerated from host-known sizes, assuming every request is
-//     max_seq_len long (a bound fixed across graph replays); units past a request's real
-//     causal range do no math.  Each CTA of a persistent grid takes one
-//     contiguous, equal share of the units, so the causal triangle is spread
-//     evenly over the SMs.
-//   * warp 0   : TMA producer: the 128 x 128 bf16 query tile (two 64-column
+//   * A unit is (request, head, 128-row query tile, pair of key blocks).
+//     Units are enumerated from host-known sizes, assuming every request is
+//     max_seq_len long (a bound fixed across graph replays); units past a
+//     request's real causal range do no math.  Each CTA of a persistent grid
+//     takes one contiguous, equal share of the units, so the causal triangle
+//     is spread evenly over the SMs.
+//   * warp 0   : TMA producer.  The 128 x 128 bf16 query tile (two 64-column
 //                boxes, 128-byte swizzle, from a 3-D map over
-//                [tokens, heads, 128]) once per tile, and each key page (from
-//                a 2-D map over [pages*128, 128]) into a 4-stage ring.
-//   * warp 1   : one thread copies each query tile into TMEM once
-//                (tcgen05.cp) and issues tcgen05.mma with A (M = 128 query
-//                rows) read from TMEM and B (N = 128 key tokens) from shared
-//                memory, K = 128, into one of three 128-column fp32 TMEM
-//                accumulators.  Reading only B from shared memory keeps the
-//                operand traffic well inside shared-memory bandwidth.
-//   * warps 2-9: epilogue, two teams of four warps taking alternate units:
-//                tcgen05.ld of the thread's query row (128 fp32 columns),
-//                causal mask only on diagonal blocks, row max with 3-input
-//                max, scale, one fp32 store per (row, block).
+//                [tokens, heads, 128]) once per tile, and the two key pages of
+//                each unit (from a 2-D map over [pages*128, 128]) into a
+//                3-stage ring of 64 KB stages laid out as one 256-row operand.
+//   * warp 1   : one thread issues tcgen05.mma, A = the query tile
+//                (M = 128), B = both pages (N = 256 key tokens), K = 128, as
+//                8 instructions into one of two 256-column fp32 TMEM
+//                accumulators.  The tensor pipe queues only a few MMAs, so
+//                the issuing thread's per-unit work (waits, commits, loop)
+//                must hide behind the queued ones: N = 256 doubles the work
+//                each instruction carries, and the producer hands the issuer
+//                one word per stage (unit shape, new tile, end) so that the
+//                issuer keeps no unit bookkeeping.
+//   * warps 2-9: epilogue, two teams of four warps (one warp per TMEM lane
+//                quadrant).  Team t drains block t of every unit: loads its
+//                row's 128 columns with tcgen05.ld, frees the accumulator,
+//                then takes the causal row max with 3-input max and stores
+//                one fp32 score per (row, block).
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "../../include/mm3idx.h"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace mm3idx {
+
+// Worst-case units of one (request, head): every query tile of a request of
+// max_seq_len tokens, its visible blocks taken in pairs.
+int64_t prefill_units_per_head(int32_t query_len, int32_t max_seq_len) {
+  const int64_t wprefix = static_cast<int64_t>(max_seq_len) - query_len;
+  const int64_t qtiles = (static_cast<int64_t>(query_len) + 127) / 128;
+  int64_t n = 0;
+  for (int64_t qt = 0; qt < qtiles; ++qt) {
+    const int64_t last = wprefix + std::min<int64_t>(qt * 128 + 127, query_len - 1);
+    n += ((last >> 7) + 2) / 2;
+  }
+  return n;
+}
+
 namespace {
 
-// The query tile is the MMA's A operand.  It is TMA-loaded into shared
-// memory and, when kQInTmem, copied once per tile into TMEM (two 64-column
-// buffers) so that every MMA reads only the key page from shared memory.
-constexpr bool kQInTmem = true;
-constexpr int kStages = 4;
-constexpr int kAcc = kQInTmem ? 3 : 4;
-constexpr uint32_t kAccCol0 = kQInTmem ? 128 : 0;  // first accumulator column
-constexpr int kTile = 32768;  // 128 x 128 bf16
+constexpr int kStages = 3;
+constexpr int kPage = 32768;                  // 128 x 128 bf16
+constexpr int kHalf = 16384;                  // 128 rows x 64 columns
+constexpr int kStageBytes = 2 * kPage;        // two pages
+constexpr uint32_t kTmemCols = 512;           // two 256-column accumulators
 constexpr int kThreads = 320;
 constexpr int oQ = 0;
-constexpr int oK = oQ + 2 * kTile;
-constexpr int oBar = oK + kStages * kTile;
-constexpr int kBars = 2 * kStages + 2 * kAcc + 6 + 1;
-constexpr int oMisc = oBar + kBars * 8;
+constexpr int oK = oQ + kPage;
+constexpr int oBar = oK + kStages * kStageBytes;
+constexpr int kBars = 2 * kStages + 4 + 2 + 1;
+constexpr int oInfo = oBar + kBars * 8;        // one word per stage, producer -> MMA
+constexpr int oMisc = oInfo + kStages * 4;
 constexpr int kSmem = oMisc + 64 + 1024;
-constexpr uint32_t kTmemCols = 512;
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 struct Misc {
   uint32_t tmem;
   int abort;
 };
+
+// What the producer tells the MMA issuer about the unit in a stage, so that
+// the issuer does no unit bookkeeping of its own.
+constexpr uint32_t kInfoValid = 1u;    // 0: no more units
+constexpr uint32_t kInfoTwo = 2u;      // both key blocks visible (N = 256), else N = 128
+constexpr uint32_t kInfoNewTile = 4u;  // first unit of a new query tile
 
 // Visible block count of query tile qt under a given prefix length
 // (positions prefix + 128*qt .. prefix + min(128*qt + 127, query_len - 1)).
@@ -67,7 +92,8 @@ __device__ __forceinline__ int tile_blocks(int prefix, int qt, int query_len) {
 // Iterates this CTA's share of the unit list.
 struct UnitIter {
   int64_t u, hi;
-  int rh, qt, b, n;   // (request*heads + head), tile, block, scheduled blocks of the tile
+  int rh, qt, p, np;  // (request*heads + head), tile, pair, scheduled pairs of the tile
+  int req, head;      // rh split into its request and head
   int wprefix;        // worst-case prefix: max_seq_len - query_len
   __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi_) {
     u = lo;
@@ -75,32 +101,51 @@ struct UnitIter {
     wprefix = a.max_seq_len - a.query_len;
     if (lo >= hi_) return;
     rh = static_cast<int>(lo / a.units_per_head);
+    req = rh / a.heads;
+    head = rh - req * a.heads;
     int64_t off = lo - static_cast<int64_t>(rh) * a.units_per_head;
     qt = 0;
     for (;;) {
-      n = tile_blocks(wprefix, qt, a.query_len);
-      if (off < n) break;
-      off -= n;
+      np = (tile_blocks(wprefix, qt, a.query_len) + 1) >> 1;
+      if (off < np) break;
+      off -= np;
       ++qt;
     }
-    b = static_cast<int>(off);
+    p = static_cast<int>(off);
   }
   __device__ bool valid() const { return u < hi; }
   __device__ void advance(const PrefillArgs& a) {
     ++u;
-    if (++b < n) return;
-    b = 0;
+    if (++p < np) return;
+    p = 0;
     if (++qt == a.qtiles) {
       qt = 0;
       ++rh;
+      if (++head == a.heads) {
+        head = 0;
+        ++req;
+      }
     }
-    n = tile_blocks(wprefix, qt, a.query_len);
+    np = (tile_blocks(wprefix, qt, a.query_len) + 1) >> 1;
   }
 };
 
-__device__ __forceinline__ int clamp_len(const PrefillArgs& a, int i) {
-  return min(max(__ldg(a.seq_lens + i), 0), a.max_seq_len);
-}
+// Per-tile facts every role needs, refreshed only when the tile changes.
+struct TileInfo {
+  int rh = -1, qt = -1, req = -1;
+  int prefix = 0, nvis = 0;  // request prefix; visible blocks of the tile
+  __device__ __forceinline__ bool refresh(const PrefillArgs& a, const UnitIter& U) {
+    if (U.rh == rh && U.qt == qt) return false;
+    if (U.req != req) {
+      req = U.req;
+      prefix = min(max(__ldg(a.seq_lens + req), 0), a.max_seq_len) - a.query_len;
+    }
+    rh = U.rh;
+    qt = U.qt;
+    nvis = tile_blocks(prefix, qt, a.query_len);
+    return true;
+  }
+};
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -119,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + oBar);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
-  uint64_t* acc_empty = acc_full + kAcc;
-  uint64_t* q_full = acc_empty + kAcc;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* qtm_free = q_empty + 2;   // TMEM query buffer free again
-  uint64_t* done_bar = qtm_free + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* done_bar = q_empty + 1;
+  volatile uint32_t* sInfo = reinterpret_cast<volatile uint32_t*>(sm + oInfo);
   Misc* misc = reinterpret_cast<Misc*>(sm + oMisc);
   volatile int* abort_flag = &misc->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,15 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kAcc; ++s) {
-      mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
-    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
-      mbar_init(&qtm_free[s], 1);
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 8);   // both epilogue teams
     }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     mbar_init(done_bar, 1);
     misc->abort = 0;
     fence_barrier_init();
@@ -162,114 +204,134 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t hi = a.total_units * (blockIdx.x + 1) / G;
   UnitIter U;
   U.init(a, lo, hi);
+  TileInfo T;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_k = policy_evict_last();   // pages are re-read by later tiles
-      const uint64_t pol_q = policy_evict_first();
-      int cur_rh = -1, cur_qt = -1;
-      uint32_t tq = 0, it = 0;
-      bool ok = true;
-      for (; ok && U.valid(); U.advance(a)) {
-        const int req = U.rh / a.heads, head = U.rh - req * a.heads;
-        const int prefix = clamp_len(a, req) - a.query_len;
-        if (U.b >= tile_blocks(prefix, U.qt, a.query_len)) continue;  // no visible token
-        if (U.rh != cur_rh || U.qt != cur_qt) {
-          cur_rh = U.rh;
-          cur_qt = U.qt;
-          const int qs = tq & 1;
-          if (tq >= 2) ok = mbar_wait(&q_empty[qs], ((tq >> 1) - 1) & 1, abort_flag);
-          if (!ok) break;
-          const int tok0 = req * a.query_len + U.qt * 128;
-          mbar_arrive_expect_tx(&q_full[qs], kTile);
-          tma_load_3d(sQ + qs * kTile, &qmap, &q_full[qs], 0, head, tok0, pol_q);
-          tma_load_3d(sQ + qs * kTile + kTile / 2, &qmap, &q_full[qs], 64, head, tok0, pol_q);
-          ++tq;
-        }
-        const uint32_t st = it % kStages, rnd = it / kStages;
-        if (rnd > 0) ok = mbar_wait(&empty[st], (rnd - 1) & 1, abort_flag);
-        if (!ok) break;
-        const int page = __ldg(a.table + static_cast<int64_t>(req) * a.table_stride + U.b);
-        if (page >= 0 && page < a.num_pages) {
-          mbar_arrive_expect_tx(&full[st], kTile);
-          tma_load_2d(sK + st * kTile, &kmap, &full[st], 0, page * 128, pol_k);
-          tma_load_2d(sK + st * kTile + kTile / 2, &kmap, &full[st], 64, page * 128, pol_k);
+    // The whole warp walks the units; lane 0 issues the copies.  Page ids are
+    // read 32 at a time (one per lane) and broadcast with shuffles.
+    const uint64_t pol_k = policy_evict_last();   // pages are re-read by later tiles
+    const uint64_t pol_q = policy_evict_first();
+    const int nblk = (a.max_seq_len + kBlock - 1) / kBlock;  // table entries that exist
+    int cur_rh = -1, cur_qt = -1;
+    int pg_req = -1, pg_base = 0, pg = -1;
+    uint32_t tq = 0, it = 0, st = 0, ph = 0;
+    bool ok = true;
+    for (; ok && U.valid(); U.advance(a)) {
+      T.refresh(a, U);
+      const int b0 = 2 * U.p;
+      if (b0 >= T.nvis) continue;  // no visible token
+      const bool two = b0 + 1 < T.nvis;
+      if (U.req != pg_req || b0 < pg_base || b0 + 1 >= pg_base + 32) {
+        pg_req = U.req;
+        pg_base = b0;
+        const int mine = pg_base + lane;
+        pg = mine < nblk ? __ldg(a.table + static_cast<int64_t>(U.req) * a.table_stride + mine)
+                         : -1;
+      }
+      const int pa = __shfl_sync(0xffffffffu, pg, b0 - pg_base);
+      const int pb = __shfl_sync(0xffffffffu, pg, b0 + 1 - pg_base);
+      if (it >= static_cast<uint32_t>(kStages)) ok = warp_wait(&empty[st], ph ^ 1u, abort_flag);
+      if (!ok) break;
+      const bool new_tile = U.rh != cur_rh || U.qt != cur_qt;
+      if (lane == 0) {
+        sInfo[st] = kInfoValid | (two ? kInfoTwo : 0u) | (new_tile ? kInfoNewTile : 0u);
+        uint8_t* dst = sK + st * kStageBytes;
+        const bool good = pa >= 0 && pa < a.num_pages && (!two || (pb >= 0 && pb < a.num_pages));
+        if (good) {
+          // Stage layout: [A cols 0-63][B cols 0-63][A cols 64-127][B cols 64-127],
+          // i.e. 256 key rows per 64-column half, as the N = 256 operand.
+          mbar_arrive_expect_tx(&full[st], two ? 2 * kPage : kPage);
+          tma_load_2d(dst, &kmap, &full[st], 0, pa * 128, pol_k);
+          tma_load_2d(dst + 2 * kHalf, &kmap, &full[st], 64, pa * 128, pol_k);
+          if (two) {
+            tma_load_2d(dst + kHalf, &kmap, &full[st], 0, pb * 128, pol_k);
+            tma_load_2d(dst + 3 * kHalf, &kmap, &full[st], 64, pb * 128, pol_k);
+          }
         } else {
           atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
           mbar_arrive(&full[st]);
         }
-        ++it;
       }
-      // Drain: let every copy started above land before the CTA may exit.
+      ++it;
+      if (++st == kStages) {
+        st = 0;
+        ph ^= 1u;
+      }
+      if (new_tile) {
+        // The tile's query rows, once the MMAs of the previous tile are done
+        // (issued after this unit's keys, which do not depend on them).
+        cur_rh = U.rh;
+        cur_qt = U.qt;
+        if (tq > 0) ok = warp_wait(q_empty, (tq - 1) & 1u, abort_flag);
+        if (!ok) break;
+        if (lane == 0) {
+          const int tok0 = U.req * a.query_len + U.qt * 128;
+          mbar_arrive_expect_tx(q_full, kPage);
+          tma_load_3d(sQ, &qmap, q_full, 0, U.head, tok0, pol_q);
+          tma_load_3d(sQ + kHalf, &qmap, q_full, 64, U.head, tok0, pol_q);
+        }
+        ++tq;
+      }
+    }
+    // Drain: let every copy started above land before the CTA may exit.
+    if (lane == 0) {
       int dummy = 0;
       const uint32_t pend = it < static_cast<uint32_t>(kStages) ? it : kStages;
       for (uint32_t k = 0; k < pend; ++k) {
         const uint32_t idx = it - 1 - k;
         mbar_wait(&full[idx % kStages], (idx / kStages) & 1, &dummy);
       }
-      if (tq > 0) mbar_wait(&q_full[(tq - 1) & 1], ((tq - 1) >> 1) & 1, &dummy);
-      if (tq > 1) mbar_wait(&q_full[(tq - 2) & 1], ((tq - 2) >> 1) & 1, &dummy);
+      if (tq > 0) mbar_wait(q_full, (tq - 1) & 1u, &dummy);
+    }
+    __syncwarp();
+    // End marker for the MMA issuer, in the next stage once it is free.
+    if (ok && it >= static_cast<uint32_t>(kStages)) ok = warp_wait(&empty[st], ph ^ 1u, abort_flag);
+    if (ok && lane == 0) {
+      sInfo[st] = 0u;
+      mbar_arrive(&full[st]);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-      int cur_rh = -1, cur_qt = -1;
-      uint32_t tq = 0, it = 0;
+      constexpr uint32_t idesc2 = idesc_bf16_f32(128, 256);
+      constexpr uint32_t idesc1 = idesc_bf16_f32(128, 128);
+      const uint64_t qdesc = sdesc_kmajor_sw128(smem_u32(sQ));
+      const uint64_t kdesc0 = sdesc_kmajor_sw128(smem_u32(sK));
+      uint32_t tq = 0, it = 0, st = 0, ph = 0, acc = 0;
       bool ok = true;
-      uint32_t qaddr = 0, qtm = 0;
-      for (; ok && U.valid(); U.advance(a)) {
-        const int req = U.rh / a.heads;
-        const int prefix = clamp_len(a, req) - a.query_len;
-        if (U.b >= tile_blocks(prefix, U.qt, a.query_len)) continue;
-        if (U.rh != cur_rh || U.qt != cur_qt) {
-          if (tq > 0) mma_commit(kQInTmem ? &qtm_free[(tq - 1) & 1] : &q_empty[(tq - 1) & 1]);
-          cur_rh = U.rh;
-          cur_qt = U.qt;
-          const int qs = tq & 1;
-          ok = mbar_wait(&q_full[qs], (tq >> 1) & 1, abort_flag);
+      for (;;) {
+        ok = mbar_wait(&full[st], ph, abort_flag);
+        if (!ok) break;
+        const uint32_t info = sInfo[st];
+        if (!(info & kInfoValid)) break;
+        if (info & kInfoNewTile) {
+          if (tq > 0) mma_commit(q_empty);   // the previous tile's query rows
+          ok = mbar_wait(q_full, tq & 1u, abort_flag);
           if (!ok) break;
-          qaddr = smem_u32(sQ + qs * kTile);
-          if constexpr (kQInTmem) {
-            // The MMAs of tile tq-2 read this TMEM buffer; let them finish.
-            if (tq >= 2) ok = mbar_wait(&qtm_free[qs], ((tq >> 1) - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            qtm = tmem_base + qs * 64;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tmem_cp_128x256b(qtm + k * 8,
-                               sdesc_kmajor_sw128(qaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32));
-            mma_commit(&q_empty[qs]);   // the shared-memory tile is free once copied
-          }
           ++tq;
         }
-        const uint32_t st = it % kStages, rnd = it / kStages;
-        ok = mbar_wait(&full[st], rnd & 1, abort_flag);
-        if (!ok) break;
-        const uint32_t ab = it % kAcc, ar = it / kAcc;
-        if (ar > 0) ok = mbar_wait(&acc_empty[ab], (ar - 1) & 1, abort_flag);
+        if (it >= 2) ok = mbar_wait(&acc_empty[acc], ((it >> 1) - 1) & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * kTile);
-        const uint32_t d = tmem_base + kAccCol0 + ab * 128;
+        const uint32_t d = tmem_base + acc * 256;
+        const uint64_t kdesc = kdesc0 + st * (kStageBytes >> 4);
+        const uint32_t idesc = (info & kInfoTwo) ? idesc2 : idesc1;
+        // K slice k: 32 bytes into a 128-byte row inside a 64-column half.
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t bd = sdesc_kmajor_sw128(kaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32);
-          if constexpr (kQInTmem) {
-            mma_bf16_ts(d, qtm + k * 8, bd, idesc, k > 0 ? 1u : 0u);
-          } else {
-            const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (kTile / 2) + (k & 3) * 32);
-            mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-          }
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_bf16(d, qdesc + (k >> 2) * (kHalf >> 4) + (k & 3) * 2,
+                   kdesc + (k >> 2) * ((2 * kHalf) >> 4) + (k & 3) * 2, idesc, k > 0 ? 1u : 0u);
         mma_commit(&empty[st]);
-        mma_commit(&acc_full[ab]);
+        mma_commit(&acc_full[acc]);
         ++it;
+        acc ^= 1u;
+        if (++st == kStages) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
-      if (ok && tq > 0 && !kQInTmem) mma_commit(&q_empty[(tq - 1) & 1]);
       mma_commit(done_bar);
       int dummy = 0;
       mbar_wait(done_bar, 0, &dummy);
@@ -277,68 +339,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue
-    // Two teams of four warps (one warp per TMEM lane quadrant) take
-    // alternate units, so two accumulators drain at once.
-    const int team = (warp - 2) >> 2;
-    const int quad = warp & 3;       // a warp may only read lanes 32*(warp%4)..+31
-    const int r = quad * 32 + lane;  // query row within the tile
-    uint32_t it = 0;
+    const int team = (warp - 2) >> 2;  // which block of the pair
+    const int quad = warp & 3;         // a warp may only read lanes 32*(warp%4)..+31
+    const int r = quad * 32 + lane;    // query row within the tile
+    uint32_t it = 0, acc = 0;
     bool ok = true;
+    bool row_ok = false;
+    int pos = 0;
+    float* srow = nullptr;
     for (; ok && U.valid(); U.advance(a)) {
-      const int req = U.rh / a.heads, head = U.rh - req * a.heads;
-      const int prefix = clamp_len(a, req) - a.query_len;
-      const int qrow = U.qt * 128 + r;            // query index inside the request
-      const bool row_ok = qrow < a.query_len;
-      const int pos = prefix + qrow;
-      float* srow = a.score + head * a.s_head +
-                    (static_cast<int64_t>(req) * a.query_len + qrow) * a.s_row;
-      const bool active = U.b < tile_blocks(prefix, U.qt, a.query_len);
-      const uint32_t mine = active ? it++ : 0u;
-      if (active && (mine & 1u) == static_cast<uint32_t>(team)) {
-        const uint32_t ab = mine % kAcc, ar = mine / kAcc;
+      if (T.refresh(a, U)) {
+        const int qrow = U.qt * 128 + r;  // query index inside the request
+        row_ok = qrow < a.query_len;
+        pos = T.prefix + qrow;
+        srow = a.score + U.head * a.s_head +
+               (static_cast<int64_t>(U.req) * a.query_len + qrow) * a.s_row;
+      }
+      const int b0 = 2 * U.p;
+      if (b0 < T.nvis) {
+        const int b = b0 + team;
+        const bool mine = b < T.nvis;
         bool got = true;
-        if (lane == 0) got = mbar_wait(&acc_full[ab], ar & 1, abort_flag);
+        if (lane == 0) got = mbar_wait(&acc_full[acc], (it >> 1) & 1u, abort_flag);
         if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol0 + ab * 128;
-        const int lim = pos - U.b * 128;  // columns 0..lim are visible
-        float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 64) {
-          uint32_t v[32], w[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_ld32(taddr + c0 + 32, w);
-          tmem_ld_wait32x2(v, w);
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        if (mine) {
+          const uint32_t taddr =
+              tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256 + team * 128;
+          tmem_ld32(taddr, v0);
+          tmem_ld32(taddr + 32, v1);
+          tmem_ld32(taddr + 64, v2);
+          tmem_ld32(taddr + 96, v3);
+          tmem_ld_wait32x4(v0, v1, v2, v3);
+        }
+        // The columns are in registers: hand the accumulator back first.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (mine && row_ok) {
+          const int lim = pos - b * 128;  // columns 0..lim are visible
+          float m0 = -INFINITY, m1 = -INFINITY;
           if (lim >= 127) {
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
-              m0 = fmax3(m0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
-              m0 = fmax3(m0, __uint_as_float(w[k]), __uint_as_float(w[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(w[k + 2]), __uint_as_float(w[k + 3]));
+              m0 = fmax3(m0, __uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(v0[k + 2]), __uint_as_float(v0[k + 3]));
+              m0 = fmax3(m0, __uint_as_float(v1[k]), __uint_as_float(v1[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(v1[k + 2]), __uint_as_float(v1[k + 3]));
+              m0 = fmax3(m0, __uint_as_float(v2[k]), __uint_as_float(v2[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(v2[k + 2]), __uint_as_float(v2[k + 3]));
+              m0 = fmax3(m0, __uint_as_float(v3[k]), __uint_as_float(v3[k + 1]));
+              m1 = fmax3(m1, __uint_as_float(v3[k + 2]), __uint_as_float(v3[k + 3]));
             }
           } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
-              if (c0 + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(w[k]));
+              if (k <= lim) m0 = fmaxf(m0, __uint_as_float(v0[k]));
+              if (32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(v1[k]));
+              if (64 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v2[k]));
+              if (96 + k <= lim) m1 = fmaxf(m1, __uint_as_float(v3[k]));
             }
           }
+          srow[b] = fmaxf(m0, m1) * a.sm_scale;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ab]);
-        if (row_ok) srow[U.b] = fmaxf(m0, m1) * a.sm_scale;
-      } else if (!active && a.fill_width > 0 && row_ok && (U.u & 1) == team) {
-        srow[U.b] = -INFINITY;
+        ++it;
+        acc ^= 1u;
       }
-      // The tile's last scheduled block: blocks past the worst-case schedule.
-      if (a.fill_width > 0 && row_ok && team == 0 && U.b == U.n - 1)
-        for (int b = U.n; b < a.fill_width; ++b) srow[b] = -INFINITY;
+      // The tile's last scheduled unit: blocks past the visible ones hold
+      // -inf.  Each warp of team 0 fills its 32 rows one row at a time, lanes
+      // on consecutive blocks, so the stores coalesce.
+      if (a.fill_width > 0 && team == 0 && U.p == U.np - 1) {
+        const int row0 = U.qt * 128 + quad * 32;
+        const int nrows = min(32, a.query_len - row0);
+        float* base = a.score + U.head * a.s_head +
+                      (static_cast<int64_t>(U.req) * a.query_len + row0) * a.s_row;
+        for (int rr = 0; rr < nrows; ++rr)
+          for (int b = T.nvis + lane; b < a.fill_width; b += 32) base[rr * a.s_row + b] = -INFINITY;
+      }
     }
   }
 

@@ -282,6 +282,15 @@ __device__ __forceinline__ void tmem_ld_wait32x2(uint32_t (&r)[32], uint32_t (&w
   asm volatile("" : MM3IDX_PLUS32(w) : : "memory");
 }
 
+// One wait covering four outstanding 32-column loads.
+__device__ __forceinline__ void tmem_ld_wait32x4(uint32_t (&r0)[32], uint32_t (&r1)[32],
+                                                 uint32_t (&r2)[32], uint32_t (&r3)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r0) : : "memory");
+  asm volatile("" : MM3IDX_PLUS32(r1) : : "memory");
+  asm volatile("" : MM3IDX_PLUS32(r2) : : "memory");
+  asm volatile("" : MM3IDX_PLUS32(r3) : : "memory");
+}
+
 // Fetch-and-add with acquire-release semantics at GPU scope: orders this
 // thread's earlier writes (and those it has observed) before the add, and the
 // writes released by earlier adds before this thread's later reads.
