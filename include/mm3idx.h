@@ -149,9 +149,9 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
 
 /*
  * mm3idx_workspace_bytes -- device workspace the fused calls need.
- * op = MM3IDX_OP_DECODE: request start offsets plus the partial top-k
- * candidate lists of requests split across CTAs (depends on the current
- * device's SM count).
+ * op = MM3IDX_OP_DECODE: one ticket counter per request plus the partial
+ * top-k candidate lists of requests split across CTAs (depends on the
+ * current device's SM count).
  * op = MM3IDX_OP_PREFILL: the fp32 score scratch [heads, rows, roundup(cdiv(max_seq_len,128), 4)].
  * Writes the size to *bytes.  Reads the current device's attributes; no
  * allocation.
@@ -167,11 +167,12 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs,
  *
  * out: int32 [h, row, k] at out[h*out_head_stride + row*out_row_stride + k].
  * workspace: >= mm3idx_workspace_bytes(MM3IDX_OP_DECODE, ...) bytes, 256-byte
- * aligned; no initialisation needed and no state is kept in it between
- * calls.  Requests longer than one CTA's share of the batch leave at most
- * topk candidate keys per row per CTA there, which a second, small kernel
- * (a programmatic dependent launch on the same stream) merges.  Launches
- * that share a workspace must not overlap.
+ * aligned, zero-filled before its first use.  A request longer than one
+ * CTA's share of the batch leaves at most topk candidate keys per row per
+ * CTA there; the last of its CTAs to finish merges them, counted by a ticket
+ * per request that every completed call returns to zero, so the workspace
+ * can be reused as it is.  After a call that reported MM3IDX_DEV_TIMEOUT,
+ * zero it again.  Launches that share a workspace must not overlap.
  */
 int mm3idx_decode(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
                   int32_t local_blocks, int32_t *out, int64_t out_head_stride,
@@ -226,9 +227,10 @@ int mm3idx_get_device_error(void *stream, int32_t *code);
  * MM3IDX_ERR_STATIC_SCRATCH.  The first call on a device looks up the
  * array's device address (once per device, with that device current); make
  * that first call before any stream capture.  All calls share the one array
- * and it keeps the previous call's contents (the decode needs none of them
- * cleared); calls whose executions overlap on the GPU race on it, so issue
- * them in one stream or otherwise order them.
+ * and it keeps the previous call's contents; each call first clears the part
+ * that must start at zero (the per-request tickets, with cudaMemsetAsync on
+ * `stream`, which allocates nothing).  Calls whose executions overlap on the
+ * GPU race on the array, so issue them in one stream or otherwise order them.
  */
 #define MM3IDX_STATIC_SCRATCH_BYTES (8u << 20)  /* 8 MiB */
 #define MM3IDX_ERR_STATIC_SCRATCH   (-12)       /* problem needs more scratch than the static array */

@@ -186,9 +186,10 @@ def workspace_bytes(op: int, heads: int, num_reqs: int, query_len: int, max_seq_
 
 def new_workspace(op, heads, num_reqs, query_len, max_seq_len, topk, device=None):
     """A workspace for :func:`decode` / :func:`prefill` (uint8, 256-byte
-    aligned by the caching allocator; needs no initialisation)."""
+    aligned by the caching allocator, zero-filled as the decode requires;
+    reusable across calls)."""
     n = workspace_bytes(op, heads, num_reqs, query_len, max_seq_len, topk)
-    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def score(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, sm_scale,

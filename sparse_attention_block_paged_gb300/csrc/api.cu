@@ -163,10 +163,10 @@ bool out_ok(int64_t head_stride, int64_t row_stride, int32_t heads, int64_t rows
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MM3IDX_OK : MM3IDX_ERR_CUDA; }
 
-// Decode workspace: [total blocks: 256 B][request starts: num_reqs x 8 B,
-// 256-aligned][partial lists: (grid + num_reqs) slots x 32 rows x tk keys].
+// Decode workspace: [tickets: num_reqs x 4 B, 256-aligned, zero between
+// calls][partial lists: (grid + num_reqs) slots x 32 rows x tk keys].
 size_t decode_ws_head(int32_t num_reqs) {
-  return 256 + (static_cast<size_t>(num_reqs) * 8 + 255) / 256 * 256;
+  return (static_cast<size_t>(num_reqs) * 4 + 255) / 256 * 256;
 }
 
 size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len, int32_t topk) {
@@ -233,8 +233,7 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   a.i_head = out_head_stride;
   a.i_row = out_row_stride;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.total_blocks = reinterpret_cast<long long*>(ws);
-  a.req_start = reinterpret_cast<long long*>(ws + 256);
+  a.tickets = reinterpret_cast<unsigned int*>(ws);
   a.partials = reinterpret_cast<uint64_t*>(ws + decode_ws_head(p->num_reqs));
   const int grid = decode_grid(p, dev->sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -248,8 +247,7 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
     if ((rc = make_kmap(p, &kmap))) return rc;
     e = launch_decode_bf16(kmap, a, grid, s);
   }
-  if (e != cudaSuccess) return MM3IDX_ERR_CUDA;
-  return cuda_status(launch_decode_merge(a, grid, s));
+  return cuda_status(e);
 }
 
 int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, int64_t row_stride,
@@ -456,6 +454,11 @@ int mm3idx_decode_static(const mm3idx_problem_t* p, int32_t topk, int32_t init_b
   if (decode_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len, topk) >
       MM3IDX_STATIC_SCRATCH_BYTES)
     return MM3IDX_ERR_STATIC_SCRATCH;
+  // The tickets must start at zero; a completed call leaves them so, but a
+  // call that gave up part-way may not have.
+  if (cudaMemsetAsync(scratch, 0, decode_ws_head(p->num_reqs), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MM3IDX_ERR_CUDA;
   return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
                     out_row_stride, scratch, MM3IDX_STATIC_SCRATCH_BYTES, stream);
 }

@@ -32,10 +32,11 @@
 //                on streaming.
 //   * warp 3   : merge warp.  Folds the two lists of each row and writes the
 //                ids of requests held by one CTA (forced blocks re-pinned,
-//                ascending, -1 pad); for a request split across CTAs it
-//                publishes the lists, and a small merge kernel -- launched as
-//                a programmatic dependent launch, so its start overlaps this
-//                grid -- merges every split request once this grid is done.
+//                ascending, -1 pad).  For a request split across CTAs it
+//                publishes the lists and takes a ticket; the last of the
+//                request's CTAs to arrive merges all their lists and writes
+//                the rows.  Split requests are streamed first, so these
+//                merges overlap the rest of the stream.
 //
 // Every wait is bounded (ptx.cuh).  A wait that gives up raises an abort flag
 // shared by the CTA's roles and the MM3IDX_DEV_TIMEOUT status bit.
@@ -152,18 +153,27 @@ __device__ __forceinline__ int cta_of(long long x, long long total, int grid) {
 
 // One warp: total block count, this CTA's share and the first request in it.
 __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
+  // Lengths are read kU per lane at a time so that their loads overlap.
+  constexpr int kU = 8;
   long long total = 0;
-  for (int b = 0; b < a.num_reqs; b += 32) {
-    const int i = b + lane;
-    if (i < a.num_reqs) {
+  for (int b = 0; b < a.num_reqs; b += 32 * kU) {
+    int raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = b + u * 32 + lane;
+      raw[u] = i < a.num_reqs ? __ldg(a.seq_lens + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = b + u * 32 + lane;
+      if (i >= a.num_reqs) continue;
       if (blockIdx.x == 0) {
-        const int raw = __ldg(a.seq_lens + i);
         int bits = 0;
-        if (raw > a.max_seq_len) bits |= MM3IDX_DEV_SEQ_TOO_LONG;
-        if (raw < a.query_len) bits |= MM3IDX_DEV_SEQ_TOO_SHORT;
+        if (raw[u] > a.max_seq_len) bits |= MM3IDX_DEV_SEQ_TOO_LONG;
+        if (raw[u] < a.query_len) bits |= MM3IDX_DEV_SEQ_TOO_SHORT;
         if (bits) atomicOr(a.status, bits);
       }
-      total += req_blocks(a, i);
+      total += (min(max(raw[u], 0), a.max_seq_len) + kBlock - 1) / kBlock;
     }
   }
 #pragma unroll
@@ -193,11 +203,6 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
       }
     }
     const unsigned hitl = __ballot_sync(0xffffffffu, i < a.num_reqs && P + incl > hi - 1);
-    // Record where each request this share touches starts (several CTAs may
-    // write the same value); the merge kernel reads it.
-    const int il_here = hitl ? b + __ffs(hitl) - 1 : a.num_reqs;
-    if (a.req_start && !need0 && i >= i0 && i <= il_here && i < a.num_reqs)
-      a.req_start[i] = P + incl - nb;
     if (hitl) {
       const int k = __ffs(hitl) - 1;
       il = b + k;
@@ -207,7 +212,6 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
     P += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) {
-    if (a.total_blocks && blockIdx.x == 0) *a.total_blocks = total;
     m->lo = lo;
     m->hi = hi;
     m->total = total;
@@ -446,8 +450,6 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   volatile int* abort_flag = &misc->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The merge kernel may be scheduled now; it waits for this grid's results.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -683,11 +685,10 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     // ------------------------------------------------------------ merge warp
     // Per request (in the walker's order): fold the two epilogue warps'
     // lists row by row (lane n owns row n).  A request held by one CTA is
-    // written here, one row at a time by the whole warp; otherwise each row's
-    // list goes to this CTA's partial slot for the merge kernel.  With
-    // total >= grid every share is non-empty, so the request's CTAs are
-    // first..last; with fewer blocks than CTAs every non-empty share is a
-    // single block, so block k sits in cta_of(preq + k).
+    // written here; a split request goes through the partial slots and its
+    // tickets.  With total >= grid every share is non-empty, so the
+    // request's CTAs are first..last; with fewer blocks than CTAs every
+    // non-empty share is a single block, so block k sits in cta_of(preq + k).
     const int n = lane;
     const int R = a.rows_per_req;
     const bool select = a.mode == kModeSelect;
@@ -716,24 +717,53 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
       const int last = cta_of(preq + nb - 1, total, gridDim.x);
       const bool dense = total >= gridDim.x;
       const int nseg = dense ? last - first + 1 : nb;
-      const bool write_rows = nseg == 1;
-      if (!write_rows && n < R) {
-        // Split request: publish this CTA's lists; the merge kernel folds
-        // the request's slots after this grid completes.
-        const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
-        ulonglong2* dst = reinterpret_cast<ulonglong2*>(
-            a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
-#pragma unroll
-        for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
-      }
-      if (write_rows && n < R) {
+      const int j = n < R ? n / a.heads : 0, h = n < R ? n - j * a.heads : 0;
+      const int pr = req_len(a, req) - a.query_len + j;
+      const int cr = pr >= 0 ? (pr >> 7) : -1;
+      int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
+      if (nseg == 1) {
         // Lane n writes row n: forced blocks, the best picks in ascending id
         // order (a sorting network over the TK candidate ids), then -1.
-        const int j = n / a.heads, h = n - j * a.heads;
-        const int pr = req_len(a, req) - a.query_len + j;
-        const int cr = pr >= 0 ? (pr >> 7) : -1;
-        int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
-        write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
+        if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
+      } else {
+        // Split request: publish this CTA's lists, then take a ticket.  The
+        // last of the request's CTAs to arrive folds every other CTA's lists
+        // into its own and writes the rows.  Split requests are the first
+        // ones each CTA streams (see Walker), so this overlaps the rest of
+        // the stream.  The ticket wraps to zero on the last arrival, ready
+        // for the next call.
+        const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
+        if (n < R) {
+          ulonglong2* dst = reinterpret_cast<ulonglong2*>(
+              a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
+#pragma unroll
+          for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
+        }
+        __threadfence();
+        __syncwarp();
+        unsigned int ticket = 0;
+        if (lane == 0) ticket = atomicInc(a.tickets + req, static_cast<unsigned int>(nseg - 1));
+        ticket = __shfl_sync(0xffffffffu, ticket, 0);
+        if (ticket == static_cast<unsigned int>(nseg - 1)) {
+          __threadfence();
+          if (n < R) {
+            for (int js = 0; js < nseg; ++js) {
+              const int cj = dense ? first + js : cta_of(preq + js, total, gridDim.x);
+              if (cj == static_cast<int>(blockIdx.x)) continue;
+              const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
+                  a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + n * TK);
+              uint64_t other[TK];
+#pragma unroll
+              for (int u = 0; u < TK / 2; ++u) {
+                const ulonglong2 x = __ldcg(src + u);
+                other[2 * u] = x.x;
+                other[2 * u + 1] = x.y;
+              }
+              list.merge_sorted(other);
+            }
+            write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&h_empty[hs]);
@@ -818,58 +848,6 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   }
 }
 
-// One warp per request split across decode CTAs, lane n owning query row n:
-// the row's partial lists (one per CTA holding part of the request, each its
-// best TK candidate keys, sorted) are merged in registers -- the next slot's
-// keys load while the current one merges -- and the lane writes the row.
-// Requests held by one CTA were written by the decode kernel.
-template <int TK>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a, int grid) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int req = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (req >= a.num_reqs || lane >= a.rows_per_req) return;
-  const int nb = req_blocks(a, req);
-  if (nb == 0) return;
-  const long long total = __ldcg(a.total_blocks);
-  const long long preq = __ldcg(a.req_start + req);
-  const int first = cta_of(preq, total, grid);
-  const int last = cta_of(preq + nb - 1, total, grid);
-  const bool dense = total >= grid;
-  const int nseg = dense ? last - first + 1 : nb;
-  if (nseg == 1) return;
-  const int n = lane;
-  const int j = n / a.heads, h = n - j * a.heads;
-  const int pr = req_len(a, req) - a.query_len + j;
-  const int cr = pr >= 0 ? (pr >> 7) : -1;
-  const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
-  auto load_slot = [&](int js, uint64_t (&k)[TK]) {
-    const int cj = dense ? first + js : cta_of(preq + js, total, grid);
-    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
-        a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + n * TK);
-#pragma unroll
-    for (int u = 0; u < TK / 2; ++u) {
-      const ulonglong2 x = __ldcg(src + u);
-      k[2 * u] = x.x;
-      k[2 * u + 1] = x.y;
-    }
-  };
-  RegList<TK> list;
-  uint64_t cur[TK], nxt[TK];
-  load_slot(0, cur);
-  load_slot(1, nxt);
-#pragma unroll
-  for (int k = 0; k < TK; ++k) list.v[k] = cur[k];
-  for (int js = 1; js < nseg; ++js) {
-#pragma unroll
-    for (int k = 0; k < TK; ++k) cur[k] = nxt[k];
-    if (js + 1 < nseg) load_slot(js + 1, nxt);   // in flight while this slot merges
-    list.merge_sorted(cur);
-  }
-  write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk,
-                     a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row);
-}
-
 template <bool FP4, int MQ, int TK>
 cudaError_t launch_t(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
   using C = Cfg<FP4, MQ, TK>;
@@ -892,22 +870,6 @@ cudaError_t dispatch(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cud
 }  // namespace
 
 int decode_ctas_per_sm() { return 1; }
-
-cudaError_t launch_decode_merge(const DecodeArgs& a, int decode_grid, cudaStream_t s) {
-  const unsigned blocks = static_cast<unsigned>((a.num_reqs + 7) / 8);
-  if (blocks == 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (decode_tk(a.topk) == 16) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<16>, a, decode_grid);
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<32>, a, decode_grid);
-}
 
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s) {
   return dispatch<false>(kmap, a, grid, s);

@@ -40,8 +40,7 @@ struct DecodeArgs {
   int32_t* ids;
   int64_t i_head, i_row;
   uint64_t* partials;         // [slots, 32 rows, tk] keys
-  long long* req_start;       // [num_reqs] first flattened block of each request
-  long long* total_blocks;    // [1] blocks of the whole batch
+  unsigned int* tickets;      // [num_reqs] arrivals per split request; 0 between calls
   int32_t* status;            // device status word
 };
 
@@ -82,9 +81,6 @@ struct SelectArgs {
 // Launchers; each returns a cudaError_t of the launch.
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s);
-// Merges the partial candidate lists of requests split across decode CTAs;
-// launched right after the decode kernel as a programmatic dependent launch.
-cudaError_t launch_decode_merge(const DecodeArgs& a, int decode_grid, cudaStream_t s);
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
