@@ -794,6 +794,11 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     // ---------------------------------------------------- NVFP4 dequantiser
     if (warp >= kDeqWarp0) {  // warp 3 has no role
       const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..127 (warps 5..8)
+      // Item dq + 128*kk is token tok0 + 16*kk, scale group g (16 elements).
+      const int g = dq & 7, tok0 = dq >> 3, sw = tok0 & 7;
+      const uint32_t row_off = (g >> 2) * (kTileBytes / 2) + (tok0 >> 3) * 1024 + sw * 128;
+      const uint32_t st_off0 = row_off + ((((g & 3) * 2) ^ sw) << 4);
+      const uint32_t st_off1 = row_off + ((((g & 3) * 2 + 1) ^ sw) << 4);
       uint32_t it = 0;
       bool ok = true;
       while (ok && walker.next(a, req, b0, b1, nb, preq)) {
@@ -812,20 +817,27 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
           const uint8_t* codes = sRaw + rs * kFp4RawBytes;
           const uint8_t* scales = codes + kFp4CodeBytes;
           uint8_t* tile = sA + st * kTileBytes;
-  #pragma unroll 2
+          // Thread dq covers group g of tokens tok0 + 16*kk, kk = 0..7.  All
+          // loads are issued before any arithmetic so that the eight
+          // independent groups overlap their latencies.
+          uint2 cw[8];
+          uint32_t sc[8];
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int item = kk * 128 + dq;
-            const int tok = item >> 3, g = item & 7;
-            const uint2 cw = *reinterpret_cast<const uint2*>(codes + tok * 64 + g * 8);
-            const uint4 t = sTab[scales[tok * 8 + g]];
+            cw[kk] = *reinterpret_cast<const uint2*>(codes + kk * 1024 + dq * 8);
+            sc[kk] = scales[kk * 128 + dq];
+          }
+          uint4 t[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) t[kk] = sTab[sc[kk]];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
             uint32_t o0[4], o1[4];
-            dequant8(cw.x, t, o0);
-            dequant8(cw.y, t, o1);
-            uint8_t* rowp = tile + (g >> 2) * (kTileBytes / 2) + (tok >> 3) * 1024 + (tok & 7) * 128;
-            const int c0 = (g & 3) * 2;
-            *reinterpret_cast<uint4*>(rowp + ((c0 ^ (tok & 7)) << 4)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (tok & 7)) << 4)) =
-                make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            dequant8(cw[kk].x, t[kk], o0);
+            dequant8(cw[kk].y, t[kk], o1);
+            uint8_t* rowp = tile + kk * 2048;
+            *reinterpret_cast<uint4*>(rowp + st_off0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<uint4*>(rowp + st_off1) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
