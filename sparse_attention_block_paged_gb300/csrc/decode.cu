@@ -17,7 +17,7 @@
 //                (two 64-column boxes, 128-byte swizzle) into a ring of stages;
 //                writes each request's query rows into a swizzled Q tile.
 //                NVFP4: bulk-copies the 9 KB code+scale page into a raw ring.
-//   * warps 5-8: (NVFP4 only) dequantise raw pages into bf16 tiles in the same
+//   * warps 5+ : (NVFP4 only) dequantise raw pages into bf16 tiles in the same
 //                swizzled layout, via a per-scale-byte magnitude table.
 //   * warp 1   : one thread issues tcgen05.mma with the query rows as A
 //                (M = 64 or 128, rows past heads*query_len unused) and the page
@@ -60,12 +60,17 @@ constexpr int kFp4ScaleBytes = kBlock * kD / 16;     // 1 KB
 constexpr int kFp4RawBytes = kFp4CodeBytes + kFp4ScaleBytes;
 constexpr int kLanes = 32;                           // rows per list slot
 constexpr int kEpiA = 0, kMmaWarp = 1, kProdWarp = 2, kMergeWarp = 3, kEpiB = 4, kDeqWarp0 = 5;
+// NVFP4: warps kDeqWarp0.. dequantise.  With 16-key lists the kernel fits
+// in 128 registers per thread, so eight warps (two per SM sub-partition) can
+// overlap one warp's shared-memory latencies with another's arithmetic;
+// 32-key lists need more registers and keep four.
 
 template <bool FP4, int MQ, int TK>
 struct Cfg {
   static constexpr int kStages = FP4 ? (MQ == 64 ? 3 : 2) : (MQ == 64 ? 5 : 4);
   static constexpr int kRawStages = FP4 ? ((MQ == 64 && TK == 16) ? 8 : 6) : 0;
-  static constexpr int kThreads = FP4 ? 288 : 160;
+  static constexpr int kDeqWarps = FP4 ? (TK == 16 ? 8 : 4) : 0;
+  static constexpr int kThreads = FP4 ? (kDeqWarp0 + kDeqWarps) * 32 : 160;
   static constexpr int kQBytes = MQ * kD * 2;
   static constexpr int oA = 0;
   static constexpr int oRaw = oA + kStages * kTileBytes;
@@ -453,12 +458,12 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], FP4 ? 4 : 1);
+      mbar_init(&full[s], FP4 ? C::kDeqWarps : 1);
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < RS; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], C::kDeqWarps);
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -793,8 +798,11 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   } else if constexpr (FP4) {
     // ---------------------------------------------------- NVFP4 dequantiser
     if (warp >= kDeqWarp0) {  // warp 3 has no role
-      const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..127 (warps 5..8)
-      // Item dq + 128*kk is token tok0 + 16*kk, scale group g (16 elements).
+      constexpr int kDqThreads = C::kDeqWarps * 32;
+      const int dq = threadIdx.x - kDeqWarp0 * 32;  // 0..kDqThreads-1
+      // A page is 1024 groups of 16 elements (128 tokens x 8).  Item
+      // dq + kDqThreads*kk is token tok0 + kT*kk, scale group g.
+      constexpr int kT = kDqThreads / 8, kItems = 1024 / kDqThreads;
       const int g = dq & 7, tok0 = dq >> 3, sw = tok0 & 7;
       const uint32_t row_off = (g >> 2) * (kTileBytes / 2) + (tok0 >> 3) * 1024 + sw * 128;
       const uint32_t st_off0 = row_off + ((((g & 3) * 2) ^ sw) << 4);
@@ -817,25 +825,25 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
           const uint8_t* codes = sRaw + rs * kFp4RawBytes;
           const uint8_t* scales = codes + kFp4CodeBytes;
           uint8_t* tile = sA + st * kTileBytes;
-          // Thread dq covers group g of tokens tok0 + 16*kk, kk = 0..7.  All
-          // loads are issued before any arithmetic so that the eight
-          // independent groups overlap their latencies.
-          uint2 cw[8];
-          uint32_t sc[8];
+          // Thread dq covers group g of tokens tok0 + kT*kk.  All loads are
+          // issued before any arithmetic so that the independent groups
+          // overlap their latencies.
+          uint2 cw[kItems];
+          uint32_t sc[kItems];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            cw[kk] = *reinterpret_cast<const uint2*>(codes + kk * 1024 + dq * 8);
-            sc[kk] = scales[kk * 128 + dq];
+          for (int kk = 0; kk < kItems; ++kk) {
+            cw[kk] = *reinterpret_cast<const uint2*>(codes + kk * kT * 64 + dq * 8);
+            sc[kk] = scales[kk * kT * 8 + dq];
           }
-          uint4 t[8];
+          uint4 t[kItems];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) t[kk] = sTab[sc[kk]];
+          for (int kk = 0; kk < kItems; ++kk) t[kk] = sTab[sc[kk]];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < kItems; ++kk) {
             uint32_t o0[4], o1[4];
             dequant8(cw[kk].x, t[kk], o0);
             dequant8(cw[kk].y, t[kk], o1);
-            uint8_t* rowp = tile + kk * 2048;
+            uint8_t* rowp = tile + kk * kT * 128;
             *reinterpret_cast<uint4*>(rowp + st_off0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
             *reinterpret_cast<uint4*>(rowp + st_off1) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
           }
