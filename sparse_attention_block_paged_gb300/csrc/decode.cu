@@ -67,8 +67,11 @@ constexpr int kEpiA = 0, kMmaWarp = 1, kProdWarp = 2, kMergeWarp = 3, kEpiB = 4,
 
 template <bool FP4, int MQ, int TK>
 struct Cfg {
-  static constexpr int kStages = FP4 ? (MQ == 64 ? 3 : 2) : (MQ == 64 ? 5 : 4);
-  static constexpr int kRawStages = FP4 ? ((MQ == 64 && TK == 16) ? 8 : 6) : 0;
+  // NVFP4 raw pages arrive far ahead of their use, so shared memory goes to
+  // the bf16 stages between the dequantisers and the tensor core first.
+  static constexpr int kStages =
+      FP4 ? ((MQ == 64 && TK == 16) ? 4 : (MQ == 64 ? 3 : 2)) : (MQ == 64 ? 5 : 4);
+  static constexpr int kRawStages = FP4 ? ((MQ == 64 && TK == 16) ? 4 : 6) : 0;
   static constexpr int kDeqWarps = FP4 ? (TK == 16 ? 8 : 4) : 0;
   static constexpr int kThreads = FP4 ? (kDeqWarp0 + kDeqWarps) * 32 : 160;
   static constexpr int kQBytes = MQ * kD * 2;
@@ -805,8 +808,15 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
       constexpr int kT = kDqThreads / 8, kItems = 1024 / kDqThreads;
       const int g = dq & 7, tok0 = dq >> 3, sw = tok0 & 7;
       const uint32_t row_off = (g >> 2) * (kTileBytes / 2) + (tok0 >> 3) * 1024 + sw * 128;
-      const uint32_t st_off0 = row_off + ((((g & 3) * 2) ^ sw) << 4);
-      const uint32_t st_off1 = row_off + ((((g & 3) * 2 + 1) ^ sw) << 4);
+      // The group's two 16-byte chunks (elements 0-7 and 8-15).  Groups g and
+      // g+4 of a token share their chunk positions in the two 64-column
+      // halves, i.e. the same banks; groups g >= 4 store their chunks in the
+      // opposite order so that each store instruction hits eight distinct
+      // chunk positions per eight lanes.
+      const bool swap = g >= 4;
+      const uint32_t off_lo = row_off + ((((g & 3) * 2) ^ sw) << 4);
+      const uint32_t off_hi = row_off + ((((g & 3) * 2 + 1) ^ sw) << 4);
+      const uint32_t st_offA = swap ? off_hi : off_lo, st_offB = swap ? off_lo : off_hi;
       uint32_t it = 0;
       bool ok = true;
       while (ok && walker.next(a, req, b0, b1, nb, preq)) {
@@ -841,11 +851,11 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kItems; ++kk) {
             uint32_t o0[4], o1[4];
-            dequant8(cw[kk].x, t[kk], o0);
-            dequant8(cw[kk].y, t[kk], o1);
+            dequant8(swap ? cw[kk].y : cw[kk].x, t[kk], o0);
+            dequant8(swap ? cw[kk].x : cw[kk].y, t[kk], o1);
             uint8_t* rowp = tile + kk * kT * 128;
-            *reinterpret_cast<uint4*>(rowp + st_off0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-            *reinterpret_cast<uint4*>(rowp + st_off1) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            *reinterpret_cast<uint4*>(rowp + st_offA) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<uint4*>(rowp + st_offB) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
