@@ -482,15 +482,21 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
     misc->abort = 0;
     fence_barrier_init();
   }
-  if (warp == kProdWarp) {
-    if (!FP4 && lane == 0) prefetch_tensormap(&kmap);
-    partition(a, misc, lane);
-  }
   if (warp == kMmaWarp) {
     tmem_alloc(&misc->tmem, kTmemCols);
     tmem_relinquish();
   }
   if constexpr (FP4) build_fp4_table(sTab, threadIdx.x, C::kThreads);
+  // Launched as a programmatic dependent launch: everything above overlaps
+  // the previous kernel on the stream, whose results (lengths, tables,
+  // queries, pages) are read only after this wait.  The next kernel may be
+  // scheduled as soon as this grid's CTAs make room.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (warp == kProdWarp) {
+    if (!FP4 && lane == 0) prefetch_tensormap(&kmap);
+    partition(a, misc, lane);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -884,8 +890,17 @@ cudaError_t launch_t(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cud
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP4, MQ, TK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  decode_kernel<FP4, MQ, TK><<<grid, C::kThreads, C::kSmem, s>>>(kmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<FP4, MQ, TK>, kmap, a);
 }
 
 template <bool FP4>
