@@ -76,6 +76,9 @@ def _load():
         lib.mm3o_select_problem.argtypes = [_P, _I64, _I64, _I32, _P, _I32, _I32,
                                             _I32, _I32, _I32, _P]
         lib.mm3o_select_problem.restype = _I32
+        lib.mm3o_sparse_table.argtypes = [_P, _I32, _P, _I32, _I32, _P, _I64, _I32, _I32, _P,
+                                          _I64, _P]
+        lib.mm3o_sparse_table.restype = _I32
         _lib = lib
         return lib
 
@@ -197,6 +200,25 @@ def select_problem(scores: np.ndarray, seq_lens: np.ndarray, query_len: int,
                                    query_len, topk, init_blocks, local_blocks, _ptr(ids)):
         raise ValueError("oracle: forced blocks exceed topk")
     return ids
+
+
+def sparse_table(ids: np.ndarray, seq_lens: np.ndarray, query_len: int,
+                 attention_block_table: np.ndarray, pages_per_block: int,
+                 block_page_stride: int):
+    """Sparse page table [rows, topk * pages_per_block] (int32, -1 in unused
+    slots) and sparse context lengths [rows] (int32) of one head's ids
+    [rows, topk], through the attention block table [num_reqs, >= blocks]."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    rows, topk = ids.shape
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    at = np.ascontiguousarray(attention_block_table, dtype=np.int32)
+    table = np.empty((rows, topk * pages_per_block), dtype=np.int32)
+    ctx = np.empty((rows,), dtype=np.int32)
+    if _load().mm3o_sparse_table(_ptr(ids), topk, _ptr(sl), sl.shape[0], query_len, _ptr(at),
+                                 at.shape[1], pages_per_block, block_page_stride, _ptr(table),
+                                 table.shape[1], _ptr(ctx)):
+        raise ValueError("oracle: an id past the row's visible blocks")
+    return table, ctx
 
 
 def subset(wl, reqs):

@@ -24,6 +24,10 @@
  *     indexer_context_scores: scores are scaled by sm_scale.
  *   - vllm.models.minimax_m3.amd.indexer_nvfp4, module docstring: an NVFP4
  *     key element is e4m3_rn_satfinite(e2m1 * scale).
+ *   - index_topk page, minimax_m3_index_decode, the sparse-table arguments:
+ *     the page table of the block-sparse attention built from one head's
+ *     ids (shapes from the pages, mapping read as stated at
+ *     mm3o_sparse_table).
  *
  * Readings where the pages are silent (the same list is kept with the
  * design notes): score = sm_scale * max (natural units, no log2(e)); query j
@@ -397,6 +401,59 @@ int mm3o_select_problem(const double *scores, int64_t head_stride,
                                 topk, init_blocks, local_blocks,
                                 ids + ((int64_t)h * rows + row) * topk))
                     return -1;
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------ sparse page table */
+
+/* The page table of the block-sparse attention that follows the selection,
+ * for one index head (index_topk page, minimax_m3_index_decode: the
+ * sparse-table arguments attention_block_table [num_reqs, >= blocks],
+ * sparse_block_table_out [total_q, topk * PAGES_PER_SPARSE_BLOCK],
+ * sparse_context_lens_out [total_q], block_page_stride equal to one or two
+ * times PAGES_PER_SPARSE_BLOCK, one index head only).
+ *
+ * The pages give the shapes but not the mapping; the reading taken here:
+ *   - a sparse block of 128 tokens spans P = pages_per_block attention pages
+ *     of 128 / P tokens;
+ *   - attention_block_table[i, b] is the physical block holding logical
+ *     block b of request i, and that block's pages are
+ *     attention_block_table[i, b] * block_page_stride + 0 .. P-1;
+ *   - slot k of row r (the k-th id of the row, ascending) holds the P pages
+ *     of that block at columns k*P .. k*P+P-1; slots whose id is -1 hold -1;
+ *   - the context length of row r is the number of key tokens the row sees
+ *     (0..pos) that lie in its selected blocks: the selected blocks laid end
+ *     to end, the last of them cut at pos.
+ * ids: [rows, topk] of one head, as the selection writes them. */
+int mm3o_sparse_table(const int32_t *ids, int topk, const int32_t *seq_lens,
+                      int num_reqs, int query_len, const int32_t *attn_table,
+                      int64_t attn_stride, int pages_per_block,
+                      int block_page_stride, int32_t *table_out,
+                      int64_t table_stride, int32_t *ctx_out)
+{
+    for (int i = 0; i < num_reqs; ++i)
+        for (int j = 0; j < query_len; ++j) {
+            int64_t row = (int64_t)i * query_len + j;
+            int64_t pos = (int64_t)seq_lens[i] - query_len + j;
+            const int32_t *id = ids + row * topk;
+            int32_t *t = table_out + row * table_stride;
+            int64_t ctx = 0;
+            for (int k = 0; k < topk; ++k) {
+                int32_t b = id[k];
+                for (int p = 0; p < pages_per_block; ++p)
+                    t[(int64_t)k * pages_per_block + p] =
+                        b < 0 ? -1
+                              : (int32_t)((int64_t)attn_table[i * attn_stride + b] *
+                                          block_page_stride + p);
+                if (b < 0)
+                    continue;
+                if ((int64_t)b * MM3O_BLOCK > pos)
+                    return -1; /* not a visible block */
+                int64_t last = (int64_t)b * MM3O_BLOCK + MM3O_BLOCK - 1;
+                ctx += (last < pos ? last : pos) - (int64_t)b * MM3O_BLOCK + 1;
+            }
+            ctx_out[row] = (int32_t)ctx;
         }
     return 0;
 }

@@ -360,3 +360,77 @@ def test_nvfp4_subnormal_results():
     assert oracle.nvfp4_value(3, tiny) == 2.0 ** -8
     assert oracle.nvfp4_value(2, tiny) == 2.0 ** -9
     assert oracle.nvfp4_value(7, tiny) == 6 * 2.0 ** -9
+
+
+# ------------------------------------------------------- sparse page table
+
+def test_sparse_table_by_hand():
+    # seq 300, one query: pos 299, blocks 0..2 (the last holds tokens 256..299).
+    # Attention blocks 7, 3, 9; two pages per block, four pages between blocks:
+    # block 7 -> pages 28, 29; block 3 -> 12, 13; block 9 -> 36, 37.
+    t, c = oracle.sparse_table(np.array([[0, 1, 2, -1]]), np.array([300]), 1,
+                               np.array([[7, 3, 9]]), 2, 4)
+    assert t.tolist() == [[28, 29, 12, 13, 36, 37, -1, -1]]
+    assert c.tolist() == [128 + 128 + 44]
+    # seq 700: pos 699 in block 5 (tokens 640..699, 60 of them); blocks 0, 2,
+    # 4, 5 selected; one page per block, two pages between blocks.
+    t, c = oracle.sparse_table(np.array([[0, 2, 4, 5]]), np.array([700]), 1,
+                               np.array([[10, 11, 12, 13, 14, 15]]), 1, 2)
+    assert t.tolist() == [[20, 24, 28, 30]]
+    assert c.tolist() == [3 * 128 + 60]
+
+
+def _walk_sparse_attention(table_row, ctx, pages_per_block, attn_row, block_page_stride):
+    """(logical token) read by a paged attention that walks `ctx` tokens of the
+    compacted table, inverted through the attention cache layout: page
+    attn_row[b] * stride + p holds tokens 128 b + p * (128 / P) ...  of block b."""
+    per_page = BLOCK // pages_per_block
+    where = {}
+    for b, blk in enumerate(attn_row):
+        for p in range(pages_per_block):
+            where[int(blk) * block_page_stride + p] = (b, p)
+    out = []
+    for u in range(ctx):
+        b, p = where[int(table_row[u // per_page])]
+        out.append(b * BLOCK + p * per_page + u % per_page)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("pages_per_block,stride_mul", [(1, 1), (2, 1), (2, 2), (4, 2), (8, 1)])
+def test_sparse_table_walk_reads_exactly_the_selected_visible_tokens(seed, pages_per_block,
+                                                                      stride_mul):
+    wl = _small(seed, heads=1, topk=6)
+    _, ids = oracle.problem(wl)
+    rng = np.random.default_rng(100 + seed)
+    nblk = wl.block_table.shape[1]
+    # distinct physical blocks per request, so the layout can be inverted
+    attn = np.stack([rng.permutation(4 * nblk)[:nblk] for _ in range(wl.num_reqs)]).astype(np.int32)
+    stride = stride_mul * pages_per_block
+    table, ctx = oracle.sparse_table(ids[0], wl.seq_lens, wl.query_len, attn, pages_per_block,
+                                     stride)
+    for r in range(wl.rows):
+        i, j = divmod(r, wl.query_len)
+        pos = int(wl.seq_lens[i]) - wl.query_len + j
+        sel = set(int(b) for b in ids[0, r] if b >= 0)
+        want = [t for t in range(pos + 1) if t // BLOCK in sel]    # token-level enumeration
+        assert _walk_sparse_attention(table[r], int(ctx[r]), pages_per_block, attn[i],
+                                      stride) == want
+        n = len(sel)
+        assert np.all(table[r, n * pages_per_block:] == -1)
+
+
+def test_sparse_table_full_selection_and_identity_layout():
+    # every visible block kept (nb <= topk): the sparse context is the whole
+    # causal context pos + 1; with one page per block and stride 1 the table
+    # row is the attention table's entries for the ids
+    wl = _small(3, heads=1, topk=16, min_len=130, max_len=1500)
+    _, ids = oracle.problem(wl)
+    table, ctx = oracle.sparse_table(ids[0], wl.seq_lens, wl.query_len, wl.block_table, 1, 1)
+    for r in range(wl.rows):
+        i, j = divmod(r, wl.query_len)
+        pos = int(wl.seq_lens[i]) - wl.query_len + j
+        assert pos // BLOCK + 1 <= wl.topk
+        assert int(ctx[r]) == pos + 1
+        valid = ids[0, r][ids[0, r] >= 0]
+        assert table[r, :len(valid)].tolist() == wl.block_table[i, valid].tolist()
