@@ -189,6 +189,34 @@ def problem(wl, *, want_scores: bool = True, out_width: int | None = None):
     return scores, ids
 
 
+def problem_ragged(wl, *, want_scores: bool = True, out_width: int | None = None):
+    """problem() of a ragged batch (wl.cu_seqlens set): every request is its
+    own uniform problem of cu[i+1] - cu[i] query rows (index_topk,
+    minimax_m3_index_score: cu_seqlens_q and prefix_lens give each request's
+    query rows and their positions), and the rows are laid out in cu order."""
+    import copy
+    cu = wl.cu_seqlens
+    H, R = wl.heads, wl.rows
+    W = out_width if out_width is not None else wl.width
+    scores = np.full((H, R, W), -np.inf) if want_scores else None
+    ids = np.empty((H, R, wl.topk), dtype=np.int32)
+    for i in range(wl.num_reqs):
+        lo, hi = int(cu[i]), int(cu[i + 1])
+        if hi == lo:
+            continue
+        sub = copy.copy(wl)
+        sub.cu_seqlens = None
+        sub.query_len = hi - lo
+        sub.seq_lens = wl.seq_lens[i:i + 1].copy()
+        sub.block_table = wl.block_table[i:i + 1].copy()
+        sub.q = wl.q[lo:hi].copy()
+        s, k = problem(sub, want_scores=want_scores, out_width=W)
+        if want_scores:
+            scores[:, lo:hi] = s
+        ids[:, lo:hi] = k
+    return scores, ids
+
+
 def select_problem(scores: np.ndarray, seq_lens: np.ndarray, query_len: int,
                    topk: int, init_blocks: int, local_blocks: int) -> np.ndarray:
     """Ids [heads, rows, topk] selected from a given score tensor [heads, rows, W]."""

@@ -28,6 +28,9 @@ def brute_force(wl, scale=None):
     H, R = wl.heads, wl.rows
     scores = np.full((H, R, wl.width), -np.inf)
     ids = np.full((H, R, wl.topk), -1, dtype=np.int32)
+    # query rows of request i: cu[i] .. cu[i+1]-1 (ragged) or query_len each
+    cu = (wl.cu_seqlens if wl.cu_seqlens is not None
+          else np.arange(wl.num_reqs + 1) * wl.query_len)
     for i in range(wl.num_reqs):
         nbmax = -(-int(wl.seq_lens[i]) // BLOCK)
         if nbmax == 0:
@@ -38,9 +41,10 @@ def brute_force(wl, scale=None):
             pages = oracle.nvfp4_dequant_bf16(wl.codes[wl.block_table[i, :nbmax]],
                                               wl.scales[wl.block_table[i, :nbmax]])
         keys = W.bf16_to_f32(pages).astype(np.float64).reshape(nbmax * BLOCK, 128)
-        for j in range(wl.query_len):
-            r = i * wl.query_len + j
-            pos = int(wl.seq_lens[i]) - wl.query_len + j
+        ql = int(cu[i + 1] - cu[i])
+        for j in range(ql):
+            r = int(cu[i]) + j
+            pos = int(wl.seq_lens[i]) - ql + j
             if pos < 0:
                 continue
             q = W.bf16_to_f32(wl.q[r]).astype(np.float64)          # [H, 128]
@@ -434,3 +438,46 @@ def test_sparse_table_full_selection_and_identity_layout():
         assert int(ctx[r]) == pos + 1
         valid = ids[0, r][ids[0, r] >= 0]
         assert table[r, :len(valid)].tolist() == wl.block_table[i, valid].tolist()
+
+
+# ------------------------------------------------------------ ragged batches
+
+def ragged_tiny_cases():
+    rng = np.random.default_rng(11)
+    cases = []
+    for k in range(60):
+        n = int(rng.integers(1, 5))
+        ql = [int(rng.choice([0, 1, 2, 5, 130, 131])) for _ in range(n)]
+        pre = [int(rng.integers(0, 4)) * BLOCK + int(rng.integers(-2, 3)) for _ in range(n)]
+        pre = [max(0, p) for p in pre]
+        if sum(ql) == 0:
+            ql[0] = 3
+        topk = int(rng.choice([2, 4, 6]))
+        cases.append(dict(seed=20_000 + k, query_lens=ql, prefix_lens=pre,
+                          heads=int(rng.choice([1, 2])), topk=topk, init_blocks=1,
+                          local_blocks=int(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", ragged_tiny_cases(), ids=lambda c: str(c["seed"]))
+def test_ragged_oracle_matches_brute_force(case):
+    wl = W.ragged_case(**case)
+    s_o, i_o = oracle.problem_ragged(wl)
+    s_b, i_b = brute_force(wl)
+    fin = np.isfinite(s_b)
+    assert np.array_equal(np.isfinite(s_o), fin)
+    np.testing.assert_allclose(s_o[fin], s_b[fin], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(i_o, i_b)
+
+
+def test_ragged_with_equal_counts_is_the_uniform_batch():
+    wl = W.ragged_case(5, query_lens=[3, 3, 3], prefix_lens=[200, 700, 1000], heads=2, topk=5,
+                       init_blocks=1, local_blocks=2)
+    s_r, i_r = oracle.problem_ragged(wl)
+    import copy
+    u = copy.copy(wl)
+    u.cu_seqlens = None
+    u.query_len = 3
+    s_u, i_u = oracle.problem(u)
+    np.testing.assert_array_equal(i_r, i_u)
+    np.testing.assert_array_equal(s_r, s_u)

@@ -73,6 +73,9 @@ class Workload:
     cache: np.ndarray | None = None    # uint16 [pages, 128, 128]
     codes: np.ndarray | None = None    # uint8  [pages, 128, 64]
     scales: np.ndarray | None = None   # uint8  [pages, 128, 8]
+    # ragged batches: int32 [num_reqs + 1] query-row offsets (query_len then
+    # holds the largest per-request count); None: query_len rows per request
+    cu_seqlens: np.ndarray | None = None
 
     @property
     def num_reqs(self) -> int:
@@ -80,6 +83,8 @@ class Workload:
 
     @property
     def rows(self) -> int:
+        if self.cu_seqlens is not None:
+            return int(self.cu_seqlens[-1])
         return self.num_reqs * self.query_len
 
     @property
@@ -199,10 +204,12 @@ def nvfp4_encode(x: np.ndarray):
 def build(name, *, seed, seq_lens, query_len, heads, topk, init_blocks,
           local_blocks, max_seq_len, sm_scale=1.0 / math.sqrt(128.0),
           kv_format="bf16", block_offset_std=0.0, pool_pages=None,
-          poison=True):
+          poison=True, query_lens=None):
     """Draw a workload with the given shape.  default_rng(seed) draws the
     block-table permutation and the block offsets; keys and queries come from
-    the child streams of SeedSequence([seed, 1]) and ([seed, 2])."""
+    the child streams of SeedSequence([seed, 1]) and ([seed, 2]).  With
+    ``query_lens`` (one count per request) the batch is ragged: request i
+    owns query rows cu[i]..cu[i+1]-1 at positions seq_len - count + j."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     table, pages = _deal_pages(rng, seq_lens, max_seq_len, pool_pages)
@@ -243,7 +250,13 @@ def build(name, *, seed, seq_lens, query_len, heads, topk, init_blocks,
         wl.codes, wl.scales = codes, scales
     else:
         raise ValueError(kv_format)
-    tokens = len(seq_lens) * query_len
+    if query_lens is not None:
+        ql = np.asarray(query_lens, dtype=np.int64)
+        wl.cu_seqlens = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        wl.query_len = int(ql.max()) if len(ql) else 1
+        tokens = int(wl.cu_seqlens[-1])
+    else:
+        tokens = len(seq_lens) * query_len
     wl.q = _normal_bf16([seed, 2], (tokens, heads, D))
     return wl
 
@@ -285,7 +298,15 @@ def _nvfp4_decode(seed=4, num_reqs=128):
                  max_seq_len=131072, kv_format="nvfp4")
 
 
-# The five named workloads, by short key.  The second argument of each maker
+def _nvfp4_prefill(seed=5, seq=32768):
+    """The causal prefill over NVFP4 keys (indexer_nvfp4 prefill branch);
+    not one of the five named configurations."""
+    return build("NVFP4 causal prefill", seed=seed, seq_lens=[seq], query_len=seq,
+                 heads=1, topk=16, init_blocks=1, local_blocks=2,
+                 max_seq_len=seq, kv_format="nvfp4")
+
+
+# The five named workloads, by short key, and the NVFP4 prefill.  The second argument of each maker
 # (request count / sequence length) lets tests draw a smaller case with the
 # same recipe.
 WORKLOADS = {
@@ -294,6 +315,7 @@ WORKLOADS = {
     "high_batch": _high_batch,
     "prefill": _causal_prefill,
     "nvfp4_decode": _nvfp4_decode,
+    "nvfp4_prefill": _nvfp4_prefill,
 }
 
 
@@ -315,3 +337,34 @@ def random_case(seed, *, num_reqs, query_len, heads, topk, init_blocks,
                  local_blocks=local_blocks, max_seq_len=msl,
                  sm_scale=sm_scale if sm_scale is not None else 1.0 / math.sqrt(128.0),
                  kv_format=kv_format, block_offset_std=block_offset_std)
+
+
+def ragged_case(seed, *, query_lens, prefix_lens, heads, topk, init_blocks, local_blocks,
+                max_seq_len=None, kv_format="bf16", sm_scale=None):
+    """A ragged batch: request i has query_lens[i] new tokens after
+    prefix_lens[i] earlier ones (seq_len = prefix + count)."""
+    ql = np.asarray(query_lens, dtype=np.int64)
+    seq = (np.asarray(prefix_lens, dtype=np.int64) + ql).astype(np.int32)
+    msl = max_seq_len or int(max(1, seq.max()))
+    return build(f"ragged-{seed}", seed=seed, seq_lens=seq, query_len=1, heads=heads,
+                 topk=topk, init_blocks=init_blocks, local_blocks=local_blocks,
+                 max_seq_len=msl,
+                 sm_scale=sm_scale if sm_scale is not None else 1.0 / math.sqrt(128.0),
+                 kv_format=kv_format, query_lens=ql)
+
+
+def attention_block_table(wl: Workload, seed: int, spare: int = 3) -> np.ndarray:
+    """A seeded attention block table for the sparse page table: int32
+    ``[num_reqs, width]``, the blocks a request uses drawn without
+    repetition from a pool ``spare`` times the need; entries a request does
+    not use hold -7777 (never to be read)."""
+    rng = np.random.default_rng(90_000 + seed)
+    width = wl.block_table.shape[1]
+    used = [min(width, -(-int(max(s, 0)) // 128)) for s in wl.seq_lens]
+    pool = rng.permutation(max(1, spare * sum(used))).astype(np.int32)
+    out = np.full((wl.num_reqs, width), -7777, dtype=np.int32)
+    k = 0
+    for i, n in enumerate(used):
+        out[i, :n] = pool[k:k + n]
+        k += n
+    return out
