@@ -8,8 +8,9 @@ pool 1.25x the need.  Inputs are resident in HBM; the L2 is flushed (a read of
 a 2x-L2 buffer) before every timed step and the flush is not timed.
 
 Printed: one JSON line with rows/s (value), the roofline of the decode kernel
-against the measured HBM copy bandwidth, the CPU oracle timed on host cores,
-an end-to-end figure through the public API with host buffers, clocks sampled
+against the measured HBM copy bandwidth, the CPU oracle timed on one host
+core and on all of them, the same decode replayed from a CUDA graph, an
+end-to-end figure through the public API with host buffers, clocks sampled
 during the run, and (under "extra") the other named workloads: high-batch
 decode, NVFP4 decode and causal prefill (tensor-core scorer + selector).
 
@@ -56,7 +57,8 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the CPU oracle sample")
-    ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill"],
+    ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill", "nvfp4_prefill",
+                                       "chunked_prefill"],
                     help="run just this extra workload and print its result (for profiling)")
     return ap.parse_args()
 
@@ -160,8 +162,10 @@ def decode_bytes(wl):
 def prefill_flops(wl):
     """2 * 128 * (visible keys of every query row), token-level causal."""
     pos = []
-    for s in wl.seq_lens.astype(np.int64):
-        start = s - wl.query_len
+    for i, s in enumerate(wl.seq_lens.astype(np.int64)):
+        ql = (int(wl.cu_seqlens[i + 1] - wl.cu_seqlens[i]) if wl.cu_seqlens is not None
+              else wl.query_len)
+        start = s - ql
         pos.append((s * (s + 1) - start * (start + 1)) // 2)   # sum of (p+1) over rows
     return 2.0 * 128 * float(sum(pos)) * wl.heads
 
@@ -220,6 +224,25 @@ def bench_decode(mm, torch, wl, steps, warmup, flush, stream, pk, min_warm_s=0.0
     return res, d, out, ws, kw, sources
 
 
+def bench_graph(mm, torch, wl, d, kw, steps, flush, stream):
+    """The same decode captured once in a CUDA graph and replayed: per-replay
+    CUDA-event times with the L2 flushed (untimed) before each replay."""
+    g = torch.cuda.CUDAGraph()
+    kw = dict(kw)
+    with torch.cuda.stream(stream):
+        kw["stream"] = stream
+        mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)   # warm, outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            kw["stream"] = torch.cuda.current_stream()
+            mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+        ms = timed_steps(torch, g.replay, steps, 3, flush, stream)
+    assert mm.get_device_error(stream) == 0, "device status word set"
+    t = statistics.mean(ms) * 1e-3
+    return dict(value=wl.rows / t, unit="rows/s", ms_per_step=t * 1e3,
+                ms_median=statistics.median(ms), steps=steps)
+
+
 def bench_e2e(mm, torch, wl, d, out, ws, kw, steps, warmup, flush, stream):
     """Same decode through the public API with host buffers: H2D of the step's
     queries, block table and lengths from pinned memory, the call, D2H of ids."""
@@ -243,24 +266,74 @@ def bench_e2e(mm, torch, wl, d, out, ws, kw, steps, warmup, flush, stream):
                 d2h_bytes_per_step=int(o_h.nbytes))
 
 
+def bench_sparse_table(mm, torch, wl, steps, flush, stream):
+    """The headline decode with the sparse page table (2 pages per block,
+    stride 4) against the plain decode, both timed the same way."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = device_inputs(wl, torch, dev)
+    attn = torch.from_numpy(W_attention_table(wl)).to(dev)
+    st = torch.empty((wl.rows, wl.topk * 2), dtype=torch.int32, device=dev)
+    ctx = torch.empty((wl.rows,), dtype=torch.int32, device=dev)
+    out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
+    ws = mm.new_workspace(mm.OP_DECODE, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len,
+                          wl.topk, dev)
+    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+              init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale,
+              out=out, workspace=ws, stream=stream)
+    fn = lambda: mm.decode_sparse_table(d["q"], d["cache"], d["table"], d["lens"], **kw,  # noqa: E731
+                                        attention_block_table=attn, sparse_block_table_out=st,
+                                        sparse_context_lens_out=ctx, block_page_stride=4,
+                                        pages_per_block=2)
+    with torch.cuda.stream(stream):
+        ms = timed_steps(torch, fn, steps, 3, flush, stream)
+    assert mm.get_device_error(stream) == 0, "device status word set"
+    t = statistics.mean(ms) * 1e-3
+    return dict(value=wl.rows / t, unit="rows/s", ms_per_step=t * 1e3, steps=steps,
+                pages_per_block=2, block_page_stride=4, workload=wl.name + " + sparse page table")
+
+
+def W_attention_table(wl):
+    import workloads as W
+    return W.attention_block_table(wl, 1)
+
+
 def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
     dev = torch.device("cuda", torch.cuda.current_device())
     d = device_inputs(wl, torch, dev)
     out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
-    n = mm.workspace_bytes(mm.OP_PREFILL, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len,
-                           wl.topk)
+    nvfp4 = wl.kv_format == "nvfp4"
+    ragged = wl.cu_seqlens is not None
+    n = mm.workspace_bytes(mm.OP_PREFILL_NVFP4 if nvfp4 else mm.OP_PREFILL, wl.heads, wl.num_reqs,
+                           wl.query_len, wl.max_seq_len, wl.topk)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
-    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, topk=wl.topk,
+    kw = dict(max_seq_len=wl.max_seq_len, topk=wl.topk,
               init_blocks=wl.init_blocks, local_blocks=wl.local_blocks, sm_scale=wl.sm_scale,
               out=out, workspace=ws, stream=stream)
-    fn = lambda: mm.prefill(d["q"], d["cache"], d["table"], d["lens"], **kw)  # noqa: E731
+    cache = d["codes"] if nvfp4 else d["cache"]
+    if ragged:
+        cu = torch.from_numpy(wl.cu_seqlens).to(dev)
+        fn = lambda: mm.prefill_ragged(d["q"], cache, d["table"], d["lens"], cu,  # noqa: E731
+                                       max_query_len=wl.query_len, index_scales=d.get("scales"),
+                                       **kw)
+    elif nvfp4:
+        fn = lambda: mm.prefill_nvfp4(d["q"], cache, d["scales"], d["table"], d["lens"],  # noqa: E731
+                                      query_len=wl.query_len, **kw)
+    else:
+        fn = lambda: mm.prefill(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len, **kw)  # noqa: E731
     with torch.cuda.stream(stream):
         ms_all = timed_steps(torch, fn, steps, warmup, flush, stream)
         w = (-(-wl.max_seq_len // BLOCK) + 3) // 4 * 4
         sc = ws.view(torch.float32)[: wl.heads * wl.rows * w].view(wl.heads, wl.rows, w)
-        sel = lambda: mm.topk(sc, d["lens"], query_len=wl.query_len, max_seq_len=wl.max_seq_len,  # noqa: E731
-                              topk=wl.topk, init_blocks=wl.init_blocks,
-                              local_blocks=wl.local_blocks, out=out, stream=stream)
+        if ragged:
+            sel = lambda: mm.topk_ragged(sc, d["lens"], cu, max_query_len=wl.query_len,  # noqa: E731
+                                         max_seq_len=wl.max_seq_len, topk=wl.topk,
+                                         init_blocks=wl.init_blocks,
+                                         local_blocks=wl.local_blocks, out=out, stream=stream)
+        else:
+            sel = lambda: mm.topk(sc, d["lens"], query_len=wl.query_len,  # noqa: E731
+                                  max_seq_len=wl.max_seq_len, topk=wl.topk,
+                                  init_blocks=wl.init_blocks, local_blocks=wl.local_blocks,
+                                  out=out, stream=stream)
         ms_sel = timed_steps(torch, sel, steps, warmup, flush, stream)
     assert mm.get_device_error(stream) == 0, "device status word set"
     t_all = statistics.mean(ms_all) * 1e-3
@@ -298,6 +371,39 @@ def cpu_baseline(wl, seconds):
                        f"request by request, {el:.1f} s on one host core")
 
 
+def cpu_baseline_all_cores(wl, seconds):
+    """The same oracle call, one request per task, on a thread per host core
+    (the C oracle runs with the interpreter lock released).  The ids of the
+    first requests are checked against a single-threaded run of the same
+    requests."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    cores = os.cpu_count() or 1
+    check = min(wl.num_reqs, 2 * cores)
+    want = {i: oracle.problem(oracle.subset(wl, [i]), want_scores=False)[1]
+            for i in range(check)}
+
+    def one(i):
+        return i, oracle.problem(oracle.subset(wl, [i % wl.num_reqs]), want_scores=False)[1]
+
+    rows, done, same = 0, 0, True
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        while True:
+            for i, ids in ex.map(one, range(done, done + 4 * cores)):
+                rows += ids.shape[1]
+                if i in want:
+                    same = same and bool(np.array_equal(ids, want[i]))
+            done += 4 * cores
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    return dict(value=rows / el, unit="rows/s", cores=cores, kind="oracle",
+                identical_to_single_core=same,
+                sample=f"{done} requests ({rows} rows) of the {wl.name} workload, "
+                       f"one request per task on {cores} threads, {el:.1f} s")
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -323,7 +429,7 @@ def run_ours(args):
 
     if args.only:
         w = W.make(args.only)
-        if args.only == "prefill":
+        if args.only in ("prefill", "nvfp4_prefill", "chunked_prefill"):
             r = bench_prefill(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
         else:
             r = bench_decode(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)[0]
@@ -349,6 +455,7 @@ def run_ours(args):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         t = float(tt.item())
     e2e = bench_e2e(mm, torch, wl, d, out, ws, kw, args.steps, max(args.warmup, 3), flush, stream)
+    graph = bench_graph(mm, torch, wl, d, kw, args.steps, flush, stream)
     extra = {}
     if not args.no_extra and rank == 0:
         for key in ("high_batch", "nvfp4_decode"):
@@ -362,6 +469,22 @@ def run_ours(args):
         r4 = bench_prefill(mm, torch, w4, max(10, args.steps // 10), 3, flush, stream, pk)
         r4["workload"] = w4.name
         extra["prefill"] = r4
+        del w4
+        w5 = W.make("nvfp4_prefill")
+        r5 = bench_prefill(mm, torch, w5, max(10, args.steps // 10), 3, flush, stream, pk)
+        r5["workload"] = w5.name
+        r5["unit"] = "TFLOP/s (dequant + scorer)"
+        r5["roofline"]["traffic"] = None      # two kernels; the summaries cover the bf16 scorer
+        extra["nvfp4_prefill"] = r5
+        del w5
+        w6 = W.make("chunked_prefill")
+        r6 = bench_prefill(mm, torch, w6, max(10, args.steps // 10), 3, flush, stream, pk)
+        r6["workload"] = w6.name
+        r6["roofline"]["traffic"] = None      # not the workload the scorer summary was taken on
+        extra["chunked_prefill"] = r6
+        del w6
+        extra["sparse_table"] = bench_sparse_table(mm, torch, wl, max(20, args.steps // 4), flush,
+                                                   stream)
     clk = clocks.stop()
     if rank != 0:
         torch.distributed.destroy_process_group()
@@ -386,7 +509,9 @@ def run_ours(args):
                    "l2": "flushed before each timed step (read of a 2x-L2 buffer), flush not timed"},
         "roofline": res["roofline"],
         "cpu_baseline": cpu_baseline(wl, args.cpu_seconds),
+        "cpu_baseline_all_cores": cpu_baseline_all_cores(wl, args.cpu_seconds / 2),
         "e2e": e2e,
+        "graph_replay": graph,
         "gpu_launches": args.steps,
         "clocks": clk,
         "extra": extra,

@@ -86,6 +86,7 @@ extern "C" {
 #define MM3IDX_DEV_SEQ_TOO_LONG  2  /* seq_lens[i] > max_seq_len (clamped)  */
 #define MM3IDX_DEV_SEQ_TOO_SHORT 4  /* seq_lens[i] < query_len              */
 #define MM3IDX_DEV_TIMEOUT       8  /* an on-chip pipeline wait gave up; outputs of that launch are invalid */
+#define MM3IDX_DEV_BAD_ROWS     16  /* ragged calls: cu_seqlens_q does not run from 0 to total_q without decreasing */
 
 #define MM3IDX_MAX_TOPK            32  /* largest topk served                  */
 #define MM3IDX_MAX_DECODE_ROWS     32  /* heads * query_len limit of the fused decode kernel */
@@ -93,6 +94,7 @@ extern "C" {
 /* workspace kinds for mm3idx_workspace_bytes */
 #define MM3IDX_OP_DECODE   1
 #define MM3IDX_OP_PREFILL  2
+#define MM3IDX_OP_PREFILL_NVFP4 3
 
 /* The problem every scoring call reads.  Host struct; the pointers in it are
  * device pointers. */
@@ -153,6 +155,9 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
  * top-k candidate lists of requests split across CTAs (depends on the
  * current device's SM count).
  * op = MM3IDX_OP_PREFILL: the fp32 score scratch [heads, rows, roundup(cdiv(max_seq_len,128), 4)].
+ * op = MM3IDX_OP_PREFILL_NVFP4: that scratch (rounded up to 256 bytes), then
+ * a bf16 copy of the keys [num_reqs * cdiv(max_seq_len,128), 128, 128] and
+ * an int32 table [num_reqs, cdiv(max_seq_len,128)].
  * Writes the size to *bytes.  Reads the current device's attributes; no
  * allocation.
  */
@@ -192,6 +197,57 @@ int mm3idx_decode_nvfp4(const mm3idx_problem_t *p, int32_t topk,
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The page table of the block-sparse attention that reads the selected
+ * blocks (index_topk, minimax_m3_index_decode: attention_block_table,
+ * sparse_block_table_out, sparse_context_lens_out, block_page_stride; the
+ * pages fix their shapes, P or 2P for the stride and one index head, but not
+ * the mapping, which is read as follows).  A 128-token block spans
+ * P = pages_per_block attention pages of 128 / P tokens.  Logical block b of
+ * request i lives in attention block attention_block_table[i, b], whose pages
+ * are attention_block_table[i, b] * block_page_stride + 0 .. P-1 (stride 2P:
+ * every attention block also spans P pages of something else, e.g. values).
+ * Row r of the output (total_q rows) holds, at columns k*P .. k*P+P-1, the
+ * pages of the row's k-th id (ids ascending, as in `out`), and -1 in the
+ * slots whose id is -1.  sparse_context_lens_out[r] is the number of key
+ * tokens the row sees (0..pos) that lie in its selected blocks: the selected
+ * blocks laid end to end, the last one cut at pos.  Entries times
+ * block_page_stride plus P must fit in int32.
+ */
+typedef struct mm3idx_sparse_table {
+    const int32_t *attention_block_table;  /* int32 [num_reqs, attention_table_stride]     */
+    int64_t        attention_table_stride; /* elements between rows, >= attention_table_width */
+    int32_t        attention_table_width;  /* readable columns, >= cdiv(max_seq_len, 128)  */
+    int32_t        pages_per_block;        /* P: 1..128, a divisor of 128                   */
+    int32_t        block_page_stride;      /* P or 2 * P                                    */
+    int32_t       *sparse_block_table_out; /* int32 [total_q, sparse_table_stride]; columns
+                                              0 .. topk*P-1 written                         */
+    int64_t        sparse_table_stride;    /* >= topk * P                                   */
+    int32_t       *sparse_context_lens_out;/* int32 [total_q]                               */
+} mm3idx_sparse_table_t;
+
+/*
+ * mm3idx_decode_sparse_table -- mm3idx_decode (bf16 cache, p->index_scales
+ * NULL) or mm3idx_decode_nvfp4 (p->index_scales set) that also writes the
+ * sparse page table of its ids, from a second kernel launched on `stream`
+ * as a programmatic dependent of the decode (it waits for the ids on the
+ * GPU, without a launch gap).  Requires p->heads == 1
+ * (MM3IDX_ERR_UNSUPPORTED otherwise).  `table` is required and, unless the
+ * batch is empty, so is every pointer in it (MM3IDX_ERR_INVALID_ARGUMENT,
+ * as is a pages_per_block that does not divide
+ * 128 or a stride other than P or 2P); attention_table_width below
+ * cdiv(max_seq_len, 128) gives MM3IDX_ERR_TABLE_LAYOUT, sparse_table_stride
+ * below topk * P MM3IDX_ERR_OUT_LAYOUT.  Workspace and other rules as
+ * mm3idx_decode.
+ */
+int mm3idx_decode_sparse_table(const mm3idx_problem_t *p, int32_t topk,
+                               int32_t init_blocks, int32_t local_blocks,
+                               int32_t *out, int64_t out_head_stride,
+                               int64_t out_row_stride,
+                               const mm3idx_sparse_table_t *table,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
  * mm3idx_prefill -- prefill scoring on the tensor cores followed by the
  * selector (index_topk, minimax_m3_index_score then minimax_m3_index_topk).
  * The fp32 scores go to the workspace (size from
@@ -202,6 +258,61 @@ int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
                    int32_t local_blocks, int32_t *out, int64_t out_head_stride,
                    int64_t out_row_stride, void *workspace,
                    size_t workspace_bytes, void *stream);
+
+/*
+ * mm3idx_prefill_nvfp4 -- mm3idx_prefill over NVFP4 index-K pages
+ * (indexer_nvfp4, MiniMaxM3IndexerRocmNvfp4Impl.forward, prefill branch:
+ * NVFP4 index scores followed by the top-k).  p->index_cache holds the e2m1
+ * codes and p->index_scales the e4m3 scales, as for mm3idx_decode_nvfp4.
+ * Every page a request can see is first dequantised, once, to bf16
+ * (e4m3_rn_satfinite(e2m1 * scale), exact in bf16) into the workspace; the
+ * bf16 tensor-core scorer and the selector then run on that copy.  Workspace:
+ * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL_NVFP4, ...) bytes, 256-byte
+ * aligned, no initialisation needed.  A block table entry outside
+ * [0, num_pages) sets MM3IDX_DEV_BAD_PAGE (its keys are taken as zero).
+ * Requires num_reqs * cdiv(max_seq_len, 128) <= INT_MAX / 128
+ * (MM3IDX_ERR_UNSUPPORTED).  out as in mm3idx_prefill.
+ */
+int mm3idx_prefill_nvfp4(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
+                         int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                         int64_t out_row_stride, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * Ragged batches (index_topk, minimax_m3_index_score and
+ * minimax_m3_index_topk: cu_seqlens_q, prefix_lens, max_query_len): request
+ * i owns the query rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 of a batch of
+ * total_q rows; row j of it sits at position seq_lens[i] - rows_i + j (the
+ * pages' prefix_lens[i] = seq_lens[i] - rows_i).  cu_seqlens_q is an int32
+ * device array [num_reqs + 1], from 0 to total_q without decreasing (else
+ * MM3IDX_DEV_BAD_ROWS, and rows outside their request get -1 ids).  In the
+ * problem struct, query_len is the largest rows_i (max_query_len, a bound
+ * that may stay fixed across graph replays); total_q must not exceed
+ * num_reqs * query_len (MM3IDX_ERR_INVALID_ARGUMENT), so a workspace sized
+ * with mm3idx_workspace_bytes(op, heads, num_reqs, query_len, ...) serves
+ * every batch under that bound.  idx_q holds total_q rows; outputs are laid
+ * out by row as in the uniform calls.
+ *
+ * mm3idx_score_ragged -- mm3idx_score of a ragged batch (tensor-core scorer).
+ * mm3idx_topk_ragged  -- mm3idx_topk of a ragged batch's score tensor.
+ * mm3idx_prefill_ragged -- mm3idx_prefill (p->index_scales NULL) or
+ *   mm3idx_prefill_nvfp4 (p->index_scales set) of a ragged batch.
+ */
+int mm3idx_score_ragged(const mm3idx_problem_t *p, const int32_t *cu_seqlens_q,
+                        int32_t total_q, float *out, int64_t out_head_stride,
+                        int64_t out_row_stride, void *stream);
+int mm3idx_topk_ragged(const float *score, int64_t score_head_stride,
+                       int64_t score_row_stride, int32_t heads,
+                       const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                       int32_t num_reqs, int32_t total_q, int32_t max_query_len,
+                       int32_t max_seq_len, int32_t topk, int32_t init_blocks,
+                       int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                       int64_t out_row_stride, void *stream);
+int mm3idx_prefill_ragged(const mm3idx_problem_t *p, const int32_t *cu_seqlens_q,
+                          int32_t total_q, int32_t topk, int32_t init_blocks,
+                          int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                          int64_t out_row_stride, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * mm3idx_get_device_error -- synchronises `stream`, then reads and clears the
@@ -237,6 +348,23 @@ int mm3idx_get_device_error(void *stream, int32_t *code);
 int mm3idx_decode_static(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
                          int32_t local_blocks, int32_t *out, int64_t out_head_stride,
                          int64_t out_row_stride, void *stream);
+
+/*
+ * mm3idx_check_wait_timeout -- exercises the failure path of the on-chip
+ * pipeline waits.  The pages have no counterpart; every scoring kernel here
+ * waits on shared-memory barriers through one bounded wait, and this call
+ * makes that wait run out on purpose, on a barrier that nothing completes.
+ *
+ * Launches one CTA of `warps` warps (1..32) on `stream`.  Every warp waits on
+ * the first phase of a fresh barrier; after the library's wait limit (2 s of
+ * GPU wall clock) the first warp to give up raises the CTA's abort flag, the
+ * others see it and stop waiting, and the kernel sets MM3IDX_DEV_TIMEOUT in
+ * the device status word and returns.  No memory is read or written besides
+ * the status word, and the context stays usable.  Returns
+ * MM3IDX_ERR_INVALID_ARGUMENT for `warps` outside 1..32, MM3IDX_ERR_CUDA when
+ * the launch fails.  Not part of any scoring call.
+ */
+int mm3idx_check_wait_timeout(int32_t warps, void *stream);
 
 /* Human-readable text of a status code (static storage). */
 const char *mm3idx_status_string(int status);

@@ -30,10 +30,11 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libmm3idx.so")
 OK = 0
 OP_DECODE = 1
 OP_PREFILL = 2
+OP_PREFILL_NVFP4 = 3
 MAX_TOPK = 32
 MAX_DECODE_ROWS = 32
 STATIC_SCRATCH_BYTES = 8 << 20
-DEV_BAD_PAGE, DEV_SEQ_TOO_LONG, DEV_SEQ_TOO_SHORT, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_PAGE, DEV_SEQ_TOO_LONG, DEV_SEQ_TOO_SHORT, DEV_TIMEOUT, DEV_BAD_ROWS = 1, 2, 4, 8, 16
 
 
 class Mm3idxError(RuntimeError):
@@ -63,6 +64,20 @@ class Problem(ctypes.Structure):
     ]
 
 
+class SparseTable(ctypes.Structure):
+    """mm3idx_sparse_table_t."""
+    _fields_ = [
+        ("attention_block_table", ctypes.c_void_p),
+        ("attention_table_stride", ctypes.c_int64),
+        ("attention_table_width", ctypes.c_int32),
+        ("pages_per_block", ctypes.c_int32),
+        ("block_page_stride", ctypes.c_int32),
+        ("sparse_block_table_out", ctypes.c_void_p),
+        ("sparse_table_stride", ctypes.c_int64),
+        ("sparse_context_lens_out", ctypes.c_void_p),
+    ]
+
+
 SYMBOLS = {
     "mm3idx_version": (ctypes.c_int32, []),
     "mm3idx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -83,7 +98,31 @@ SYMBOLS = {
     "mm3idx_prefill": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "mm3idx_prefill_nvfp4": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                            ctypes.c_void_p]),
+    "mm3idx_score_ragged": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p]),
+    "mm3idx_topk_ragged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_void_p]),
+    "mm3idx_prefill_ragged": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_void_p,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                             ctypes.c_void_p]),
     "mm3idx_get_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    "mm3idx_decode_sparse_table": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32,
+                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                                  ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.POINTER(SparseTable), ctypes.c_void_p,
+                                                  ctypes.c_size_t, ctypes.c_void_p]),
+    "mm3idx_check_wait_timeout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_void_p]),
     "mm3idx_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
@@ -131,7 +170,7 @@ def _need(cond, msg):
 
 
 def _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale,
-             index_scales=None, nvfp4=False):
+             index_scales=None, nvfp4=False, rows=None):
     """Layout checks of check_context_score_inputs, then the C struct."""
     _need(idx_q.ndim == 3 and idx_q.shape[2] == 128 and idx_q.dtype == torch.bfloat16
           and idx_q.stride(2) == 1, "index queries must be BF16 [tokens,heads,128] with contiguous D")
@@ -155,7 +194,8 @@ def _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, 
           and (index_scales is None or index_scales.device == dev),
           "all score inputs must be on the same GPU")
     num_reqs = seq_lens.shape[0]
-    _need(idx_q.shape[0] == num_reqs * query_len, "rows != batch * query_len")
+    _need(idx_q.shape[0] == (num_reqs * query_len if rows is None else rows),
+          "rows != batch * query_len")
     _need(block_table.shape[0] == num_reqs, "block table must have one row per request")
     p = Problem()
     p.idx_q = idx_q.data_ptr()
@@ -267,12 +307,141 @@ def decode_nvfp4(idx_q, codes, scales, block_table, seq_lens, *, query_len, max_
                   local_blocks, sm_scale, out, workspace, stream)
 
 
+def decode_sparse_table(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len,
+                        topk, init_blocks, local_blocks, sm_scale, attention_block_table,
+                        sparse_block_table_out, sparse_context_lens_out, block_page_stride,
+                        pages_per_block, index_scales=None, out=None, workspace=None,
+                        stream=None):
+    """:func:`decode` (or :func:`decode_nvfp4` when ``index_scales`` is given)
+    for one index head that also writes the sparse page table of its ids:
+    ``sparse_block_table_out`` int32 [rows, topk * pages_per_block] (pages of
+    block b: attention_block_table[i, b] * block_page_stride + 0.., -1 in
+    unused slots) and ``sparse_context_lens_out`` int32 [rows] (visible
+    tokens in the selected blocks).  Returns the ids."""
+    nvfp4 = index_scales is not None
+    p = _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale,
+                 index_scales=index_scales, nvfp4=nvfp4)
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    at, st, ctx = attention_block_table, sparse_block_table_out, sparse_context_lens_out
+    _need(all(t.dtype == torch.int32 and t.device == idx_q.device for t in (at, st, ctx)),
+          "sparse tables must be int32 on the query device")
+    _need(at.ndim == 2 and at.shape[0] == seq_lens.shape[0] and at.stride(1) == 1,
+          "attention block table must be [num_reqs, blocks] with contiguous rows")
+    _need(st.ndim == 2 and st.shape[0] >= rows and st.shape[1] == topk * pages_per_block
+          and st.stride(1) == 1, "sparse block table must be [rows, topk * pages_per_block]")
+    _need(ctx.ndim == 1 and ctx.shape[0] >= rows and ctx.stride(0) == 1,
+          "sparse context lengths must be [rows]")
+    t = SparseTable()
+    t.attention_block_table = at.data_ptr()
+    t.attention_table_stride = at.stride(0) if at.shape[0] > 1 else max(at.shape[1], 1)
+    t.attention_table_width = at.shape[1]
+    t.pages_per_block = pages_per_block
+    t.block_page_stride = block_page_stride
+    t.sparse_block_table_out = st.data_ptr()
+    t.sparse_table_stride = st.stride(0) if st.shape[0] > 1 else max(st.shape[1], 1)
+    t.sparse_context_lens_out = ctx.data_ptr()
+    out = _ids_out(out, heads, rows, topk, idx_q.device)
+    if workspace is None:
+        workspace = new_workspace(OP_DECODE, heads, seq_lens.shape[0], query_len, max_seq_len,
+                                  topk, idx_q.device)
+    _check(lib.mm3idx_decode_sparse_table(ctypes.byref(p), topk, init_blocks, local_blocks,
+                                          out.data_ptr(), out.stride(0), out.stride(1),
+                                          ctypes.byref(t), workspace.data_ptr(),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream)), "mm3idx_decode_sparse_table")
+    return out[:, :rows, :]
+
+
 def prefill(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
             init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
     """Tensor-core prefill scores (to the workspace) followed by the selector."""
     return _fused(lib.mm3idx_prefill, "mm3idx_prefill", OP_PREFILL, idx_q, index_cache,
                   block_table, seq_lens, None, False, query_len, max_seq_len, topk, init_blocks,
                   local_blocks, sm_scale, out, workspace, stream)
+
+
+def prefill_nvfp4(idx_q, codes, scales, block_table, seq_lens, *, query_len, max_seq_len, topk,
+                  init_blocks, local_blocks, sm_scale, out=None, workspace=None, stream=None):
+    """:func:`prefill` over NVFP4 pages (codes uint8 [pages,128,64], scales
+    uint8 e4m3 [pages,128,8]): the visible pages are dequantised once into
+    the workspace, then scored on the tensor cores and selected."""
+    return _fused(lib.mm3idx_prefill_nvfp4, "mm3idx_prefill_nvfp4", OP_PREFILL_NVFP4, idx_q, codes,
+                  block_table, seq_lens, scales, True, query_len, max_seq_len, topk, init_blocks,
+                  local_blocks, sm_scale, out, workspace, stream)
+
+
+def _ragged_problem(idx_q, cache, block_table, seq_lens, cu_seqlens_q, max_query_len,
+                    max_seq_len, sm_scale, scales=None):
+    _need(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.ndim == 1
+          and cu_seqlens_q.shape[0] == seq_lens.shape[0] + 1 and cu_seqlens_q.is_contiguous()
+          and cu_seqlens_q.device == idx_q.device,
+          "cu_seqlens_q must be contiguous int32 [num_reqs + 1] on the query device")
+    num_reqs = seq_lens.shape[0]
+    total_q = idx_q.shape[0]
+    _need(total_q <= num_reqs * max_query_len, "more query rows than num_reqs * max_query_len")
+    p = _problem(idx_q, cache, block_table, seq_lens, max_query_len, max_seq_len, sm_scale,
+                 index_scales=scales, nvfp4=scales is not None, rows=total_q)
+    return p, total_q
+
+
+def score_ragged(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q, *, max_query_len,
+                 max_seq_len, sm_scale, out=None, stream=None):
+    """:func:`score` of a ragged batch: request i owns query rows
+    cu_seqlens_q[i]..cu_seqlens_q[i+1]-1 (at positions seq_len - rows_i + j)."""
+    p, total_q = _ragged_problem(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q,
+                                 max_query_len, max_seq_len, sm_scale)
+    heads = idx_q.shape[1]
+    width = _cdiv(max_seq_len, 128)
+    if out is None:
+        out = torch.empty((heads, total_q, width), dtype=torch.float32, device=idx_q.device)
+    _need(out.dtype == torch.float32 and out.ndim == 3 and out.shape[0] == heads
+          and out.shape[1] >= total_q and out.shape[2] >= width and out.stride(2) == 1,
+          "out must be fp32 [heads, >=rows, >=cdiv(max_seq_len,128)] with unit inner stride")
+    _check(lib.mm3idx_score_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q,
+                                   out.data_ptr(), out.stride(0), out.stride(1), _stream(stream)),
+           "mm3idx_score_ragged")
+    return out[:, :total_q, :width]
+
+
+def topk_ragged(score_t, seq_lens, cu_seqlens_q, *, max_query_len, max_seq_len, topk,
+                init_blocks, local_blocks, out=None, stream=None):
+    """:func:`topk` of a ragged batch's score tensor [heads, total_q, blocks]."""
+    _need(score_t.dtype == torch.float32 and score_t.ndim == 3 and score_t.stride(2) == 1,
+          "score must be fp32 [heads, rows, blocks] with unit inner stride")
+    _need(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.ndim == 1
+          and cu_seqlens_q.shape[0] == seq_lens.shape[0] + 1 and cu_seqlens_q.is_contiguous(),
+          "cu_seqlens_q must be contiguous int32 [num_reqs + 1]")
+    heads, total_q = score_t.shape[0], score_t.shape[1]
+    out = _ids_out(out, heads, total_q, topk, score_t.device)
+    _check(lib.mm3idx_topk_ragged(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,
+                                  cu_seqlens_q.data_ptr(), seq_lens.data_ptr(), seq_lens.shape[0],
+                                  total_q, max_query_len, max_seq_len, topk, init_blocks,
+                                  local_blocks, out.data_ptr(), out.stride(0), out.stride(1),
+                                  _stream(stream)), "mm3idx_topk_ragged")
+    return out[:, :total_q, :]
+
+
+def prefill_ragged(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q, *, max_query_len,
+                   max_seq_len, topk, init_blocks, local_blocks, sm_scale, index_scales=None,
+                   out=None, workspace=None, stream=None):
+    """:func:`prefill` (or :func:`prefill_nvfp4` with ``index_scales``) of a
+    ragged batch.  A workspace from ``new_workspace(OP_PREFILL[_NVFP4], heads,
+    num_reqs, max_query_len, max_seq_len, topk)`` serves any batch under
+    those bounds."""
+    p, total_q = _ragged_problem(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q,
+                                 max_query_len, max_seq_len, sm_scale, scales=index_scales)
+    heads = idx_q.shape[1]
+    op = OP_PREFILL_NVFP4 if index_scales is not None else OP_PREFILL
+    out = _ids_out(out, heads, total_q, topk, idx_q.device)
+    if workspace is None:
+        workspace = new_workspace(op, heads, seq_lens.shape[0], max_query_len, max_seq_len, topk,
+                                  idx_q.device)
+    _check(lib.mm3idx_prefill_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q, topk,
+                                     init_blocks, local_blocks, out.data_ptr(), out.stride(0),
+                                     out.stride(1), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "mm3idx_prefill_ragged")
+    return out[:, :total_q, :]
 
 
 def decode_static(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,
@@ -287,6 +456,12 @@ def decode_static(idx_q, index_cache, block_table, seq_lens, *, query_len, max_s
                                     out.data_ptr(), out.stride(0), out.stride(1), _stream(stream)),
            "mm3idx_decode_static")
     return out[:, :rows, :]
+
+
+def check_wait_timeout(warps: int = 4, stream=None):
+    """Make the bounded on-chip wait run out on purpose (about 2 s); the
+    device status word then holds DEV_TIMEOUT (read it with get_device_error)."""
+    _check(lib.mm3idx_check_wait_timeout(warps, _stream(stream)), "mm3idx_check_wait_timeout")
 
 
 def get_device_error(stream=None) -> int:

@@ -13,6 +13,7 @@
 
 #include "../../include/mm3idx.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 using namespace mm3idx;
 
@@ -84,10 +85,9 @@ int make_kmap(const mm3idx_problem_t* p, CUtensorMap* m) {
 }
 
 // [rows, heads, 128] bf16 queries, boxes of 64 columns x 1 head x 128 rows.
-int make_qmap(const mm3idx_problem_t* p, CUtensorMap* m) {
+int make_qmap(const mm3idx_problem_t* p, int64_t rows, CUtensorMap* m) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MM3IDX_ERR_CUDA;
-  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p->heads),
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->q_head_stride) * 2,
@@ -181,6 +181,17 @@ size_t prefill_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len, int3
   return static_cast<size_t>(heads) * num_reqs * query_len * w * 4;
 }
 
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// NVFP4 prefill workspace: [scores as the bf16 prefill][bf16 pages:
+// num_reqs x cdiv(max_seq_len,128) x 32 KB][identity table, int32].
+size_t prefill_nvfp4_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len,
+                              int32_t max_seq_len) {
+  const size_t slots = static_cast<size_t>(num_reqs) * cdiv(max_seq_len, kBlock);
+  return align256(prefill_ws_bytes(heads, num_reqs, query_len, max_seq_len)) +
+         slots * kBlock * kD * 2 + align256(slots * 4);
+}
+
 DecodeArgs decode_args(const mm3idx_problem_t* p, int* status) {
   DecodeArgs a{};
   a.q = static_cast<const uint16_t*>(p->idx_q);
@@ -207,12 +218,31 @@ int decode_grid(const mm3idx_problem_t* p, int sms) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// The sparse-table arguments (index_topk, minimax_m3_index_decode): all or
+// none, one index head, stride P or 2P, table wide enough.
+int check_sparse_table(const mm3idx_problem_t* p, int32_t topk, const mm3idx_sparse_table_t* t) {
+  if (p->num_reqs > 0 &&
+      (!t->attention_block_table || !t->sparse_block_table_out || !t->sparse_context_lens_out))
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (p->heads != 1) return MM3IDX_ERR_UNSUPPORTED;
+  const int32_t P = t->pages_per_block;
+  if (P < 1 || P > kBlock || kBlock % P != 0) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (t->block_page_stride != P && t->block_page_stride != 2 * P) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (t->attention_table_width < cdiv(p->max_seq_len, kBlock) ||
+      t->attention_table_stride < t->attention_table_width)
+    return MM3IDX_ERR_TABLE_LAYOUT;
+  if (t->sparse_table_stride < static_cast<int64_t>(topk) * P) return MM3IDX_ERR_OUT_LAYOUT;
+  return MM3IDX_OK;
+}
+
 int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init_blocks,
                int32_t local_blocks, int32_t* out, int64_t out_head_stride, int64_t out_row_stride,
-               void* workspace, size_t workspace_bytes, void* stream) {
+               void* workspace, size_t workspace_bytes, void* stream,
+               const mm3idx_sparse_table_t* table = nullptr) {
   int rc = check_problem(p, nvfp4);
   if (rc) return rc;
   if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  if (table && (rc = check_sparse_table(p, topk, table))) return rc;
   const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
   if (rows == 0) return MM3IDX_OK;
   if (p->heads * static_cast<int64_t>(p->query_len) > MM3IDX_MAX_DECODE_ROWS)
@@ -247,11 +277,32 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
     if ((rc = make_kmap(p, &kmap))) return rc;
     e = launch_decode_bf16(kmap, a, grid, s);
   }
+  if (e == cudaSuccess && table) {
+    SparseTableArgs t{};
+    t.ids = out;
+    t.i_row = out_row_stride;
+    t.topk = topk;
+    t.seq_lens = p->seq_lens;
+    t.num_reqs = p->num_reqs;
+    t.query_len = p->query_len;
+    t.max_seq_len = p->max_seq_len;
+    t.attn_table = table->attention_block_table;
+    t.attn_stride = table->attention_table_stride;
+    t.pages_per_block = table->pages_per_block;
+    t.block_page_stride = table->block_page_stride;
+    t.st_out = table->sparse_block_table_out;
+    t.st_stride = table->sparse_table_stride;
+    t.ctx_out = table->sparse_context_lens_out;
+    e = launch_sparse_table(t, s);
+  }
   return cuda_status(e);
 }
 
-int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, int64_t row_stride,
-                   int32_t fill_width, int sms, int32_t* status, cudaStream_t s) {
+// Scores of a batch on the tensor-core scorer; cu == nullptr: query_len
+// rows per request, else the ragged row offsets (total_q rows).
+int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q, float* out,
+                   int64_t head_stride, int64_t row_stride, int32_t fill_width, int sms,
+                   int32_t* status, cudaStream_t s) {
   PrefillArgs a{};
   a.heads = p->heads;
   a.num_reqs = p->num_reqs;
@@ -266,27 +317,31 @@ int prefill_scores(const mm3idx_problem_t* p, float* out, int64_t head_stride, i
   a.s_head = head_stride;
   a.s_row = row_stride;
   a.fill_width = fill_width;
-  a.qtiles = static_cast<int32_t>(cdiv(p->query_len, 128));
-  const int64_t uph = prefill_units_per_head(p->query_len, p->max_seq_len);
-  a.units_per_head = uph;
-  a.total_units = uph * p->heads * p->num_reqs;
+  a.cu = cu;
+  a.total_q = total_q;
   a.status = status;
+  // The kernel counts the units itself; a bound on them keeps tiny batches
+  // from launching idle CTAs: tiles x pairs of blocks per tile.
+  const int64_t tiles = cdiv(total_q, 128) + p->num_reqs;
+  const int64_t bound = static_cast<int64_t>(p->heads) * tiles * ((cdiv(p->max_seq_len, kBlock) + 1) / 2);
   int64_t grid = sms;
-  if (a.total_units < grid) grid = a.total_units;
+  if (bound < grid) grid = bound;
   if (grid < 1) return MM3IDX_OK;
   CUtensorMap qmap, kmap;
   int rc;
-  if ((rc = make_qmap(p, &qmap))) return rc;
+  if ((rc = make_qmap(p, total_q, &qmap))) return rc;
   if ((rc = make_kmap(p, &kmap))) return rc;
   return cuda_status(launch_prefill(qmap, kmap, a, static_cast<int>(grid), s));
 }
 
 SelectArgs select_args(const float* score, int64_t sh, int64_t sr, int32_t heads,
                        const int32_t* seq_lens, int32_t num_reqs, int32_t query_len,
-                       int32_t max_seq_len, int32_t topk, int32_t init_blocks,
-                       int32_t local_blocks, int32_t* out, int64_t oh, int64_t orow,
-                       int32_t* status) {
+                       const int32_t* cu, int32_t total_q, int32_t max_seq_len, int32_t topk,
+                       int32_t init_blocks, int32_t local_blocks, int32_t* out, int64_t oh,
+                       int64_t orow, int32_t* status) {
   SelectArgs a{};
+  a.cu = cu;
+  a.total_q = total_q;
   a.score = score;
   a.s_head = sh;
   a.s_row = sr;
@@ -305,9 +360,135 @@ SelectArgs select_args(const float* score, int64_t sh, int64_t sr, int32_t heads
   return a;
 }
 
+// Ragged batches: row offsets on the device, total_q rows, at most
+// max_query_len rows per request (the bound the workspace is sized with).
+int check_ragged(int32_t num_reqs, int32_t max_query_len, const int32_t* cu, int32_t total_q) {
+  if (total_q < 0 || max_query_len < 1) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(total_q) > static_cast<int64_t>(num_reqs) * max_query_len)
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (num_reqs > 0 && (!cu || (reinterpret_cast<uintptr_t>(cu) & 3u)))
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  return MM3IDX_OK;
+}
+
+int run_topk(const float* score, int64_t sh, int64_t sr, int32_t heads, const int32_t* seq_lens,
+             int32_t num_reqs, int32_t query_len, const int32_t* cu, int32_t total_q,
+             int32_t max_seq_len, int32_t topk, int32_t init_blocks, int32_t local_blocks,
+             int32_t* out, int64_t oh, int64_t orow, void* stream) {
+  if (heads < 1 || num_reqs < 0) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (query_len < 1 || max_seq_len < query_len) return MM3IDX_ERR_QUERY_LEN;
+  if (cdiv(max_seq_len, kBlock) >= 0xFFFF) return MM3IDX_ERR_TOO_MANY_BLOCKS;
+  int rc = check_topk(topk, init_blocks, local_blocks);
+  if (rc) return rc;
+  if (total_q == 0) return MM3IDX_OK;
+  if (!score || !seq_lens || !out) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (!out_ok(sh, sr, heads, total_q, cdiv(max_seq_len, kBlock)) ||
+      !out_ok(oh, orow, heads, total_q, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  SelectArgs a = select_args(score, sh, sr, heads, seq_lens, num_reqs, query_len, cu, total_q,
+                             max_seq_len, topk, init_blocks, local_blocks, out, oh, orow,
+                             dev->status);
+  return cuda_status(launch_select(a, dev->sms, static_cast<cudaStream_t>(stream)));
+}
+
+// Prefill: scores to the workspace, then the selector.  NVFP4 keys are first
+// dequantised, once per page, into a bf16 copy in the workspace.  cu ==
+// nullptr: query_len rows per request; else ragged (total_q rows).
+int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_t total_q,
+                int32_t topk, int32_t init_blocks, int32_t local_blocks, int32_t* out,
+                int64_t out_head_stride, int64_t out_row_stride, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  int rc = check_problem(p, nvfp4);
+  if (rc) return rc;
+  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  if (cu) {
+    if ((rc = check_ragged(p->num_reqs, p->query_len, cu, total_q))) return rc;
+  } else {
+    total_q = p->num_reqs * p->query_len;   // < INT_MAX (check_problem)
+  }
+  const int64_t rows = total_q;
+  if (rows == 0) return MM3IDX_OK;
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  const int64_t width = cdiv(p->max_seq_len, kBlock);
+  if (nvfp4 && static_cast<int64_t>(p->num_reqs) * width > INT_MAX / kBlock)
+    return MM3IDX_ERR_UNSUPPORTED;
+  const size_t need = nvfp4 ? prefill_nvfp4_ws_bytes(p->heads, p->num_reqs, p->query_len,
+                                                     p->max_seq_len)
+                            : prefill_ws_bytes(p->heads, p->num_reqs, p->query_len, p->max_seq_len);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MM3IDX_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mm3idx_problem_t q = *p;
+  if (nvfp4) {
+    const size_t score_bytes = align256(prefill_ws_bytes(p->heads, p->num_reqs, p->query_len,
+                                                         p->max_seq_len));
+    const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
+    DequantArgs d{};
+    d.codes = static_cast<const uint8_t*>(p->index_cache);
+    d.scales = static_cast<const uint8_t*>(p->index_scales);
+    d.num_pages = p->num_pages;
+    d.table = p->block_table;
+    d.table_stride = p->table_stride;
+    d.seq_lens = p->seq_lens;
+    d.num_reqs = p->num_reqs;
+    d.max_seq_len = p->max_seq_len;
+    d.width = static_cast<int32_t>(width);
+    d.pages_out = reinterpret_cast<uint16_t*>(ws + score_bytes);
+    d.table_out = reinterpret_cast<int32_t*>(ws + score_bytes + slots * kBlock * kD * 2);
+    d.status = dev->status;
+    if ((rc = cuda_status(launch_dequant_pages(d, dev->sms, s)))) return rc;
+    // the bf16 scorer then reads the copy through an identity table
+    q.index_cache = d.pages_out;
+    q.index_scales = nullptr;
+    q.num_pages = static_cast<int32_t>(slots);
+    q.block_table = d.table_out;
+    q.table_stride = width;
+    q.table_width = static_cast<int32_t>(width);
+  }
+  const int64_t w = (width + 3) / 4 * 4;
+  float* score = reinterpret_cast<float*>(ws);
+  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, 0, dev->sms, dev->status, s)))
+    return rc;
+  SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
+                             cu, total_q, p->max_seq_len, topk, init_blocks, local_blocks, out,
+                             out_head_stride, out_row_stride, dev->status);
+  return cuda_status(launch_select(a, dev->sms, s));
+}
+
+// Every warp waits on the first phase of a barrier that nothing arrives at,
+// through the bounded wait of the pipeline kernels, so the wait runs out.
+__global__ void wait_timeout_check_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = warp_wait(&bar, 0, &abort_flag);
+  __syncthreads();
+  if (threadIdx.x == 0 && (!ok || abort_flag)) atomicOr(status, MM3IDX_DEV_TIMEOUT);
+}
+
 }  // namespace
 
 extern "C" {
+
+int mm3idx_check_wait_timeout(int32_t warps, void* stream) {
+  if (warps < 1 || warps > 32) return MM3IDX_ERR_INVALID_ARGUMENT;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  wait_timeout_check_kernel<<<1, warps * 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status);
+  return cuda_status(cudaGetLastError());
+}
 
 int32_t mm3idx_version(void) { return kVersion; }
 
@@ -347,6 +528,10 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t 
     *bytes = prefill_ws_bytes(heads, num_reqs, query_len, max_seq_len);
     return MM3IDX_OK;
   }
+  if (op == MM3IDX_OP_PREFILL_NVFP4) {
+    *bytes = prefill_nvfp4_ws_bytes(heads, num_reqs, query_len, max_seq_len);
+    return MM3IDX_OK;
+  }
   return MM3IDX_ERR_INVALID_ARGUMENT;
 }
 
@@ -374,30 +559,48 @@ int mm3idx_score(const mm3idx_problem_t* p, float* out, int64_t out_head_stride,
     if ((rc = make_kmap(p, &kmap))) return rc;
     return cuda_status(launch_decode_bf16(kmap, a, decode_grid(p, dev->sms), s));
   }
-  return prefill_scores(p, out, out_head_stride, out_row_stride, width, dev->sms, dev->status, s);
+  return prefill_scores(p, nullptr, static_cast<int32_t>(rows), out, out_head_stride,
+                        out_row_stride, width, dev->sms, dev->status, s);
+}
+
+int mm3idx_score_ragged(const mm3idx_problem_t* p, const int32_t* cu_seqlens_q, int32_t total_q,
+                        float* out, int64_t out_head_stride, int64_t out_row_stride,
+                        void* stream) {
+  int rc = check_problem(p, false);
+  if (rc) return rc;
+  if ((rc = check_ragged(p->num_reqs, p->query_len, cu_seqlens_q, total_q))) return rc;
+  if (total_q == 0) return MM3IDX_OK;
+  const int32_t width = static_cast<int32_t>(cdiv(p->max_seq_len, kBlock));
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, total_q, width))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  return prefill_scores(p, cu_seqlens_q, total_q, out, out_head_stride, out_row_stride, width,
+                        dev->sms, dev->status, static_cast<cudaStream_t>(stream));
 }
 
 int mm3idx_topk(const float* score, int64_t score_head_stride, int64_t score_row_stride,
                 int32_t heads, const int32_t* seq_lens, int32_t num_reqs, int32_t query_len,
                 int32_t max_seq_len, int32_t topk, int32_t init_blocks, int32_t local_blocks,
                 int32_t* out, int64_t out_head_stride, int64_t out_row_stride, void* stream) {
-  if (heads < 1 || num_reqs < 0) return MM3IDX_ERR_INVALID_ARGUMENT;
-  if (query_len < 1 || max_seq_len < query_len) return MM3IDX_ERR_QUERY_LEN;
-  if (cdiv(max_seq_len, kBlock) >= 0xFFFF) return MM3IDX_ERR_TOO_MANY_BLOCKS;
-  int rc = check_topk(topk, init_blocks, local_blocks);
-  if (rc) return rc;
   const int64_t rows = static_cast<int64_t>(num_reqs) * query_len;
-  if (rows == 0) return MM3IDX_OK;
-  if (!score || !seq_lens || !out) return MM3IDX_ERR_INVALID_ARGUMENT;
-  if (!out_ok(score_head_stride, score_row_stride, heads, rows, cdiv(max_seq_len, kBlock)) ||
-      !out_ok(out_head_stride, out_row_stride, heads, rows, topk))
-    return MM3IDX_ERR_OUT_LAYOUT;
-  DeviceInfo* dev = nullptr;
-  if ((rc = device_info(&dev))) return rc;
-  SelectArgs a = select_args(score, score_head_stride, score_row_stride, heads, seq_lens, num_reqs,
-                             query_len, max_seq_len, topk, init_blocks, local_blocks, out,
-                             out_head_stride, out_row_stride, dev->status);
-  return cuda_status(launch_select(a, dev->sms, static_cast<cudaStream_t>(stream)));
+  if (rows >= INT_MAX) return MM3IDX_ERR_INVALID_ARGUMENT;
+  return run_topk(score, score_head_stride, score_row_stride, heads, seq_lens, num_reqs,
+                  query_len, nullptr, static_cast<int32_t>(rows), max_seq_len, topk, init_blocks,
+                  local_blocks, out, out_head_stride, out_row_stride, stream);
+}
+
+int mm3idx_topk_ragged(const float* score, int64_t score_head_stride, int64_t score_row_stride,
+                       int32_t heads, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                       int32_t num_reqs, int32_t total_q, int32_t max_query_len,
+                       int32_t max_seq_len, int32_t topk, int32_t init_blocks,
+                       int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                       int64_t out_row_stride, void* stream) {
+  int rc = check_ragged(num_reqs, max_query_len, cu_seqlens_q, total_q);
+  if (rc) return rc;
+  return run_topk(score, score_head_stride, score_row_stride, heads, seq_lens, num_reqs,
+                  max_query_len, cu_seqlens_q, total_q, max_seq_len, topk, init_blocks,
+                  local_blocks, out, out_head_stride, out_row_stride, stream);
 }
 
 int mm3idx_decode(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
@@ -405,6 +608,15 @@ int mm3idx_decode(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
                   int64_t out_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
   return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
                     out_row_stride, workspace, workspace_bytes, stream);
+}
+
+int mm3idx_decode_sparse_table(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                               int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                               int64_t out_row_stride, const mm3idx_sparse_table_t* table,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || !table) return MM3IDX_ERR_INVALID_ARGUMENT;
+  return run_decode(p, p->index_scales != nullptr, topk, init_blocks, local_blocks, out,
+                    out_head_stride, out_row_stride, workspace, workspace_bytes, stream, table);
 }
 
 int mm3idx_decode_nvfp4(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
@@ -418,26 +630,28 @@ int mm3idx_decode_nvfp4(const mm3idx_problem_t* p, int32_t topk, int32_t init_bl
 int mm3idx_prefill(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
                    int32_t local_blocks, int32_t* out, int64_t out_head_stride,
                    int64_t out_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_problem(p, false);
-  if (rc) return rc;
-  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
-  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
-  if (rows == 0) return MM3IDX_OK;
-  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, topk))
-    return MM3IDX_ERR_OUT_LAYOUT;
-  const size_t need = prefill_ws_bytes(p->heads, p->num_reqs, p->query_len, p->max_seq_len);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return MM3IDX_ERR_WORKSPACE;
-  DeviceInfo* dev = nullptr;
-  if ((rc = device_info(&dev))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t w = (cdiv(p->max_seq_len, kBlock) + 3) / 4 * 4;
-  float* score = static_cast<float*>(workspace);
-  if ((rc = prefill_scores(p, score, rows * w, w, 0, dev->sms, dev->status, s))) return rc;
-  SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
-                             p->max_seq_len, topk, init_blocks, local_blocks, out, out_head_stride,
-                             out_row_stride, dev->status);
-  return cuda_status(launch_select(a, dev->sms, s));
+  return run_prefill(p, false, nullptr, -1, topk, init_blocks, local_blocks, out,
+                     out_head_stride, out_row_stride, workspace, workspace_bytes, stream);
+}
+
+int mm3idx_prefill_nvfp4(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,
+                         int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                         int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return run_prefill(p, true, nullptr, -1, topk, init_blocks, local_blocks, out,
+                     out_head_stride, out_row_stride, workspace, workspace_bytes, stream);
+}
+
+int mm3idx_prefill_ragged(const mm3idx_problem_t* p, const int32_t* cu_seqlens_q,
+                          int32_t total_q, int32_t topk, int32_t init_blocks,
+                          int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                          int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!p) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (!cu_seqlens_q && p->num_reqs > 0) return MM3IDX_ERR_INVALID_ARGUMENT;
+  return run_prefill(p, p->index_scales != nullptr, cu_seqlens_q, total_q, topk, init_blocks,
+                     local_blocks, out, out_head_stride, out_row_stride, workspace,
+                     workspace_bytes, stream);
 }
 
 int mm3idx_decode_static(const mm3idx_problem_t* p, int32_t topk, int32_t init_blocks,

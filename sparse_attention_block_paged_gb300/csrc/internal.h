@@ -57,10 +57,8 @@ struct PrefillArgs {
   float* score;
   int64_t s_head, s_row;
   int32_t fill_width;         // 0: leave invisible blocks untouched; else write -inf up to it
-  int32_t qtiles;             // cdiv(query_len, 128)
-  int64_t units_per_head;     // prefill_units_per_head(query_len, max_seq_len)
-  int64_t total_units;
-  int32_t status_dummy;
+  const int32_t* cu;          // ragged: [num_reqs + 1] query-row offsets; nullptr: query_len each
+  int32_t total_q;            // rows of the batch
   int32_t* status;
 };
 
@@ -70,12 +68,47 @@ struct SelectArgs {
   int32_t heads;
   const int32_t* seq_lens;
   int32_t num_reqs;
-  int32_t query_len;
+  int32_t query_len;          // rows per request (uniform batches)
+  const int32_t* cu;          // ragged: [num_reqs + 1] query-row offsets; nullptr: uniform
+  int32_t total_q;            // rows of the batch
   int32_t max_seq_len;
   int32_t topk, init_blocks, local_blocks;
   int32_t* ids;
   int64_t i_head, i_row;
   int32_t* status;
+};
+
+struct DequantArgs {
+  const uint8_t* codes;       // NVFP4 [num_pages, 128, 64]
+  const uint8_t* scales;      // e4m3 [num_pages, 128, 8]
+  int32_t num_pages;
+  const int32_t* table;
+  int64_t table_stride;
+  const int32_t* seq_lens;
+  int32_t num_reqs;
+  int32_t max_seq_len;
+  int32_t width;              // cdiv(max_seq_len, 128): slots per request
+  uint16_t* pages_out;        // bf16 [num_reqs * width, 128, 128]
+  int32_t* table_out;         // [num_reqs, width]: slot ids (identity)
+  int32_t* status;
+};
+
+// The sparse page table of one head's ids (see sparse_table.cu).
+struct SparseTableArgs {
+  const int32_t* ids;         // [rows, i_row] ascending ids, -1 pad
+  int64_t i_row;
+  int32_t topk;
+  const int32_t* seq_lens;
+  int32_t num_reqs;
+  int32_t query_len;
+  int32_t max_seq_len;
+  const int32_t* attn_table;  // [num_reqs, attn_stride] logical block -> attention block
+  int64_t attn_stride;
+  int32_t pages_per_block;    // attention pages per 128-token block
+  int32_t block_page_stride;  // pages between consecutive attention blocks
+  int32_t* st_out;            // [rows, st_stride], topk * pages_per_block used
+  int64_t st_stride;
+  int32_t* ctx_out;           // [rows] visible tokens in the selected blocks
 };
 
 // Launchers; each returns a cudaError_t of the launch.
@@ -84,9 +117,9 @@ cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
-// Work units of the prefill scorer for one (request, head), counted for a
-// request of max_seq_len tokens (the unit is defined in prefill.cu).
-int64_t prefill_units_per_head(int32_t query_len, int32_t max_seq_len);
+cudaError_t launch_dequant_pages(const DequantArgs& a, int num_sms, cudaStream_t s);
+// Launched as a programmatic dependent of the kernel before it in the stream.
+cudaError_t launch_sparse_table(const SparseTableArgs& a, cudaStream_t s);
 
 // Grid sizing of the decode kernel (persistent; one CTA per SM).
 int decode_ctas_per_sm();

@@ -7,11 +7,11 @@
 // request's prefix).  The design is ours:
 //
 //   * A unit is (request, head, 128-row query tile, pair of key blocks).
-//     Units are enumerated from host-known sizes, assuming every request is
-//     max_seq_len long (a bound fixed across graph replays); units past a
-//     request's real causal range do no math.  Each CTA of a persistent grid
-//     takes one contiguous, equal share of the units, so the causal triangle
-//     is spread evenly over the SMs.
+//     A request's query rows are query_len per request, or for a ragged
+//     batch the rows given by its row offsets (minimax_m3_index_score:
+//     cu_seqlens_q).  The CTAs count the units exactly on the device (a
+//     closed form per request) and each takes one contiguous, equal share,
+//     so the causal triangle is spread evenly over the SMs.
 //   * warp 0   : TMA producer.  The 128 x 128 bf16 query tile (two 64-column
 //                boxes, 128-byte swizzle, from a 3-D map over
 //                [tokens, heads, 128]) once per tile, and the two key pages of
@@ -28,9 +28,12 @@
 //                issuer keeps no unit bookkeeping.
 //   * warps 2-9: epilogue, two teams of four warps (one warp per TMEM lane
 //                quadrant).  Team t drains block t of every unit: loads its
-//                row's 128 columns with tcgen05.ld, frees the accumulator,
-//                then takes the causal row max with 3-input max and stores
-//                one fp32 score per (row, block).
+//                row's 128 columns with tcgen05.ld in two 64-column halves,
+//                taking the causal row max of each with 3-input max, frees
+//                the accumulator and stores one fp32 score per (row, block).
+//                Ten warps put three on one SM sub-partition, which caps a
+//                thread at 168 registers; holding all 128 columns at once
+//                spilled the loop state to local memory.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -40,19 +43,6 @@
 #include "ptx.cuh"
 
 namespace mm3idx {
-
-// Worst-case units of one (request, head): every query tile of a request of
-// max_seq_len tokens, its visible blocks taken in pairs.
-int64_t prefill_units_per_head(int32_t query_len, int32_t max_seq_len) {
-  const int64_t wprefix = static_cast<int64_t>(max_seq_len) - query_len;
-  const int64_t qtiles = (static_cast<int64_t>(query_len) + 127) / 128;
-  int64_t n = 0;
-  for (int64_t qt = 0; qt < qtiles; ++qt) {
-    const int64_t last = wprefix + std::min<int64_t>(qt * 128 + 127, query_len - 1);
-    n += ((last >> 7) + 2) / 2;
-  }
-  return n;
-}
 
 namespace {
 
@@ -89,60 +79,150 @@ __device__ __forceinline__ int tile_blocks(int prefix, int qt, int query_len) {
   return last < 0 ? 0 : (last >> 7) + 1;
 }
 
-// Iterates this CTA's share of the unit list.
-struct UnitIter {
-  int64_t u, hi;
-  int rh, qt, p, np;  // (request*heads + head), tile, pair, scheduled pairs of the tile
-  int req, head;      // rh split into its request and head
-  int wprefix;        // worst-case prefix: max_seq_len - query_len
-  __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi_) {
-    u = lo;
-    hi = hi_;
-    wprefix = a.max_seq_len - a.query_len;
-    if (lo >= hi_) return;
-    rh = static_cast<int>(lo / a.units_per_head);
-    req = rh / a.heads;
-    head = rh - req * a.heads;
-    int64_t off = lo - static_cast<int64_t>(rh) * a.units_per_head;
-    qt = 0;
-    for (;;) {
-      np = (tile_blocks(wprefix, qt, a.query_len) + 1) >> 1;
-      if (off < np) break;
-      off -= np;
-      ++qt;
-    }
-    p = static_cast<int>(off);
-  }
-  __device__ bool valid() const { return u < hi; }
-  __device__ void advance(const PrefillArgs& a) {
-    ++u;
-    if (++p < np) return;
-    p = 0;
-    if (++qt == a.qtiles) {
-      qt = 0;
-      ++rh;
-      if (++head == a.heads) {
-        head = 0;
-        ++req;
-      }
-    }
-    np = (tile_blocks(wprefix, qt, a.query_len) + 1) >> 1;
-  }
+// Where a request's query rows are: a uniform batch has query_len rows per
+// request; a ragged one takes them from the row offsets cu (index_topk,
+// minimax_m3_index_score: cu_seqlens_q).  prefix = seq_len - rows, so row j
+// sits at position prefix + j.
+struct ReqGeom {
+  int qbeg = 0, ql = 0, prefix = 0, qtiles = 0;
 };
 
-// Per-tile facts every role needs, refreshed only when the tile changes.
-struct TileInfo {
-  int rh = -1, qt = -1, req = -1;
-  int prefix = 0, nvis = 0;  // request prefix; visible blocks of the tile
-  __device__ __forceinline__ bool refresh(const PrefillArgs& a, const UnitIter& U) {
-    if (U.rh == rh && U.qt == qt) return false;
-    if (U.req != req) {
-      req = U.req;
-      prefix = min(max(__ldg(a.seq_lens + req), 0), a.max_seq_len) - a.query_len;
+__device__ __forceinline__ ReqGeom req_geom(const PrefillArgs& a, int i) {
+  ReqGeom g;
+  if (a.cu != nullptr) {
+    const int b = __ldg(a.cu + i), e = __ldg(a.cu + i + 1);
+    g.qbeg = min(max(b, 0), a.total_q);
+    g.ql = min(max(e, g.qbeg), a.total_q) - g.qbeg;  // malformed offsets are flagged by the selector
+  } else {
+    g.qbeg = i * a.query_len;
+    g.ql = a.query_len;
+  }
+  g.prefix = min(max(__ldg(a.seq_lens + i), 0), a.max_seq_len) - g.ql;
+  g.qtiles = (g.ql + 127) >> 7;
+  return g;
+}
+
+// Units of one query tile: its visible blocks in pairs; at least one, so
+// that every tile's rows get their -inf fill.
+__device__ __forceinline__ int tile_units(const ReqGeom& g, int qt) {
+  return max(1, (tile_blocks(g.prefix, qt, g.ql) + 1) >> 1);
+}
+
+// sum of ceil(k / 2) for k = 1..n
+__device__ __forceinline__ int64_t half_ceil_sum(int64_t n) { return ((n + 1) >> 1) * ((n + 2) >> 1); }
+
+// Units of one (request, head) in its tiles 0..qt-1.  A full tile t holds
+// A + t + 1 visible blocks (A = (prefix + 127) / 128), so the full tiles sum
+// in closed form; a request shorter than its rows (malformed) is counted
+// tile by tile.
+__device__ __forceinline__ int64_t units_before(const ReqGeom& g, int qt) {
+  if (g.prefix < 0) {
+    int64_t n = 0;
+    for (int t = 0; t < qt; ++t) n += tile_units(g, t);
+    return n;
+  }
+  const int full = g.ql >> 7;
+  const int64_t A = (g.prefix + 127) >> 7;
+  const int f = min(qt, full);
+  int64_t n = half_ceil_sum(A + f) - half_ceil_sum(A);
+  if (qt > full) n += tile_units(g, full);
+  return n;
+}
+
+// Iterates this CTA's share of the unit list (request, head, query tile,
+// pair of key blocks).  The list holds exactly each request's units, so the
+// shares are computed on the device: total() and init() are warp-collective.
+// The state is kept small: the epilogue's loop also holds a 128-column
+// accumulator row in registers.
+struct UnitIter {
+  int left = 0;  // units still to visit, this one included
+  int req = 0, head = 0, qt = 0, p = 0, np = 0, nvis = 0;
+  ReqGeom g;
+
+  // Total units of the batch (all lanes get it).
+  __device__ static int64_t total(const PrefillArgs& a) {
+    const int lane = threadIdx.x & 31;
+    int64_t sum = 0;
+    for (int base = 0; base < a.num_reqs; base += 32) {
+      const int i = base + lane;
+      if (i < a.num_reqs) {
+        const ReqGeom gi = req_geom(a, i);
+        sum += units_before(gi, gi.qtiles);
+      }
     }
-    rh = U.rh;
-    qt = U.qt;
-    nvis = tile_blocks(prefix, qt, a.query_len);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    return sum * a.heads;
+  }
+
+  __device__ __forceinline__ void load_tile() {
+    nvis = tile_blocks(g.prefix, qt, g.ql);
+    np = max(1, (nvis + 1) >> 1);
+  }
+
+  // Position at unit lo of the list; the share ends at hi.
+  __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi) {
+    left = static_cast<int>(hi - lo);
+    if (left <= 0) return;
+    const int lane = threadIdx.x & 31;
+    int64_t acc = 0;  // units of the requests before `base`
+    for (int base = 0; base < a.num_reqs; base += 32) {
+      const int i = base + lane;
+      int64_t mine = 0;
+      if (i < a.num_reqs) {
+        const ReqGeom gi = req_geom(a, i);
+        mine = units_before(gi, gi.qtiles) * a.heads;
+      }
+      int64_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > lo);
+      if (hit != 0u) {
+        const int l = __ffs(hit) - 1;
+        req = base + l;
+        acc += __shfl_sync(0xffffffffu, incl - mine, l);
+        break;
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    g = req_geom(a, req);
+    const int64_t uph = units_before(g, g.qtiles);  // units per head
+    int64_t off = lo - acc;
+    head = static_cast<int>(off / uph);
+    off -= head * uph;
+    // the tile holding unit `off`: the last qt with units_before(qt) <= off
+    int t_lo = 0, t_hi = g.qtiles - 1;
+    while (t_lo < t_hi) {
+      const int mid = (t_lo + t_hi + 1) >> 1;
+      if (units_before(g, mid) <= off) t_lo = mid;
+      else t_hi = mid - 1;
+    }
+    qt = t_lo;
+    p = static_cast<int>(off - units_before(g, qt));
+    load_tile();
+  }
+  __device__ __forceinline__ bool valid() const { return left > 0; }
+  // Next unit; true when it starts a new query tile.
+  __device__ __forceinline__ bool advance(const PrefillArgs& a) {
+    --left;
+    if (++p < np) return false;
+    p = 0;
+    if (++qt == g.qtiles) {
+      qt = 0;
+      if (++head == a.heads) {
+        head = 0;
+        // the next request with query rows (one without any has no units)
+        do {
+          ++req;
+          if (req >= a.num_reqs) return true;  // only past the end of the list
+          g = req_geom(a, req);
+        } while (g.qtiles == 0);
+      }
+    }
+    load_tile();
     return true;
   }
 };
@@ -199,12 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem;
 
-  const int64_t G = gridDim.x;
-  const int64_t lo = a.total_units * blockIdx.x / G;
-  const int64_t hi = a.total_units * (blockIdx.x + 1) / G;
+  // This CTA's equal share of the batch's units (every warp computes it).
   UnitIter U;
-  U.init(a, lo, hi);
-  TileInfo T;
+  if (warp != 1) {
+    const int64_t total = UnitIter::total(a);
+    const int64_t G = gridDim.x;
+    U.init(a, total * blockIdx.x / G, total * (blockIdx.x + 1) / G);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -213,15 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_k = policy_evict_last();   // pages are re-read by later tiles
     const uint64_t pol_q = policy_evict_first();
     const int nblk = (a.max_seq_len + kBlock - 1) / kBlock;  // table entries that exist
-    int cur_rh = -1, cur_qt = -1;
     int pg_req = -1, pg_base = 0, pg = -1;
     uint32_t tq = 0, it = 0, st = 0, ph = 0;
     bool ok = true;
-    for (; ok && U.valid(); U.advance(a)) {
-      T.refresh(a, U);
+    bool new_tile = true;  // the share's first unit starts a tile for this CTA
+    for (; ok && U.valid(); new_tile |= U.advance(a)) {
       const int b0 = 2 * U.p;
-      if (b0 >= T.nvis) continue;  // no visible token
-      const bool two = b0 + 1 < T.nvis;
+      if (b0 >= U.nvis) continue;  // no visible token (the tile's rows are loaded with its next unit)
+      const bool two = b0 + 1 < U.nvis;
       if (U.req != pg_req || b0 < pg_base || b0 + 1 >= pg_base + 32) {
         pg_req = U.req;
         pg_base = b0;
@@ -233,7 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pb = __shfl_sync(0xffffffffu, pg, b0 + 1 - pg_base);
       if (it >= static_cast<uint32_t>(kStages)) ok = warp_wait(&empty[st], ph ^ 1u, abort_flag);
       if (!ok) break;
-      const bool new_tile = U.rh != cur_rh || U.qt != cur_qt;
       if (lane == 0) {
         sInfo[st] = kInfoValid | (two ? kInfoTwo : 0u) | (new_tile ? kInfoNewTile : 0u);
         uint8_t* dst = sK + st * kStageBytes;
@@ -261,12 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (new_tile) {
         // The tile's query rows, once the MMAs of the previous tile are done
         // (issued after this unit's keys, which do not depend on them).
-        cur_rh = U.rh;
-        cur_qt = U.qt;
+        new_tile = false;
         if (tq > 0) ok = warp_wait(q_empty, (tq - 1) & 1u, abort_flag);
         if (!ok) break;
         if (lane == 0) {
-          const int tok0 = U.req * a.query_len + U.qt * 128;
+          const int tok0 = U.g.qbeg + U.qt * 128;
           mbar_arrive_expect_tx(q_full, kPage);
           tma_load_3d(sQ, &qmap, q_full, 0, U.head, tok0, pol_q);
           tma_load_3d(sQ + kHalf, &qmap, q_full, 64, U.head, tok0, pol_q);
@@ -347,18 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool row_ok = false;
     int pos = 0;
     float* srow = nullptr;
-    for (; ok && U.valid(); U.advance(a)) {
-      if (T.refresh(a, U)) {
+    bool new_tile = true;
+    for (; ok && U.valid(); new_tile = U.advance(a)) {
+      if (new_tile) {
         const int qrow = U.qt * 128 + r;  // query index inside the request
-        row_ok = qrow < a.query_len;
-        pos = T.prefix + qrow;
-        srow = a.score + U.head * a.s_head +
-               (static_cast<int64_t>(U.req) * a.query_len + qrow) * a.s_row;
+        row_ok = qrow < U.g.ql;
+        pos = U.g.prefix + qrow;
+        srow = a.score + U.head * a.s_head + static_cast<int64_t>(U.g.qbeg + qrow) * a.s_row;
       }
       const int b0 = 2 * U.p;
-      if (b0 < T.nvis) {
+      if (b0 < U.nvis) {
         const int b = b0 + team;
-        const bool mine = b < T.nvis;
+        const bool mine = b < U.nvis;
         bool got = true;
         if (lane == 0) got = mbar_wait(&acc_full[acc], (it >> 1) & 1u, abort_flag);
         if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -366,46 +444,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t v0[32], v1[32], v2[32], v3[32];
+        // The row's 128 columns in two halves (64 registers live), then the
+        // accumulator goes back.
+        const int lim = row_ok ? pos - b * 128 : -1;  // columns 0..lim are visible
+        float m0 = -INFINITY, m1 = -INFINITY;
         if (mine) {
           const uint32_t taddr =
               tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256 + team * 128;
-          tmem_ld32(taddr, v0);
-          tmem_ld32(taddr + 32, v1);
-          tmem_ld32(taddr + 64, v2);
-          tmem_ld32(taddr + 96, v3);
-          tmem_ld_wait32x4(v0, v1, v2, v3);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(taddr + 64 * h, v0);
+            tmem_ld32(taddr + 64 * h + 32, v1);
+            tmem_ld_wait32x2(v0, v1);
+            if (lim >= 127) {
+#pragma unroll
+              for (int k = 0; k < 32; k += 4) {
+                m0 = fmax3(m0, __uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
+                m1 = fmax3(m1, __uint_as_float(v0[k + 2]), __uint_as_float(v0[k + 3]));
+                m0 = fmax3(m0, __uint_as_float(v1[k]), __uint_as_float(v1[k + 1]));
+                m1 = fmax3(m1, __uint_as_float(v1[k + 2]), __uint_as_float(v1[k + 3]));
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                if (64 * h + k <= lim) m0 = fmaxf(m0, __uint_as_float(v0[k]));
+                if (64 * h + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(v1[k]));
+              }
+            }
+          }
         }
-        // The columns are in registers: hand the accumulator back first.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        if (mine && row_ok) {
-          const int lim = pos - b * 128;  // columns 0..lim are visible
-          float m0 = -INFINITY, m1 = -INFINITY;
-          if (lim >= 127) {
-#pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-              m0 = fmax3(m0, __uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(v0[k + 2]), __uint_as_float(v0[k + 3]));
-              m0 = fmax3(m0, __uint_as_float(v1[k]), __uint_as_float(v1[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(v1[k + 2]), __uint_as_float(v1[k + 3]));
-              m0 = fmax3(m0, __uint_as_float(v2[k]), __uint_as_float(v2[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(v2[k + 2]), __uint_as_float(v2[k + 3]));
-              m0 = fmax3(m0, __uint_as_float(v3[k]), __uint_as_float(v3[k + 1]));
-              m1 = fmax3(m1, __uint_as_float(v3[k + 2]), __uint_as_float(v3[k + 3]));
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              if (k <= lim) m0 = fmaxf(m0, __uint_as_float(v0[k]));
-              if (32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(v1[k]));
-              if (64 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v2[k]));
-              if (96 + k <= lim) m1 = fmaxf(m1, __uint_as_float(v3[k]));
-            }
-          }
-          srow[b] = fmaxf(m0, m1) * a.sm_scale;
-        }
+        if (mine && row_ok) srow[b] = fmaxf(m0, m1) * a.sm_scale;
         ++it;
         acc ^= 1u;
       }
@@ -414,11 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // on consecutive blocks, so the stores coalesce.
       if (a.fill_width > 0 && team == 0 && U.p == U.np - 1) {
         const int row0 = U.qt * 128 + quad * 32;
-        const int nrows = min(32, a.query_len - row0);
-        float* base = a.score + U.head * a.s_head +
-                      (static_cast<int64_t>(U.req) * a.query_len + row0) * a.s_row;
+        const int nrows = min(32, U.g.ql - row0);
+        float* base = a.score + U.head * a.s_head + static_cast<int64_t>(U.g.qbeg + row0) * a.s_row;
         for (int rr = 0; rr < nrows; ++rr)
-          for (int b = T.nvis + lane; b < a.fill_width; b += 32) base[rr * a.s_row + b] = -INFINITY;
+          for (int b = U.nvis + lane; b < a.fill_width; b += 32) base[rr * a.s_row + b] = -INFINITY;
       }
     }
   }

@@ -6,6 +6,10 @@
 // output [heads, total_q, topk] of logical block ids counted from 0, -1 pad) and the
 // "indexer_cp_exchange" page (ranking by score, then lower block id).
 //
+// Rows: query_len per request, or, for a ragged batch, the rows
+// cu[i]..cu[i+1]-1 of request i (minimax_m3_index_topk: cu_seqlens_q and
+// prefix_lens), row j of request i at position seq_len[i] - rows_i + j.
+//
 // Per row: forced blocks F = [0, f_lo) and [l_lo, c]; candidates are the
 // visible blocks in [f_lo, l_lo).  When there are at most m = topk - |F| of
 // them the row is simply 0..c.  Otherwise the warp takes the candidates 256
@@ -71,26 +75,56 @@ __device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
+// Ragged batches: the request owning `row` (the last i with cu[i] <= row)
+// and the row's index j in it; false when the offsets do not place the row
+// inside its request (malformed offsets).
+__device__ __forceinline__ bool ragged_row(const SelectArgs& a, int64_t row, int& i, int& j,
+                                           int& ql) {
+  int lo = 0, hi = a.num_reqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.cu + mid) <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  i = lo;
+  const int b = __ldg(a.cu + i), e = __ldg(a.cu + i + 1);
+  ql = e - b;
+  j = static_cast<int>(row - b);
+  return b <= row && row < e;
+}
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const SelectArgs a) {
   __shared__ uint64_t s_buf[kWarpsPerBlock][32];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   uint64_t* buf = s_buf[wib];
-  const int64_t rows = static_cast<int64_t>(a.num_reqs) * a.query_len;
+  const int64_t rows = a.total_q;
   const int64_t work = rows * a.heads;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  if (a.cu != nullptr && blockIdx.x == 0 && wib == 0) {
+    // the offsets must run from 0 to total_q without decreasing
+    bool bad = lane == 0 && (__ldg(a.cu) != 0 || __ldg(a.cu + a.num_reqs) != a.total_q);
+    for (int i = lane; i < a.num_reqs; i += 32) bad |= __ldg(a.cu + i + 1) < __ldg(a.cu + i);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, MM3IDX_DEV_BAD_ROWS);
+  }
   // 32-bit index arithmetic when the problem allows it (64-bit divisions
   // cost more than the selection itself).
   const bool small = work < (int64_t{1} << 31);
   for (int64_t w = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib; w < work; w += nwarps) {
     int h, i, j;
     int64_t row;
-    if (small) {
+    int ql = a.query_len;
+    bool row_ok = true;
+    if (a.cu != nullptr) {
+      h = static_cast<int>(w / rows);
+      row = w - static_cast<int64_t>(h) * rows;
+      row_ok = ragged_row(a, row, i, j, ql);
+    } else if (small) {
       const uint32_t w32 = static_cast<uint32_t>(w), rows32 = static_cast<uint32_t>(rows);
-      const uint32_t ql = static_cast<uint32_t>(a.query_len);
+      const uint32_t ql32 = static_cast<uint32_t>(a.query_len);
       h = static_cast<int>(w32 / rows32);
       const uint32_t r32 = w32 - static_cast<uint32_t>(h) * rows32;
-      i = static_cast<int>(r32 / ql);
-      j = static_cast<int>(r32 - static_cast<uint32_t>(i) * ql);
+      i = static_cast<int>(r32 / ql32);
+      j = static_cast<int>(r32 - static_cast<uint32_t>(i) * ql32);
       row = r32;
     } else {
       h = static_cast<int>(w / rows);
@@ -99,8 +133,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
       j = static_cast<int>(row - static_cast<int64_t>(i) * a.query_len);
     }
     const int seq = min(max(__ldg(a.seq_lens + i), 0), a.max_seq_len);
-    const int pos = seq - a.query_len + j;
-    const int c = pos >= 0 ? (pos >> 7) : -1;
+    const int pos = seq - ql + j;
+    const int c = row_ok && pos >= 0 ? (pos >> 7) : -1;
     int32_t* out = a.ids + h * a.i_head + row * a.i_row;
     const int topk = a.topk;
     if (c < 0) {
@@ -208,7 +242,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s) {
-  const int64_t work = static_cast<int64_t>(a.num_reqs) * a.query_len * a.heads;
+  const int64_t work = static_cast<int64_t>(a.total_q) * a.heads;
   int64_t blocks = (work + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;

@@ -66,14 +66,23 @@ def check_ids_row(got_row, want_row, scores, c, topk, init_blocks, local_blocks,
         assert b in cand and scores[b] >= kth - tol, f"{where}: pick {b} too weak {got_row}"
 
 
+def row_request(wl, r):
+    """(request, index in it, rows of it) of batch row r, uniform or ragged."""
+    if wl.cu_seqlens is None:
+        i, j = divmod(r, wl.query_len)
+        return i, j, wl.query_len
+    i = int(np.searchsorted(wl.cu_seqlens, r, side="right")) - 1
+    return i, r - int(wl.cu_seqlens[i]), int(wl.cu_seqlens[i + 1] - wl.cu_seqlens[i])
+
+
 def check_ids(got, want, scores, wl, rows=None, where=""):
     """got/want int32 [H, R, topk] (or the sampled rows), scores fp64 [H, R, W]."""
     H = got.shape[0]
     rows = range(got.shape[1]) if rows is None else rows
     for h in range(H):
         for k, r in enumerate(rows):
-            i, j = divmod(r, wl.query_len)
-            pos = int(min(max(wl.seq_lens[i], 0), wl.max_seq_len)) - wl.query_len + j
+            i, j, ql = row_request(wl, r)
+            pos = int(min(max(wl.seq_lens[i], 0), wl.max_seq_len)) - ql + j
             c = pos // BLOCK if pos >= 0 else -1
             check_ids_row(got[h, k], want[h, k], scores[h, k], c, wl.topk, wl.init_blocks,
                           wl.local_blocks, where=f"{where} h{h} row{r}")

@@ -38,11 +38,13 @@ def test_constants_match_binding():
     c = header_constants()
     assert c["MM3IDX_OK"] == mm.OK
     assert c["MM3IDX_OP_DECODE"] == mm.OP_DECODE and c["MM3IDX_OP_PREFILL"] == mm.OP_PREFILL
+    assert c["MM3IDX_OP_PREFILL_NVFP4"] == mm.OP_PREFILL_NVFP4
     assert c["MM3IDX_MAX_TOPK"] == mm.MAX_TOPK
     assert c["MM3IDX_MAX_DECODE_ROWS"] == mm.MAX_DECODE_ROWS
     assert (c["MM3IDX_DEV_BAD_PAGE"], c["MM3IDX_DEV_SEQ_TOO_LONG"], c["MM3IDX_DEV_SEQ_TOO_SHORT"],
-            c["MM3IDX_DEV_TIMEOUT"]) == (mm.DEV_BAD_PAGE, mm.DEV_SEQ_TOO_LONG,
-                                         mm.DEV_SEQ_TOO_SHORT, mm.DEV_TIMEOUT)
+            c["MM3IDX_DEV_TIMEOUT"], c["MM3IDX_DEV_BAD_ROWS"]) == (
+                mm.DEV_BAD_PAGE, mm.DEV_SEQ_TOO_LONG, mm.DEV_SEQ_TOO_SHORT, mm.DEV_TIMEOUT,
+                mm.DEV_BAD_ROWS)
     assert mm.Problem.sm_scale.offset > mm.Problem.max_seq_len.offset
     for k, v in c.items():
         if k.startswith("MM3IDX_ERR_"):
@@ -123,9 +125,85 @@ def test_topk_validation():
     assert f(FAKE, 1000, 8, 1, FAKE, 0, 1, 1000, 4, 1, 1, FAKE, 100, 4, None) == 0
 
 
+def sparse_status(p=None, topk=4, **kw):
+    t = mm.SparseTable()
+    vals = dict(attention_block_table=FAKE, attention_table_stride=8, attention_table_width=8,
+                pages_per_block=2, block_page_stride=4, sparse_block_table_out=FAKE,
+                sparse_table_stride=topk * 2, sparse_context_lens_out=FAKE)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(t, k, v)
+    p = p or problem()
+    return mm.lib.mm3idx_decode_sparse_table(ctypes.byref(p), topk, 1, 1, FAKE, 1024, 4,
+                                             ctypes.byref(t), FAKE, 1 << 20, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(attention_block_table=None), -1),
+    (dict(sparse_block_table_out=None), -1),
+    (dict(sparse_context_lens_out=None), -1),
+    (dict(pages_per_block=0), -1),
+    (dict(pages_per_block=3, block_page_stride=3), -1),        # does not divide 128
+    (dict(pages_per_block=2, block_page_stride=6), -1),        # neither P nor 2P
+    (dict(pages_per_block=256, block_page_stride=256), -1),
+    (dict(attention_table_width=7), -4),                       # < cdiv(1000, 128)
+    (dict(attention_table_stride=4), -4),
+    (dict(sparse_table_stride=7), -8),                         # < topk * P
+])
+def test_sparse_table_validation(kw, code):
+    assert sparse_status(**kw) == code
+
+
+def test_sparse_table_needs_one_head_and_a_table():
+    assert sparse_status(problem(heads=2, q_token_stride=256)) == -10
+    p = problem()
+    assert mm.lib.mm3idx_decode_sparse_table(ctypes.byref(p), 4, 1, 1, FAKE, 1024, 4, None, FAKE,
+                                             1 << 20, None) == -1
+
+
+def test_nvfp4_prefill_validation_and_workspace():
+    p = problem()                                   # no scales: not an NVFP4 problem
+    f = mm.lib.mm3idx_prefill_nvfp4
+    assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -3
+    p = problem(index_scales=FAKE, num_reqs=0)
+    assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == 0
+    p = problem(index_scales=FAKE)
+    assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1000, None) == -9
+    n = ctypes.c_size_t(0)
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL_NVFP4, 2, 3, 300, 1000, 16,
+                                         ctypes.byref(n)) == 0
+    scores = 2 * 3 * 300 * 8 * 4                     # as OP_PREFILL, 256-byte multiple here
+    slots = 3 * 8                                    # requests x cdiv(1000, 128)
+    assert n.value == scores + slots * 128 * 128 * 2 + 256
+
+
+def test_ragged_validation():
+    f = mm.lib.mm3idx_prefill_ragged
+    p = problem(query_len=4)                        # 2 requests of at most 4 rows
+    assert f(ctypes.byref(p), FAKE, 9, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), None, 8, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), FAKE + 2, 8, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), FAKE, -1, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), FAKE, 0, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == 0
+    assert f(ctypes.byref(p), FAKE, 8, 4, 1, 1, FAKE, 1000, 4, FAKE, 100, None) == -9
+    g = mm.lib.mm3idx_score_ragged
+    assert g(ctypes.byref(p), FAKE, 9, FAKE, 1000, 8, None) == -1
+    assert g(ctypes.byref(p), FAKE, 0, FAKE, 1000, 8, None) == 0
+    assert g(ctypes.byref(p), FAKE, 8, FAKE, 1000, 7, None) == -8
+    t = mm.lib.mm3idx_topk_ragged
+    assert t(FAKE, 1000, 8, 1, FAKE, FAKE, 2, 9, 4, 1000, 4, 1, 1, FAKE, 100, 4, None) == -1
+    assert t(FAKE, 1000, 8, 1, FAKE, FAKE, 2, 0, 4, 1000, 4, 1, 1, FAKE, 100, 4, None) == 0
+    assert t(FAKE, 1000, 8, 1, FAKE, FAKE, 2, 8, 4, 1000, 40, 1, 1, FAKE, 100, 4, None) == -7
+
+
+def test_wait_timeout_check_validates_warps_before_any_launch():
+    assert mm.lib.mm3idx_check_wait_timeout(0, None) == -1
+    assert mm.lib.mm3idx_check_wait_timeout(33, None) == -1
+
+
 def test_workspace_query_validation():
     n = ctypes.c_size_t(0)
-    assert mm.lib.mm3idx_workspace_bytes(3, 1, 1, 1, 128, 4, ctypes.byref(n)) == -1
+    assert mm.lib.mm3idx_workspace_bytes(9, 1, 1, 1, 128, 4, ctypes.byref(n)) == -1
     assert mm.lib.mm3idx_workspace_bytes(mm.OP_DECODE, 1, 1, 1, 128, 40, ctypes.byref(n)) == -7
     assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 16, ctypes.byref(n)) == 0
     assert n.value == 2 * 3 * 300 * 8 * 4      # [heads, rows, roundup(cdiv(1000,128), 4)] fp32

@@ -306,7 +306,19 @@ def _nvfp4_prefill(seed=5, seq=32768):
                  max_seq_len=seq, kv_format="nvfp4")
 
 
-# The five named workloads, by short key, and the NVFP4 prefill.  The second argument of each maker
+def _chunked_prefill(seed=6, num_reqs=8):
+    """A ragged prefill batch: request i brings U[1000, 8000] new tokens after
+    U[0, 24000] earlier ones (chunked prefill); not one of the five named
+    configurations."""
+    rng = np.random.default_rng(1000 + seed)
+    ql = rng.integers(1000, 8000, size=num_reqs, endpoint=True)
+    pre = rng.integers(0, 24000, size=num_reqs, endpoint=True)
+    return ragged_case(seed, query_lens=ql, prefix_lens=pre, heads=1, topk=16, init_blocks=1,
+                       local_blocks=2, max_seq_len=32768)
+
+
+# The five named workloads, by short key, the NVFP4 prefill and a chunked
+# (ragged) prefill batch.  The second argument of each maker
 # (request count / sequence length) lets tests draw a smaller case with the
 # same recipe.
 WORKLOADS = {
@@ -316,6 +328,7 @@ WORKLOADS = {
     "prefill": _causal_prefill,
     "nvfp4_decode": _nvfp4_decode,
     "nvfp4_prefill": _nvfp4_prefill,
+    "chunked_prefill": _chunked_prefill,
 }
 
 
