@@ -45,7 +45,7 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel sources whose hash a committed ncu summary must match for its
 # dram traffic to be reported
 DECODE_SOURCES = ["decode.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
-PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "internal.h"]
+PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
 
 
 def parse_args():
@@ -320,8 +320,44 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                                       query_len=wl.query_len, **kw)
     else:
         fn = lambda: mm.prefill(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len, **kw)  # noqa: E731
+    fused = wl.topk <= 16
     with torch.cuda.stream(stream):
         ms_all = timed_steps(torch, fn, steps, warmup, flush, stream)
+    if fused:
+        # topk <= 16: the scorer keeps each row's candidates and a small merge
+        # kernel writes the ids (after the dequant pass for NVFP4); `value` is
+        # the whole step's rate.  The roofline is the scorer kernel's: the
+        # same kernel in score mode, timed alone through the score call
+        # (bf16, uniform rows), which also writes -inf past each row's block.
+        assert mm.get_device_error(stream) == 0, "device status word set"
+        t_all = statistics.mean(ms_all) * 1e-3
+        fl = prefill_flops(wl)
+        res = dict(value=fl / t_all / 1e12, unit="TFLOP/s (scores + top-k)",
+                   rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3)
+        t_sc = None
+        if not nvfp4 and not ragged:
+            width = -(-wl.max_seq_len // BLOCK)
+            sc_out = torch.empty((wl.heads, wl.rows, width), dtype=torch.float32, device=dev)
+            scf = lambda: mm.score(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len,  # noqa: E731
+                                   max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale, out=sc_out,
+                                   stream=stream)
+            with torch.cuda.stream(stream):
+                ms_sc = timed_steps(torch, scf, steps, warmup, flush, stream)
+            t_sc = statistics.mean(ms_sc) * 1e-3
+            res["scorer_ms"] = t_sc * 1e3
+            del sc_out
+        t_roof = t_sc if t_sc is not None else t_all
+        res["roofline"] = dict(bound="tensor", achieved=fl / t_roof / 1e12,
+                               peak=pk["bf16_tflops"], unit="TFLOP/s",
+                               frac=fl / t_roof / 1e12 / pk["bf16_tflops"],
+                               traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
+                                                        PREFILL_SOURCES) if t_sc else None,
+                               algorithmic_flops=fl,
+                               kernel="score-mode prefill kernel alone" if t_sc
+                               else "whole step (scores + top-k)",
+                               peak_source=pk["source"] + " cuBLAS bf16 burst")
+        return res
+    with torch.cuda.stream(stream):
         w = (-(-wl.max_seq_len // BLOCK) + 3) // 4 * 4
         sc = ws.view(torch.float32)[: wl.heads * wl.rows * w].view(wl.heads, wl.rows, w)
         if ragged:
@@ -473,7 +509,7 @@ def run_ours(args):
         w5 = W.make("nvfp4_prefill")
         r5 = bench_prefill(mm, torch, w5, max(10, args.steps // 10), 3, flush, stream, pk)
         r5["workload"] = w5.name
-        r5["unit"] = "TFLOP/s (dequant + scorer)"
+        r5["unit"] = "TFLOP/s (dequant + scores + top-k)"
         r5["roofline"]["traffic"] = None      # two kernels; the summaries cover the bf16 scorer
         extra["nvfp4_prefill"] = r5
         del w5

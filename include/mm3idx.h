@@ -154,10 +154,14 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
  * op = MM3IDX_OP_DECODE: one ticket counter per request plus the partial
  * top-k candidate lists of requests split across CTAs (depends on the
  * current device's SM count).
- * op = MM3IDX_OP_PREFILL: the fp32 score scratch [heads, rows, roundup(cdiv(max_seq_len,128), 4)].
- * op = MM3IDX_OP_PREFILL_NVFP4: that scratch (rounded up to 256 bytes), then
- * a bf16 copy of the keys [num_reqs * cdiv(max_seq_len,128), 128, 128] and
- * an int32 table [num_reqs, cdiv(max_seq_len,128)].
+ * op = MM3IDX_OP_PREFILL: topk <= 16 (selection inside the scorer): one
+ * ticket word per (tile of 128 query rows, lane quadrant) and two candidate
+ * lists per row of each tile a CTA touches (depends on the current device's
+ * SM count); topk > 16: the fp32 score scratch
+ * [heads, rows, roundup(cdiv(max_seq_len,128), 4)] for the selector.
+ * op = MM3IDX_OP_PREFILL_NVFP4: that (rounded up to 256 bytes), then a bf16
+ * copy of the keys [num_reqs * cdiv(max_seq_len,128), 128, 128] and an
+ * int32 table [num_reqs, cdiv(max_seq_len,128)].
  * Writes the size to *bytes.  Reads the current device's attributes; no
  * allocation.
  */
@@ -248,11 +252,15 @@ int mm3idx_decode_sparse_table(const mm3idx_problem_t *p, int32_t topk,
                                void *stream);
 
 /*
- * mm3idx_prefill -- prefill scoring on the tensor cores followed by the
- * selector (index_topk, minimax_m3_index_score then minimax_m3_index_topk).
- * The fp32 scores go to the workspace (size from
- * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL, ...), 256-byte aligned, no
- * initialisation needed).  out as in mm3idx_decode.  Any heads/query_len.
+ * mm3idx_prefill -- prefill scoring on the tensor cores and top-k selection
+ * (index_topk, minimax_m3_index_score then minimax_m3_index_topk).  For
+ * topk <= 16 the scorer selects as it goes: each row's best candidates stay
+ * in registers and the CTAs that share a query tile merge them at its end,
+ * so no score tensor is written; the call clears the workspace's ticket
+ * words first (cudaMemsetAsync on `stream`).  For larger topk the fp32
+ * scores go to the workspace and the selector follows.  Workspace:
+ * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL, ...) bytes, 256-byte aligned, no
+ * initialisation needed.  out as in mm3idx_decode.  Any heads/query_len.
  */
 int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
                    int32_t local_blocks, int32_t *out, int64_t out_head_stride,

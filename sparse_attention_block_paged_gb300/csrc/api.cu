@@ -176,20 +176,39 @@ size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_l
   return decode_ws_head(num_reqs) + slots * 32 * decode_tk(topk) * 8;
 }
 
-size_t prefill_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len, int32_t max_seq_len) {
-  const int64_t w = (cdiv(max_seq_len, kBlock) + 3) / 4 * 4;
-  return static_cast<size_t>(heads) * num_reqs * query_len * w * 4;
-}
-
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// NVFP4 prefill workspace: [scores as the bf16 prefill][bf16 pages:
-// num_reqs x cdiv(max_seq_len,128) x 32 KB][identity table, int32].
-size_t prefill_nvfp4_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len,
-                              int32_t max_seq_len) {
+// Prefill workspace, part A.  topk <= kPrefillSelectTK (selection fused into
+// the scorer): tile records [tiles][kTileRecInts] (256-aligned), then
+// 2 * (grid + tiles) list slots of 128 rows x kPrefillSelectTK keys.  Larger topk: the fp32
+// scores [heads, rows, roundup(cdiv(max_seq_len,128), 4)] for the selector.
+// `rows` bounds the batch's query rows; tiles are bounded by
+// heads * (cdiv(rows, 128) + num_reqs).
+int64_t prefill_tiles_bound(int32_t heads, int32_t num_reqs, int64_t rows) {
+  return static_cast<int64_t>(heads) * (cdiv(rows, 128) + num_reqs);
+}
+
+size_t prefill_part_a(int sms, int32_t heads, int32_t num_reqs, int32_t query_len,
+                      int32_t max_seq_len, int32_t topk) {
+  const int64_t rows = static_cast<int64_t>(num_reqs) * query_len;
+  if (topk <= kPrefillSelectTK) {
+    const int64_t tiles = prefill_tiles_bound(heads, num_reqs, rows);
+    return align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4) +
+           static_cast<size_t>(2 * (sms + tiles)) * 128 * kPrefillSelectTK * 8;
+  }
+  const int64_t w = (cdiv(max_seq_len, kBlock) + 3) / 4 * 4;
+  return static_cast<size_t>(heads) * rows * w * 4;
+}
+
+// Whole prefill workspace: part A, then for NVFP4 a bf16 copy of the keys
+// [num_reqs * cdiv(max_seq_len,128), 128, 128] and an int32 table
+// [num_reqs, cdiv(max_seq_len,128)].
+size_t prefill_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len,
+                        int32_t max_seq_len, int32_t topk, bool nvfp4) {
+  const size_t a = prefill_part_a(sms, heads, num_reqs, query_len, max_seq_len, topk);
+  if (!nvfp4) return a;
   const size_t slots = static_cast<size_t>(num_reqs) * cdiv(max_seq_len, kBlock);
-  return align256(prefill_ws_bytes(heads, num_reqs, query_len, max_seq_len)) +
-         slots * kBlock * kD * 2 + align256(slots * 4);
+  return align256(a) + slots * kBlock * kD * 2 + align256(slots * 4);
 }
 
 DecodeArgs decode_args(const mm3idx_problem_t* p, int* status) {
@@ -300,10 +319,27 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
 
 // Scores of a batch on the tensor-core scorer; cu == nullptr: query_len
 // rows per request, else the ragged row offsets (total_q rows).
+// Selection fused into the prefill scorer (topk <= kPrefillSelectTK).
+struct PrefillSelect {
+  int32_t* ids;
+  int64_t i_head, i_row;
+  int32_t topk, init_blocks, local_blocks;
+  uint64_t* partials;
+  int32_t* tile_rec;
+  int64_t tiles;              // records (a bound on the batch's tiles)
+};
+
 int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q, float* out,
-                   int64_t head_stride, int64_t row_stride, int32_t fill_width, int sms,
-                   int32_t* status, cudaStream_t s) {
+                   int64_t head_stride, int64_t row_stride, int sms, int32_t* status,
+                   cudaStream_t s, const PrefillSelect* sel = nullptr) {
   PrefillArgs a{};
+  if (sel) {
+    a.topk = sel->topk;
+    a.init_blocks = sel->init_blocks;
+    a.local_blocks = sel->local_blocks;
+    a.partials = sel->partials;
+    a.tile_rec = sel->tile_rec;
+  }
   a.heads = p->heads;
   a.num_reqs = p->num_reqs;
   a.query_len = p->query_len;
@@ -316,7 +352,6 @@ int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q
   a.score = out;
   a.s_head = head_stride;
   a.s_row = row_stride;
-  a.fill_width = fill_width;
   a.cu = cu;
   a.total_q = total_q;
   a.status = status;
@@ -331,7 +366,22 @@ int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q
   int rc;
   if ((rc = make_qmap(p, total_q, &qmap))) return rc;
   if ((rc = make_kmap(p, &kmap))) return rc;
-  return cuda_status(launch_prefill(qmap, kmap, a, static_cast<int>(grid), s));
+  if ((rc = cuda_status(launch_prefill(qmap, kmap, a, static_cast<int>(grid), s)))) return rc;
+  if (!sel) return MM3IDX_OK;
+  PrefillMergeArgs m{};
+  m.partials = sel->partials;
+  m.tile_rec = sel->tile_rec;
+  m.tiles = sel->tiles;
+  m.grid = static_cast<int32_t>(grid);
+  m.heads = p->heads;
+  m.total_q = total_q;
+  m.topk = sel->topk;
+  m.init_blocks = sel->init_blocks;
+  m.local_blocks = sel->local_blocks;
+  m.ids = sel->ids;
+  m.i_head = sel->i_head;
+  m.i_row = sel->i_row;
+  return cuda_status(launch_prefill_merge(m, s));
 }
 
 SelectArgs select_args(const float* score, int64_t sh, int64_t sr, int32_t heads,
@@ -358,6 +408,21 @@ SelectArgs select_args(const float* score, int64_t sh, int64_t sr, int32_t heads
   a.i_row = orow;
   a.status = status;
   return a;
+}
+
+// The score calls on the tensor-core scorer: the scores of the visible
+// blocks, then -inf past each row's block up to `width` by a row-parallel
+// kernel (in the scorer's epilogue that fill fell mostly on the CTAs of the
+// first, short tiles and held up their MMAs).
+int score_then_fill(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q, float* out,
+                    int64_t head_stride, int64_t row_stride, int32_t width, DeviceInfo* dev,
+                    cudaStream_t s) {
+  int rc = prefill_scores(p, cu, total_q, out, head_stride, row_stride, dev->sms, dev->status, s);
+  if (rc) return rc;
+  SelectArgs f = select_args(out, head_stride, row_stride, p->heads, p->seq_lens, p->num_reqs,
+                             p->query_len, cu, total_q, p->max_seq_len, 1, 0, 0, nullptr, 0, 0,
+                             dev->status);
+  return cuda_status(launch_fill_invisible(f, width, dev->sms, s));
 }
 
 // Ragged batches: row offsets on the device, total_q rows, at most
@@ -393,9 +458,11 @@ int run_topk(const float* score, int64_t sh, int64_t sr, int32_t heads, const in
   return cuda_status(launch_select(a, dev->sms, static_cast<cudaStream_t>(stream)));
 }
 
-// Prefill: scores to the workspace, then the selector.  NVFP4 keys are first
-// dequantised, once per page, into a bf16 copy in the workspace.  cu ==
-// nullptr: query_len rows per request; else ragged (total_q rows).
+// Prefill.  topk <= kPrefillSelectTK: the scorer selects as it goes (no
+// score tensor); larger topk: scores to the workspace, then the selector.
+// NVFP4 keys are first dequantised, once per page, into a bf16 copy in the
+// workspace.  cu == nullptr: query_len rows per request; else ragged
+// (total_q rows).
 int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_t total_q,
                 int32_t topk, int32_t init_blocks, int32_t local_blocks, int32_t* out,
                 int64_t out_head_stride, int64_t out_row_stride, void* workspace,
@@ -415,19 +482,21 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   const int64_t width = cdiv(p->max_seq_len, kBlock);
   if (nvfp4 && static_cast<int64_t>(p->num_reqs) * width > INT_MAX / kBlock)
     return MM3IDX_ERR_UNSUPPORTED;
-  const size_t need = nvfp4 ? prefill_nvfp4_ws_bytes(p->heads, p->num_reqs, p->query_len,
-                                                     p->max_seq_len)
-                            : prefill_ws_bytes(p->heads, p->num_reqs, p->query_len, p->max_seq_len);
+  // The fused selection's workspace depends on the grid (the SM count); the
+  // two-kernel one does not, so it is checked before any CUDA call.
+  DeviceInfo* dev = nullptr;
+  if (topk <= kPrefillSelectTK && (rc = device_info(&dev))) return rc;
+  const size_t need = prefill_ws_bytes(dev ? dev->sms : 0, p->heads, p->num_reqs, p->query_len,
+                                       p->max_seq_len, topk, nvfp4);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MM3IDX_ERR_WORKSPACE;
-  DeviceInfo* dev = nullptr;
-  if ((rc = device_info(&dev))) return rc;
+  if (!dev && (rc = device_info(&dev))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len,
+                                                p->max_seq_len, topk));
   mm3idx_problem_t q = *p;
   if (nvfp4) {
-    const size_t score_bytes = align256(prefill_ws_bytes(p->heads, p->num_reqs, p->query_len,
-                                                         p->max_seq_len));
     const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
     DequantArgs d{};
     d.codes = static_cast<const uint8_t*>(p->index_cache);
@@ -439,8 +508,8 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
     d.num_reqs = p->num_reqs;
     d.max_seq_len = p->max_seq_len;
     d.width = static_cast<int32_t>(width);
-    d.pages_out = reinterpret_cast<uint16_t*>(ws + score_bytes);
-    d.table_out = reinterpret_cast<int32_t*>(ws + score_bytes + slots * kBlock * kD * 2);
+    d.pages_out = reinterpret_cast<uint16_t*>(ws + part_a);
+    d.table_out = reinterpret_cast<int32_t*>(ws + part_a + slots * kBlock * kD * 2);
     d.status = dev->status;
     if ((rc = cuda_status(launch_dequant_pages(d, dev->sms, s)))) return rc;
     // the bf16 scorer then reads the copy through an identity table
@@ -451,9 +520,25 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
     q.table_stride = width;
     q.table_width = static_cast<int32_t>(width);
   }
+  if (topk <= kPrefillSelectTK) {
+    const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
+                                              static_cast<int64_t>(p->num_reqs) * p->query_len);
+    PrefillSelect sel{};
+    sel.ids = out;
+    sel.i_head = out_head_stride;
+    sel.i_row = out_row_stride;
+    sel.topk = topk;
+    sel.init_blocks = init_blocks;
+    sel.local_blocks = local_blocks;
+    sel.tile_rec = reinterpret_cast<int32_t*>(ws);
+    sel.tiles = tiles;
+    sel.partials = reinterpret_cast<uint64_t*>(
+        ws + align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4));
+    return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel);
+  }
   const int64_t w = (width + 3) / 4 * 4;
   float* score = reinterpret_cast<float*>(ws);
-  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, 0, dev->sms, dev->status, s)))
+  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, dev->sms, dev->status, s)))
     return rc;
   SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
                              cu, total_q, p->max_seq_len, topk, init_blocks, local_blocks, out,
@@ -524,12 +609,17 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t 
     *bytes = decode_ws_bytes(dev->sms, heads, num_reqs, query_len, topk);
     return MM3IDX_OK;
   }
-  if (op == MM3IDX_OP_PREFILL) {
-    *bytes = prefill_ws_bytes(heads, num_reqs, query_len, max_seq_len);
-    return MM3IDX_OK;
-  }
-  if (op == MM3IDX_OP_PREFILL_NVFP4) {
-    *bytes = prefill_nvfp4_ws_bytes(heads, num_reqs, query_len, max_seq_len);
+  if (op == MM3IDX_OP_PREFILL || op == MM3IDX_OP_PREFILL_NVFP4) {
+    if (topk < 1 || topk > MM3IDX_MAX_TOPK) return MM3IDX_ERR_TOPK;
+    int sms = 0;
+    if (topk <= kPrefillSelectTK) {   // the list slots depend on the grid
+      DeviceInfo* dev = nullptr;
+      int rc = device_info(&dev);
+      if (rc) return rc;
+      sms = dev->sms;
+    }
+    *bytes = prefill_ws_bytes(sms, heads, num_reqs, query_len, max_seq_len, topk,
+                              op == MM3IDX_OP_PREFILL_NVFP4);
     return MM3IDX_OK;
   }
   return MM3IDX_ERR_INVALID_ARGUMENT;
@@ -559,8 +649,8 @@ int mm3idx_score(const mm3idx_problem_t* p, float* out, int64_t out_head_stride,
     if ((rc = make_kmap(p, &kmap))) return rc;
     return cuda_status(launch_decode_bf16(kmap, a, decode_grid(p, dev->sms), s));
   }
-  return prefill_scores(p, nullptr, static_cast<int32_t>(rows), out, out_head_stride,
-                        out_row_stride, width, dev->sms, dev->status, s);
+  return score_then_fill(p, nullptr, static_cast<int32_t>(rows), out, out_head_stride,
+                         out_row_stride, width, dev, s);
 }
 
 int mm3idx_score_ragged(const mm3idx_problem_t* p, const int32_t* cu_seqlens_q, int32_t total_q,
@@ -575,8 +665,8 @@ int mm3idx_score_ragged(const mm3idx_problem_t* p, const int32_t* cu_seqlens_q, 
     return MM3IDX_ERR_OUT_LAYOUT;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
-  return prefill_scores(p, cu_seqlens_q, total_q, out, out_head_stride, out_row_stride, width,
-                        dev->sms, dev->status, static_cast<cudaStream_t>(stream));
+  return score_then_fill(p, cu_seqlens_q, total_q, out, out_head_stride, out_row_stride, width,
+                         dev, static_cast<cudaStream_t>(stream));
 }
 
 int mm3idx_topk(const float* score, int64_t score_head_stride, int64_t score_row_stride,

@@ -56,10 +56,30 @@ struct PrefillArgs {
   float sm_scale;
   float* score;
   int64_t s_head, s_row;
-  int32_t fill_width;         // 0: leave invisible blocks untouched; else write -inf up to it
   const int32_t* cu;          // ragged: [num_reqs + 1] query-row offsets; nullptr: query_len each
   int32_t total_q;            // rows of the batch
+  // fused selection (partials != nullptr; topk <= 16): candidate lists
+  // instead of scores, merged into ids by launch_prefill_merge
+  int32_t topk, init_blocks, local_blocks;
+  uint64_t* partials;         // [2 * (grid + tiles)] slots of [128 rows][16 keys]
+  int32_t* tile_rec;          // [1 + tiles][kTileRecInts]: [0][0] = tile count, then one per tile
   int32_t* status;
+};
+
+// Per query tile, written by the selecting prefill kernel for the merge:
+// first and last CTA holding its units, head, first row, rows, prefix,
+// tile index in its request, visible blocks, units total (2 words).
+constexpr int kTileRecInts = 16;
+
+struct PrefillMergeArgs {
+  const uint64_t* partials;
+  const int32_t* tile_rec;
+  int64_t tiles;              // a bound on the batch's tiles (the count is tile_rec[0])
+  int32_t grid;               // CTAs of the prefill launch
+  int32_t heads, total_q;     // bounds every record is checked against
+  int32_t topk, init_blocks, local_blocks;
+  int32_t* ids;
+  int64_t i_head, i_row;
 };
 
 struct SelectArgs {
@@ -116,7 +136,12 @@ cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int
 cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
+constexpr int kPrefillSelectTK = 16;  // list length of the fused prefill selection (topk <= 16)
+// The merge of the selecting prefill's lists; a programmatic dependent of it.
+cudaError_t launch_prefill_merge(const PrefillMergeArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
+// -inf for the blocks past each row's own block, up to `width` (score calls).
+cudaError_t launch_fill_invisible(const SelectArgs& a, int width, int num_sms, cudaStream_t s);
 cudaError_t launch_dequant_pages(const DequantArgs& a, int num_sms, cudaStream_t s);
 // Launched as a programmatic dependent of the kernel before it in the stream.
 cudaError_t launch_sparse_table(const SparseTableArgs& a, cudaStream_t s);

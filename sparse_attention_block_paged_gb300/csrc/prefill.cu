@@ -41,6 +41,7 @@
 #include "../../include/mm3idx.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "warp_select.cuh"
 
 namespace mm3idx {
 
@@ -137,21 +138,29 @@ __device__ __forceinline__ int64_t units_before(const ReqGeom& g, int qt) {
 struct UnitIter {
   int left = 0;  // units still to visit, this one included
   int req = 0, head = 0, qt = 0, p = 0, np = 0, nvis = 0;
+  int tile = 0;     // index of the (request, head, tile) in the batch
+  int64_t u = 0;    // index of the unit in the batch's list
   ReqGeom g;
 
-  // Total units of the batch (all lanes get it).
-  __device__ static int64_t total(const PrefillArgs& a) {
+  // Total units of the batch (all lanes get it); *tiles gets its tiles.
+  __device__ static int64_t total(const PrefillArgs& a, int* tiles = nullptr) {
     const int lane = threadIdx.x & 31;
     int64_t sum = 0;
+    int nt = 0;
     for (int base = 0; base < a.num_reqs; base += 32) {
       const int i = base + lane;
       if (i < a.num_reqs) {
         const ReqGeom gi = req_geom(a, i);
         sum += units_before(gi, gi.qtiles);
+        nt += gi.qtiles;
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      nt += __shfl_xor_sync(0xffffffffu, nt, o);
+    }
+    if (tiles) *tiles = nt * a.heads;
     return sum * a.heads;
   }
 
@@ -163,30 +172,41 @@ struct UnitIter {
   // Position at unit lo of the list; the share ends at hi.
   __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi) {
     left = static_cast<int>(hi - lo);
+    u = lo;
     if (left <= 0) return;
     const int lane = threadIdx.x & 31;
     int64_t acc = 0;  // units of the requests before `base`
+    int tacc = 0;     // tiles of the requests before `base`
     for (int base = 0; base < a.num_reqs; base += 32) {
       const int i = base + lane;
       int64_t mine = 0;
+      int tmine = 0;
       if (i < a.num_reqs) {
         const ReqGeom gi = req_geom(a, i);
         mine = units_before(gi, gi.qtiles) * a.heads;
+        tmine = gi.qtiles * a.heads;
       }
       int64_t incl = mine;
+      int tincl = tmine;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const int ty = __shfl_up_sync(0xffffffffu, tincl, o);
+        if (lane >= o) {
+          incl += y;
+          tincl += ty;
+        }
       }
       const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > lo);
       if (hit != 0u) {
         const int l = __ffs(hit) - 1;
         req = base + l;
         acc += __shfl_sync(0xffffffffu, incl - mine, l);
+        tacc += __shfl_sync(0xffffffffu, tincl - tmine, l);
         break;
       }
       acc += __shfl_sync(0xffffffffu, incl, 31);
+      tacc += __shfl_sync(0xffffffffu, tincl, 31);
     }
     g = req_geom(a, req);
     const int64_t uph = units_before(g, g.qtiles);  // units per head
@@ -202,14 +222,17 @@ struct UnitIter {
     }
     qt = t_lo;
     p = static_cast<int>(off - units_before(g, qt));
+    tile = tacc + head * g.qtiles + qt;
     load_tile();
   }
   __device__ __forceinline__ bool valid() const { return left > 0; }
   // Next unit; true when it starts a new query tile.
   __device__ __forceinline__ bool advance(const PrefillArgs& a) {
     --left;
+    ++u;
     if (++p < np) return false;
     p = 0;
+    ++tile;
     if (++qt == g.qtiles) {
       qt = 0;
       if (++head == a.heads) {
@@ -227,12 +250,25 @@ struct UnitIter {
   }
 };
 
+// Whether CTA c's share [total*c/G, total*(c+1)/G) holds any unit.
+__device__ __forceinline__ bool has_units(int c, int64_t total, int64_t G) {
+  return total * (c + 1) / G > total * c / G;
+}
+
+// The CTA whose share [total*c/G, total*(c+1)/G) holds unit x.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int64_t G) {
+  return static_cast<int>(((x + 1) * G - 1) / total);
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
+// kSelect: instead of the scores, the top-k ids (topk <= 16), see the
+// epilogue.
+template <bool kSelect>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap, const PrefillArgs a) {
@@ -279,12 +315,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem;
 
+  // No early launch of dependents (griddepcontrol.launch_dependents): the
+  // selection's merge CTAs would sit on the SMs waiting, beside this grid,
+  // which measured 20 % slower; they launch when this grid completes.
+
   // This CTA's equal share of the batch's units (every warp computes it).
   UnitIter U;
+  int64_t total = 0, share_lo = 0, share_hi = 0;
+  const int64_t G = gridDim.x;
   if (warp != 1) {
-    const int64_t total = UnitIter::total(a);
-    const int64_t G = gridDim.x;
-    U.init(a, total * blockIdx.x / G, total * (blockIdx.x + 1) / G);
+    int tiles = 0;
+    total = UnitIter::total(a, &tiles);
+    // the selection's merge reads the batch's tile count from the first record
+    if (kSelect && blockIdx.x == 0 && warp == 0 && lane == 0) a.tile_rec[0] = tiles;
+    share_lo = total * blockIdx.x / G;
+    share_hi = total * (blockIdx.x + 1) / G;
+    U.init(a, share_lo, share_hi);
+  }
+
+  if (a.cu != nullptr && blockIdx.x == 0 && warp == 0) {
+    // ragged batches: the offsets must run from 0 to total_q without decreasing
+    bool bad = lane == 0 && (__ldg(a.cu) != 0 || __ldg(a.cu + a.num_reqs) != a.total_q);
+    for (int i = lane; i < a.num_reqs; i += 32) bad |= __ldg(a.cu + i + 1) < __ldg(a.cu + i);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, MM3IDX_DEV_BAD_ROWS);
   }
 
   if (warp == 0) {
@@ -424,14 +477,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     bool row_ok = false;
     int pos = 0;
-    float* srow = nullptr;
+    float* srow = nullptr;   // score mode: the row's scores
+    int f_lo = 0, l_lo = 0;  // select mode: the row's forced blocks [0, f_lo), [l_lo, c]
+    RegList<kPrefillSelectTK> list;  // select mode: best non-forced keys of the tile so far
     bool new_tile = true;
     for (; ok && U.valid(); new_tile = U.advance(a)) {
       if (new_tile) {
         const int qrow = U.qt * 128 + r;  // query index inside the request
         row_ok = qrow < U.g.ql;
         pos = U.g.prefix + qrow;
-        srow = a.score + U.head * a.s_head + static_cast<int64_t>(U.g.qbeg + qrow) * a.s_row;
+        const int64_t row = U.g.qbeg + qrow;
+        if constexpr (kSelect) {
+          const Forced F(pos >= 0 ? pos >> 7 : -1, a.init_blocks, a.local_blocks);
+          f_lo = F.f_lo;
+          l_lo = F.l_lo;
+          list.clear();
+        } else {
+          srow = a.score + U.head * a.s_head + row * a.s_row;
+        }
       }
       const int b0 = 2 * U.p;
       if (b0 < U.nvis) {
@@ -477,19 +540,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        if (mine && row_ok) srow[b] = fmaxf(m0, m1) * a.sm_scale;
+        if (mine && row_ok) {
+          const float score = fmaxf(m0, m1) * a.sm_scale;
+          if constexpr (kSelect) {
+            if (b >= f_lo && b < l_lo) list.offer_shallow(make_key(score, b));
+          } else {
+            srow[b] = score;
+          }
+        }
         ++it;
         acc ^= 1u;
       }
       // The tile's last scheduled unit: blocks past the visible ones hold
       // -inf.  Each warp of team 0 fills its 32 rows one row at a time, lanes
       // on consecutive blocks, so the stores coalesce.
-      if (a.fill_width > 0 && team == 0 && U.p == U.np - 1) {
-        const int row0 = U.qt * 128 + quad * 32;
-        const int nrows = min(32, U.g.ql - row0);
-        float* base = a.score + U.head * a.s_head + static_cast<int64_t>(U.g.qbeg + row0) * a.s_row;
-        for (int rr = 0; rr < nrows; ++rr)
-          for (int b = U.nvis + lane; b < a.fill_width; b += 32) base[rr * a.s_row + b] = -INFINITY;
+      if constexpr (kSelect) {
+        // The last unit of the tile in this CTA's share: the warp's 32 lists
+        // (of this team's blocks) go to the tile's slot in the workspace,
+        // unless every row of the tile keeps all its blocks.  The CTA that
+        // holds the tile's first unit also leaves the tile's record.  A
+        // dependent kernel merges the lists after this one.
+        if (U.p == U.np - 1 || U.left == 1) {
+          constexpr int TK = kPrefillSelectTK;
+          if (U.nvis > a.topk) {
+            const int64_t slot = 2 * (static_cast<int64_t>(blockIdx.x) + U.tile) + team;
+            ulonglong2* dst = reinterpret_cast<ulonglong2*>(a.partials + (slot * 128 + r) * TK);
+#pragma unroll
+            for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
+          }
+          const int64_t tfirst = U.u - U.p, tlast = tfirst + U.np - 1;
+          if (warp == 2 && lane == 0 && tfirst >= share_lo) {
+            int32_t* rec = a.tile_rec + (static_cast<int64_t>(U.tile) + 1) * kTileRecInts;
+            rec[1] = tlast < share_hi ? static_cast<int>(blockIdx.x) : cta_of(tlast, total, G);
+            rec[2] = U.head;
+            rec[3] = U.g.qbeg;
+            rec[4] = U.g.ql;
+            rec[5] = U.g.prefix;
+            rec[6] = U.qt;
+            rec[7] = U.nvis;
+            rec[8] = static_cast<int32_t>(total & 0xffffffff);
+            rec[9] = static_cast<int32_t>(total >> 32);
+            rec[0] = static_cast<int>(blockIdx.x);
+          }
+        }
       }
     }
   }
@@ -505,13 +598,93 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// The fused prefill's selection, finished: warp per (query tile, lane
+// quadrant).  A tile whose last row sees at most topk blocks keeps them all
+// (rows 0..c); otherwise the 32 rows' lists of every CTA that held part of
+// the tile (one list per team) are merged and the rows written.  Launched
+// as a programmatic dependent of the prefill kernel, whose completion it
+// waits for on the GPU.
+constexpr int kMergeWarps = 2;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const PrefillMergeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int TK = kPrefillSelectTK;
+  const int lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int64_t tile = item >> 2;
+  const int q = static_cast<int>(item & 3);
+  if (tile >= min(a.tiles, static_cast<int64_t>(a.tile_rec[0]))) return;  // the batch's tiles
+  const int32_t* rec = a.tile_rec + (tile + 1) * kTileRecInts;
+  const int c0 = rec[0], c1 = rec[1], head = rec[2], qbeg = rec[3], ql = rec[4], prefix = rec[5];
+  const int qt = rec[6], nvis = rec[7];
+  const int64_t total = static_cast<int64_t>(static_cast<uint32_t>(rec[8])) |
+                        (static_cast<int64_t>(rec[9]) << 32);
+  const int r = q * 32 + lane;
+  const int qrow = qt * 128 + r;
+  // Every field is checked against this call's sizes: a prefill that gave up
+  // (MM3IDX_DEV_TIMEOUT) may leave a record of an earlier call, which must
+  // not send a read or write out of bounds.
+  if (c0 < 0 || c1 < c0 || c1 >= a.grid || head < 0 || head >= a.heads || qbeg < 0 ||
+      qrow >= ql || qbeg + qrow >= a.total_q || total <= 0)
+    return;
+  const int pos = prefix + qrow;
+  const int c = pos >= 0 ? pos >> 7 : -1;
+  int32_t* out = a.ids + head * a.i_head + static_cast<int64_t>(qbeg + qrow) * a.i_row;
+  if (nvis <= a.topk) {
+    for (int t = 0; t < a.topk; ++t) out[t] = t <= c ? t : -1;
+    return;
+  }
+  RegList<TK> m;
+  m.clear();
+  for (int cj = c0; cj <= c1; ++cj) {
+    if (!has_units(cj, total, a.grid)) continue;
+    uint64_t l0[TK], l1[TK];
+    const ulonglong2* s0 = reinterpret_cast<const ulonglong2*>(
+        a.partials + ((2 * (static_cast<int64_t>(cj) + tile)) * 128 + r) * TK);
+    const ulonglong2* s1 = s0 + 128 * TK / 2;
+#pragma unroll
+    for (int j = 0; j < TK / 2; ++j) {
+      const ulonglong2 x = __ldcg(s0 + j), y = __ldcg(s1 + j);
+      l0[2 * j] = x.x;
+      l0[2 * j + 1] = x.y;
+      l1[2 * j] = y.x;
+      l1[2 * j + 1] = y.y;
+    }
+    m.merge_sorted(l0);
+    m.merge_sorted(l1);
+  }
+  write_row_lane<TK>(m.v, c, a.init_blocks, a.local_blocks, a.topk, out);
+}
+
+template <bool kSelect>
+cudaError_t launch_prefill_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
+                     int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kSelect>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<kSelect><<<grid, kThreads, kSmem, s>>>(qmap, kmap, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s) {
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  prefill_kernel<<<grid, kThreads, kSmem, s>>>(qmap, kmap, a);
-  return cudaGetLastError();
+  return a.partials != nullptr ? launch_prefill_t<true>(qmap, kmap, a, grid, s)
+                               : launch_prefill_t<false>(qmap, kmap, a, grid, s);
+}
+
+cudaError_t launch_prefill_merge(const PrefillMergeArgs& a, cudaStream_t s) {
+  const int64_t warps = a.tiles * 4;
+  if (warps == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + kMergeWarps - 1) / kMergeWarps));
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_merge_kernel, a);
 }
 
 }  // namespace mm3idx

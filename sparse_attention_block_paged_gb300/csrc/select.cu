@@ -241,6 +241,43 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
 
 }  // namespace
 
+// Blocks past each row's own block hold -inf, up to `width` (the score call's
+// output contract): one warp per (head, row), lanes on consecutive blocks.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) fill_invisible_kernel(const SelectArgs a,
+                                                                             int width) {
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t rows = a.total_q;
+  const int64_t work = rows * a.heads;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib; w < work; w += nwarps) {
+    const int h = static_cast<int>(w / rows);
+    const int64_t row = w - static_cast<int64_t>(h) * rows;
+    int i, j, ql = a.query_len;
+    bool row_ok = true;
+    if (a.cu != nullptr) {
+      row_ok = ragged_row(a, row, i, j, ql);
+    } else {
+      i = static_cast<int>(row / a.query_len);
+      j = static_cast<int>(row - static_cast<int64_t>(i) * a.query_len);
+    }
+    const int seq = min(max(__ldg(a.seq_lens + i), 0), a.max_seq_len);
+    const int pos = seq - ql + j;
+    const int c = row_ok && pos >= 0 ? (pos >> 7) : -1;
+    float* srow = const_cast<float*>(a.score) + h * a.s_head + row * a.s_row;
+    for (int b = c + 1 + lane; b < width; b += 32) srow[b] = -INFINITY;
+  }
+}
+
+cudaError_t launch_fill_invisible(const SelectArgs& a, int width, int num_sms, cudaStream_t s) {
+  const int64_t work = static_cast<int64_t>(a.total_q) * a.heads;
+  int64_t blocks = (work + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) return cudaSuccess;
+  fill_invisible_kernel<<<static_cast<int>(blocks), kWarpsPerBlock * 32, 0, s>>>(a, width);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s) {
   const int64_t work = static_cast<int64_t>(a.total_q) * a.heads;
   int64_t blocks = (work + kWarpsPerBlock - 1) / kWarpsPerBlock;

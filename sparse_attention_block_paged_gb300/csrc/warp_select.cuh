@@ -1,5 +1,5 @@
-// warp_select.cuh -- the forced-block rule shared by the selector kernel and
-// the decode kernel's row writers.
+// warp_select.cuh -- the forced-block rule, the per-thread candidate list
+// and the row writer shared by the selector, decode and prefill kernels.
 //
 // Selection rule (vLLM MiniMax-M3 "index_topk" page, minimax_m3_index_decode
 // and minimax_m3_index_topk; "indexer_cp_exchange" module docstring): for a
@@ -24,5 +24,119 @@ struct Forced {
     nf = f_lo + (c + 1 - l_lo);
   }
 };
+
+constexpr int kListLanes = 32;  // rows of a shared-memory hand-over table
+
+// A row's best candidate keys, descending, held in registers (0 = empty).
+// Insertion is a branchless compare-and-swap cascade with static indices.
+template <int TK>
+struct RegList {
+  uint64_t v[TK];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) v[k] = 0ull;
+  }
+  // Keys at or below this cannot enter.
+  __device__ __forceinline__ uint64_t floor() const { return v[TK - 1]; }
+  __device__ __forceinline__ void insert(uint64_t key) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) {
+      const uint64_t cur = v[k];
+      const bool gt = key > cur;
+      v[k] = gt ? key : cur;
+      key = gt ? cur : key;
+    }
+  }
+  __device__ __forceinline__ void offer(uint64_t key) {
+    if (key > floor()) insert(key);
+  }
+  // The same insertion with a short dependency chain: in a list sorted
+  // descending, "v[k] > key" holds exactly for k below the key's place, so
+  // each new slot follows from the old slot, its predecessor and the key
+  // alone (about four dependent steps instead of TK).
+  __device__ __forceinline__ void offer_shallow(uint64_t key) {
+    if (key <= floor()) return;
+    bool above_prev = true;  // v[k-1] > key, with v[-1] taken as above every key
+    uint64_t prev = 0ull;
+#pragma unroll
+    for (int k = 0; k < TK; ++k) {
+      const uint64_t cur = v[k];
+      const bool above = cur > key;
+      v[k] = above ? cur : (above_prev ? key : prev);
+      above_prev = above;
+      prev = cur;
+    }
+  }
+  // Replace the list by the best TK keys of itself and `b` (b sorted
+  // descending): the elementwise max of the list and reversed b holds exactly
+  // those keys as a bitonic sequence, which a bitonic sort orders again.
+  __device__ __forceinline__ void merge_sorted(const uint64_t (&b)[TK]) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) v[k] = v[k] > b[TK - 1 - k] ? v[k] : b[TK - 1 - k];
+#pragma unroll
+    for (int half = TK / 2; half > 0; half >>= 1) {
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        if ((k & half) == 0) {
+          const uint64_t x = v[k], y = v[k + half];
+          v[k] = x > y ? x : y;
+          v[k + half] = x > y ? y : x;
+        }
+      }
+    }
+  }
+  // Row-major store to a [k][kListLanes] shared-memory table at column n.
+  __device__ __forceinline__ void store_cols(uint64_t* t, int n) const {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) t[k * kListLanes + n] = v[k];
+  }
+};
+
+// One thread writes one output row from its candidate list (keys sorted
+// descending, 0 = none): forced blocks [0, f_lo) and [l_lo, c] around the best
+// topk - |forced| picks, picks in ascending id order, then -1.
+template <int TK>
+__device__ __forceinline__ void write_row_lane(const uint64_t (&v)[TK], int c, int init_blocks,
+                                               int local_blocks, int topk, int32_t* out) {
+  if (c < 0) {
+    for (int k = 0; k < topk; ++k) out[k] = -1;
+    return;
+  }
+  const Forced F(c, init_blocks, local_blocks);
+  const int m = topk - F.nf;
+  int id[TK];
+  int npick = 0;
+#pragma unroll
+  for (int k = 0; k < TK; ++k) {
+    const bool take = k < m && v[k] != 0ull;
+    id[k] = take ? key_block(v[k]) : 0x7fffffff;
+    npick += take;
+  }
+  // Bitonic sort of the ids, ascending (absent picks sort to the end).
+#pragma unroll
+  for (int size = 2; size <= TK; size <<= 1) {
+#pragma unroll
+    for (int stride = size / 2; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        const int l = k ^ stride;
+        if (l > k) {
+          const bool up = (k & size) == 0;
+          const int x = id[k], y = id[l];
+          id[k] = (x < y) == up ? x : y;
+          id[l] = (x < y) == up ? y : x;
+        }
+      }
+    }
+  }
+  int o = 0;
+  for (int b = 0; b < F.f_lo; ++b) out[o++] = b;
+#pragma unroll
+  for (int k = 0; k < TK; ++k)
+    if (k < npick) out[o + k] = id[k];
+  o += npick;
+  for (int b = F.l_lo; b <= c; ++b) out[o++] = b;
+  for (; o < topk; ++o) out[o] = -1;
+}
 
 }  // namespace mm3idx

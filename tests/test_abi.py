@@ -168,9 +168,9 @@ def test_nvfp4_prefill_validation_and_workspace():
     p = problem(index_scales=FAKE, num_reqs=0)
     assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == 0
     p = problem(index_scales=FAKE)
-    assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1000, None) == -9
+    assert f(ctypes.byref(p), 32, 1, 1, FAKE, 1000, 32, FAKE, 1000, None) == -9
     n = ctypes.c_size_t(0)
-    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL_NVFP4, 2, 3, 300, 1000, 16,
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL_NVFP4, 2, 3, 300, 1000, 32,
                                          ctypes.byref(n)) == 0
     scores = 2 * 3 * 300 * 8 * 4                     # as OP_PREFILL, 256-byte multiple here
     slots = 3 * 8                                    # requests x cdiv(1000, 128)
@@ -185,7 +185,7 @@ def test_ragged_validation():
     assert f(ctypes.byref(p), FAKE + 2, 8, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
     assert f(ctypes.byref(p), FAKE, -1, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == -1
     assert f(ctypes.byref(p), FAKE, 0, 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == 0
-    assert f(ctypes.byref(p), FAKE, 8, 4, 1, 1, FAKE, 1000, 4, FAKE, 100, None) == -9
+    assert f(ctypes.byref(p), FAKE, 8, 32, 1, 1, FAKE, 1000, 32, FAKE, 100, None) == -9
     g = mm.lib.mm3idx_score_ragged
     assert g(ctypes.byref(p), FAKE, 9, FAKE, 1000, 8, None) == -1
     assert g(ctypes.byref(p), FAKE, 0, FAKE, 1000, 8, None) == 0
@@ -205,8 +205,10 @@ def test_workspace_query_validation():
     n = ctypes.c_size_t(0)
     assert mm.lib.mm3idx_workspace_bytes(9, 1, 1, 1, 128, 4, ctypes.byref(n)) == -1
     assert mm.lib.mm3idx_workspace_bytes(mm.OP_DECODE, 1, 1, 1, 128, 40, ctypes.byref(n)) == -7
-    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 16, ctypes.byref(n)) == 0
+    # topk > 16: the two-kernel prefill's score scratch (no device needed)
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 32, ctypes.byref(n)) == 0
     assert n.value == 2 * 3 * 300 * 8 * 4      # [heads, rows, roundup(cdiv(1000,128), 4)] fp32
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 33, ctypes.byref(n)) == -7
 
 
 def test_binding_layout_errors():

@@ -72,7 +72,8 @@ def test_nvfp4_dequantised_pages_bit_exact(mm):
     """Every (code, scale byte) pair except the two NaN scales, read back from
     the workspace's bf16 copy and compared with the oracle's value."""
     import torch
-    wl = W.random_case(8, num_reqs=1, query_len=256, heads=1, topk=4, init_blocks=1,
+    # topk 32: the two-kernel prefill, whose workspace starts with the scores
+    wl = W.random_case(8, num_reqs=1, query_len=256, heads=1, topk=32, init_blocks=1,
                        local_blocks=1, min_len=256, max_len=256, kv_format="nvfp4")
     pages = wl.block_table[0, :2]
     scale_bytes = np.array([b if b not in (0x7F, 0xFF) else 0 for b in range(256)], dtype=np.uint8)
@@ -82,8 +83,8 @@ def test_nvfp4_dequantised_pages_bit_exact(mm):
         nib = np.tile(np.arange(16, dtype=np.uint8), 128 * 8).reshape(128, 128)
         nib = np.roll(nib, k, axis=1)
         wl.codes[pg] = nib[:, 0::2] | (nib[:, 1::2] << 4)
-    ws = torch.zeros(mm.workspace_bytes(mm.OP_PREFILL_NVFP4, 1, 1, 256, 256, 4), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.zeros(mm.workspace_bytes(mm.OP_PREFILL_NVFP4, 1, 1, 256, 256, 32),
+                     dtype=torch.uint8, device="cuda")
     run_prefill_nvfp4(mm, wl, workspace=ws)
     assert mm.get_device_error() == 0
     width = 2

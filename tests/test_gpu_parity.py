@@ -148,6 +148,25 @@ def test_prefill_matches_oracle(mm, case):
     assert mm.get_device_error() == 0
 
 
+@pytest.mark.parametrize("topk,init,local", [(16, 1, 2), (4, 0, 0), (9, 3, 2)])
+def test_fused_prefill_selection_equals_two_kernels(mm, topk, init, local):
+    """topk <= 16: the prefill kernel selects as it scores.  Its ids must be
+    those of the score kernel followed by the selector, bit for bit (the
+    same fp32 scores and the same keys)."""
+    wl = W.random_case(70 + topk, num_reqs=3, query_len=700, heads=2, topk=topk,
+                       init_blocks=init, local_blocks=local, min_len=700, max_len=5000)
+    d = to_device(wl)
+    fused = run_prefill(mm, wl)
+    sc = mm.score(d["q"], d["cache"], d["table"], d["lens"], query_len=wl.query_len,
+                  max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale)
+    two = mm.topk(sc, d["lens"], query_len=wl.query_len, max_seq_len=wl.max_seq_len,
+                  topk=topk, init_blocks=init, local_blocks=local).cpu().numpy()
+    np.testing.assert_array_equal(fused, two)
+    s, want = oracle.problem(wl)
+    check_ids(fused, want, s, wl, where=f"fused topk{topk}")
+    assert mm.get_device_error() == 0
+
+
 def test_topk_selector_bit_exact_on_same_scores(mm):
     """Given the same fp32 scores, selection must agree bit for bit."""
     import torch
