@@ -604,13 +604,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the tile (one list per team) are merged and the rows written.  Launched
 // as a programmatic dependent of the prefill kernel, whose completion it
 // waits for on the GPU.
-constexpr int kMergeWarps = 2;
+constexpr int kMergeWarps = 8;
 
 __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const PrefillMergeArgs a) {
+  // Each warp builds its 32 rows in shared memory (lane = row) and writes
+  // them out row by row, so the stores are contiguous.
+  __shared__ int32_t s_rows[kMergeWarps][32][kPrefillSelectTK];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int TK = kPrefillSelectTK;
-  const int lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + wib;
   const int64_t tile = item >> 2;
   const int q = static_cast<int>(item & 3);
   if (tile >= min(a.tiles, static_cast<int64_t>(a.tile_rec[0]))) return;  // the batch's tiles
@@ -619,41 +622,49 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
   const int qt = rec[6], nvis = rec[7];
   const int64_t total = static_cast<int64_t>(static_cast<uint32_t>(rec[8])) |
                         (static_cast<int64_t>(rec[9]) << 32);
-  const int r = q * 32 + lane;
-  const int qrow = qt * 128 + r;
+  const int row0 = qt * 128 + q * 32;   // the warp's first row in the request
   // Every field is checked against this call's sizes: a prefill that gave up
   // (MM3IDX_DEV_TIMEOUT) may leave a record of an earlier call, which must
   // not send a read or write out of bounds.
   if (c0 < 0 || c1 < c0 || c1 >= a.grid || head < 0 || head >= a.heads || qbeg < 0 ||
-      qrow >= ql || qbeg + qrow >= a.total_q || total <= 0)
+      row0 >= ql || total <= 0)
     return;
-  const int pos = prefix + qrow;
+  const int nrows = min(min(32, ql - row0), a.total_q - (qbeg + row0));
+  if (nrows <= 0) return;
+  const int r = q * 32 + lane;
+  const int pos = prefix + row0 + lane;
   const int c = pos >= 0 ? pos >> 7 : -1;
-  int32_t* out = a.ids + head * a.i_head + static_cast<int64_t>(qbeg + qrow) * a.i_row;
+  int32_t* srow = s_rows[wib][lane];
   if (nvis <= a.topk) {
-    for (int t = 0; t < a.topk; ++t) out[t] = t <= c ? t : -1;
-    return;
-  }
-  RegList<TK> m;
-  m.clear();
-  for (int cj = c0; cj <= c1; ++cj) {
-    if (!has_units(cj, total, a.grid)) continue;
-    uint64_t l0[TK], l1[TK];
-    const ulonglong2* s0 = reinterpret_cast<const ulonglong2*>(
-        a.partials + ((2 * (static_cast<int64_t>(cj) + tile)) * 128 + r) * TK);
-    const ulonglong2* s1 = s0 + 128 * TK / 2;
+    for (int t = 0; t < a.topk; ++t) srow[t] = t <= c ? t : -1;
+  } else {
+    RegList<TK> m;
+    m.clear();
+    for (int cj = c0; cj <= c1; ++cj) {
+      if (!has_units(cj, total, a.grid)) continue;
+      uint64_t l0[TK], l1[TK];
+      const ulonglong2* s0 = reinterpret_cast<const ulonglong2*>(
+          a.partials + ((2 * (static_cast<int64_t>(cj) + tile)) * 128 + r) * TK);
+      const ulonglong2* s1 = s0 + 128 * TK / 2;
 #pragma unroll
-    for (int j = 0; j < TK / 2; ++j) {
-      const ulonglong2 x = __ldcg(s0 + j), y = __ldcg(s1 + j);
-      l0[2 * j] = x.x;
-      l0[2 * j + 1] = x.y;
-      l1[2 * j] = y.x;
-      l1[2 * j + 1] = y.y;
+      for (int j = 0; j < TK / 2; ++j) {
+        const ulonglong2 x = __ldcg(s0 + j), y = __ldcg(s1 + j);
+        l0[2 * j] = x.x;
+        l0[2 * j + 1] = x.y;
+        l1[2 * j] = y.x;
+        l1[2 * j + 1] = y.y;
+      }
+      m.merge_sorted(l0);
+      m.merge_sorted(l1);
     }
-    m.merge_sorted(l0);
-    m.merge_sorted(l1);
+    write_row_lane<TK>(m.v, c, a.init_blocks, a.local_blocks, a.topk, srow);
   }
-  write_row_lane<TK>(m.v, c, a.init_blocks, a.local_blocks, a.topk, out);
+  __syncwarp();
+  int32_t* out = a.ids + head * a.i_head + static_cast<int64_t>(qbeg + row0) * a.i_row;
+  for (int idx = lane; idx < nrows * a.topk; idx += 32) {
+    const int rr = idx / a.topk, k = idx - rr * a.topk;
+    out[rr * a.i_row + k] = s_rows[wib][rr][k];
+  }
 }
 
 template <bool kSelect>
