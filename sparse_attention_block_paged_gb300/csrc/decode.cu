@@ -402,6 +402,18 @@ __global__ void __launch_bounds__(Cfg<FP4, MQ, TK>::kThreads, 1)
   if (warp == kProdWarp) {
     if (!FP4 && lane == 0) prefetch_tensormap(&kmap);
     partition(a, misc, lane);
+  } else if (warp == kMergeWarp) {
+    // While the producer reads the lengths: pull the block table and the
+    // queries into L2, one 128-byte line per lane of this warp in every CTA
+    // (all of both for the named batches), so that the first table and
+    // query reads after the partition do not go to HBM.
+    const int64_t line = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * 128;
+    const int64_t tbytes = static_cast<int64_t>(a.num_reqs) * a.table_stride * 4;
+    const int64_t qbytes = static_cast<int64_t>(a.num_reqs) * a.query_len * a.q_tok * 2;
+    if (line < tbytes)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(a.table) + line));
+    if (line < qbytes)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(a.q) + line));
   }
   tc_fence_before();
   __syncthreads();
