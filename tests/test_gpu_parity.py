@@ -292,3 +292,41 @@ def test_full_size_prefill_sampled(mm):
         from helpers import check_ids_row
         check_ids_row(got[0, r], want, s, c, wl.topk, wl.init_blocks, wl.local_blocks,
                       where=f"prefill row {r}")
+
+
+def test_fused_prefill_workspace_reuse_and_graph_replay(mm):
+    """topk <= 16 keeps tile records and candidate lists in the workspace.
+    A larger batch, then a smaller one, then a graph replay of the smaller
+    one on the same workspace: each must match the oracle (records and
+    lists of the earlier call must not leak into the later one)."""
+    import torch
+    big = W.random_case(81, num_reqs=3, query_len=900, heads=2, topk=16, init_blocks=1,
+                        local_blocks=2, min_len=900, max_len=6000, max_seq_len=6000)
+    small = W.random_case(82, num_reqs=2, query_len=300, heads=2, topk=16, init_blocks=1,
+                          local_blocks=2, min_len=300, max_len=2000, max_seq_len=6000)
+    ws = torch.full((mm.workspace_bytes(mm.OP_PREFILL, 2, 3, 900, 6000, 16),), 0xA5,
+                    dtype=torch.uint8, device="cuda")
+    kw = lambda wl: dict(query_len=wl.query_len, max_seq_len=6000, topk=16,  # noqa: E731
+                         init_blocks=1, local_blocks=2, sm_scale=wl.sm_scale, workspace=ws)
+    for wl in (big, small):
+        d = to_device(wl)
+        got = mm.prefill(d["q"], d["cache"], d["table"], d["lens"], **kw(wl)).cpu().numpy()
+        s, want = oracle.problem(wl)
+        check_ids(got, want, s, wl, where=f"reuse {wl.name}")
+    d = to_device(small)
+    out = torch.full((2, small.rows, 16), -9, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        mm.prefill(d["q"], d["cache"], d["table"], d["lens"], **kw(small), out=out, stream=stream)
+        torch.cuda.synchronize()
+        out.fill_(-9)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            mm.prefill(d["q"], d["cache"], d["table"], d["lens"], **kw(small), out=out,
+                       stream=torch.cuda.current_stream())
+        g.replay()
+    torch.cuda.synchronize()
+    s, want = oracle.problem(small)
+    check_ids(out.cpu().numpy(), want, s, small, where="graph fused prefill")
+    assert mm.get_device_error() == 0
