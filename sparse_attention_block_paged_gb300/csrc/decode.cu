@@ -104,6 +104,19 @@ __device__ __forceinline__ int req_blocks(const DecodeArgs& a, int i) {
   return (req_len(a, i) + kBlock - 1) / kBlock;
 }
 
+// A request with blocks occupies kSegCost + blocks positions of the list the
+// CTAs share out: each request a CTA serves costs it a query tile and, when
+// split, a cross-CTA merge, which the blocks alone do not count.  The extra
+// positions come first and hold no work.  Measured on one GB300 over 0-20:
+// 6 gave high-batch 171 -> 163 us and kept spec-decode at its faster 60.6 us;
+// larger values lose again.
+constexpr int kSegCost = 6;
+
+__device__ __forceinline__ int req_slots(const DecodeArgs& a, int i) {
+  const int n = req_blocks(a, i);
+  return n > 0 ? n + kSegCost : 0;
+}
+
 // Walks this CTA's share [lo, hi) of the flattened (request, block) list and
 // yields one segment (request, blocks [b0, b1)) at a time.  The two boundary
 // segments come first -- the share's first request (whose earlier blocks
@@ -117,17 +130,20 @@ struct Walker {
   long long lo, hi;
   int stage = 0, i = 0;   // 0: first, 1: last, 2: interior requests
   long long P = 0;
+  // Request r's positions start at pr; its blocks at pr + kSegCost, which
+  // is what preq reports.
   __device__ bool emit(const DecodeArgs& a, int r, long long pr, int& req, int& b0, int& b1,
                        int& nb, long long& preq) const {
     const int n = req_blocks(a, r);
-    const long long s = pr > lo ? pr : lo;
-    const long long e = (pr + n) < hi ? (pr + n) : hi;
-    if (e <= s) return false;
+    const long long pb = pr + kSegCost;
+    const long long s = pb > lo ? pb : lo;
+    const long long e = (pb + n) < hi ? (pb + n) : hi;
+    if (n == 0 || e <= s) return false;
     req = r;
-    preq = pr;
+    preq = pb;
     nb = n;
-    b0 = static_cast<int>(s - pr);
-    b1 = static_cast<int>(e - pr);
+    b0 = static_cast<int>(s - pb);
+    b1 = static_cast<int>(e - pb);
     return true;
   }
   __device__ bool next(const DecodeArgs& a, int& req, int& b0, int& b1, int& nb,
@@ -140,13 +156,13 @@ struct Walker {
     if (stage == 1) {
       stage = 2;
       i = i0 + 1;
-      P = p0 + req_blocks(a, i0);
+      P = p0 + req_slots(a, i0);
       if (il != i0 && emit(a, il, pl, req, b0, b1, nb, preq)) return true;
     }
     while (i < il) {
       const int r = i;
       const long long pr = P;
-      P += req_blocks(a, r);
+      P += req_slots(a, r);
       ++i;
       if (emit(a, r, pr, req, b0, b1, nb, preq)) return true;
     }
@@ -181,7 +197,8 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
         if (raw[u] < a.query_len) bits |= MM3IDX_DEV_SEQ_TOO_SHORT;
         if (bits) atomicOr(a.status, bits);
       }
-      total += (min(max(raw[u], 0), a.max_seq_len) + kBlock - 1) / kBlock;
+      const int nbu = (min(max(raw[u], 0), a.max_seq_len) + kBlock - 1) / kBlock;
+      total += nbu > 0 ? nbu + kSegCost : 0;
     }
   }
 #pragma unroll
@@ -194,7 +211,7 @@ __device__ void partition(const DecodeArgs& a, Misc* m, int lane) {
   bool need0 = true;
   for (int b = 0; b < a.num_reqs && hi > lo; b += 32) {
     const int i = b + lane;
-    const long long nb = i < a.num_reqs ? req_blocks(a, i) : 0;
+    const long long nb = i < a.num_reqs ? req_slots(a, i) : 0;
     long long incl = nb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
