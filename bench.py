@@ -244,26 +244,38 @@ def bench_graph(mm, torch, wl, d, kw, steps, flush, stream):
 
 
 def bench_e2e(mm, torch, wl, d, out, ws, kw, steps, warmup, flush, stream):
-    """Same decode through the public API with host buffers: H2D of the step's
-    queries, block table and lengths from pinned memory, the call, D2H of ids."""
-    q_h = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    t_h = torch.from_numpy(wl.block_table).pin_memory()
-    l_h = torch.from_numpy(wl.seq_lens).pin_memory()
+    """Same decode through the public API with host buffers: one H2D copy of
+    the step's queries, block table and lengths (packed in one pinned
+    buffer), the call on device views of them, and a D2H copy of the ids."""
+    parts = [wl.q.view(np.uint8).reshape(-1), wl.block_table.view(np.uint8).reshape(-1),
+             wl.seq_lens.view(np.uint8).reshape(-1)]
+    offs, n = [], 0
+    for p in parts:
+        offs.append(n)
+        n += (p.nbytes + 255) // 256 * 256
+    host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    for p, o in zip(parts, offs):
+        host[o:o + p.nbytes] = torch.from_numpy(p)
+    dev = torch.empty(n, dtype=torch.uint8, device=d["q"].device)
+    q = dev[offs[0]:offs[0] + parts[0].nbytes].view(torch.bfloat16).view(d["q"].shape)
+    table = dev[offs[1]:offs[1] + parts[1].nbytes].view(torch.int32).view(d["table"].shape)
+    lens = dev[offs[2]:offs[2] + parts[2].nbytes].view(torch.int32).view(d["lens"].shape)
     o_h = torch.empty(out.shape, dtype=torch.int32).pin_memory()
 
     def fn():
-        d["q"].copy_(q_h, non_blocking=True)
-        d["table"].copy_(t_h, non_blocking=True)
-        d["lens"].copy_(l_h, non_blocking=True)
-        mm.decode(d["q"], d["cache"], d["table"], d["lens"], **kw)
+        dev.copy_(host, non_blocking=True)
+        mm.decode(q, d["cache"], table, lens, **kw)
         o_h.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         ms = timed_steps(torch, fn, steps, warmup, flush, stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(o_h.numpy(), out.cpu().numpy())
     t = statistics.mean(ms) * 1e-3
     return dict(value=wl.rows / t, unit="rows/s",
-                h2d_bytes_per_step=int(q_h.nbytes + t_h.nbytes + l_h.nbytes),
-                d2h_bytes_per_step=int(o_h.nbytes))
+                h2d_bytes_per_step=int(sum(p.nbytes for p in parts)),
+                d2h_bytes_per_step=int(o_h.nbytes),
+                copies="one H2D of the packed inputs, one D2H of the ids")
 
 
 def bench_sparse_table(mm, torch, wl, steps, flush, stream):
