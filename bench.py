@@ -452,6 +452,22 @@ def cpu_baseline_all_cores(wl, seconds):
                        f"one request per task on {cores} threads, {el:.1f} s")
 
 
+def max_over_ranks(t_ms, device):
+    """The slowest rank's time (ms); the local time when running alone."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t_ms
+    tt = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(rows_per_rank, world, t_ms):
+    """Whole-job throughput: every rank's rows over the slowest rank's time."""
+    return world * rows_per_rank / (t_ms * 1e-3)
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -497,11 +513,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    t = res["ms_per_step"]
-    if world > 1:
-        tt = torch.tensor([t], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(res["ms_per_step"], dev)
     e2e = bench_e2e(mm, torch, wl, d, out, ws, kw, args.steps, max(args.warmup, 3), flush, stream)
     graph = bench_graph(mm, torch, wl, d, kw, args.steps, flush, stream)
     extra = {}
@@ -539,7 +551,7 @@ def run_ours(args):
         return
     line = {
         "metric": METRIC,
-        "value": world * wl.rows / (t * 1e-3),
+        "value": job_value(wl.rows, world, t),
         "unit": "rows/s",
         "n_gpus": world,
         "steps": args.steps,
