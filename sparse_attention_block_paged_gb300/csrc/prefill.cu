@@ -640,8 +640,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
   } else {
     RegList<TK> m;
     m.clear();
+    // With at least as many units as CTAs every share holds some (no check).
+    const bool dense = total >= a.grid;
     for (int cj = c0; cj <= c1; ++cj) {
-      if (!has_units(cj, total, a.grid)) continue;
+      if (!dense && !has_units(cj, total, a.grid)) continue;
       uint64_t l0[TK], l1[TK];
       const ulonglong2* s0 = reinterpret_cast<const ulonglong2*>(
           a.partials + ((2 * (static_cast<int64_t>(cj) + tile)) * 128 + r) * TK);

@@ -249,13 +249,25 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fill_invisible_kernel(con
   const int64_t rows = a.total_q;
   const int64_t work = rows * a.heads;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  const bool small = work < (int64_t{1} << 31);  // 32-bit index arithmetic
   for (int64_t w = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib; w < work; w += nwarps) {
-    const int h = static_cast<int>(w / rows);
-    const int64_t row = w - static_cast<int64_t>(h) * rows;
-    int i, j, ql = a.query_len;
+    int h, i, j, ql = a.query_len;
+    int64_t row;
     bool row_ok = true;
+    if (small) {
+      const uint32_t w32 = static_cast<uint32_t>(w), rows32 = static_cast<uint32_t>(rows);
+      h = static_cast<int>(w32 / rows32);
+      row = w32 - static_cast<uint32_t>(h) * rows32;
+    } else {
+      h = static_cast<int>(w / rows);
+      row = w - static_cast<int64_t>(h) * rows;
+    }
     if (a.cu != nullptr) {
       row_ok = ragged_row(a, row, i, j, ql);
+    } else if (small) {
+      const uint32_t r32 = static_cast<uint32_t>(row), ql32 = static_cast<uint32_t>(a.query_len);
+      i = static_cast<int>(r32 / ql32);
+      j = static_cast<int>(r32 - static_cast<uint32_t>(i) * ql32);
     } else {
       i = static_cast<int>(row / a.query_len);
       j = static_cast<int>(row - static_cast<int64_t>(i) * a.query_len);
@@ -269,9 +281,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fill_invisible_kernel(con
 }
 
 cudaError_t launch_fill_invisible(const SelectArgs& a, int width, int num_sms, cudaStream_t s) {
+  // A warp per row, all rows at once (the rows are independent and short).
   const int64_t work = static_cast<int64_t>(a.total_q) * a.heads;
   int64_t blocks = (work + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 512;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) return cudaSuccess;
   fill_invisible_kernel<<<static_cast<int>(blocks), kWarpsPerBlock * 32, 0, s>>>(a, width);
