@@ -455,6 +455,25 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                               peak_source=pk["source"] + " cuBLAS bf16 burst"))
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl, seconds):
     """The oracle as it stands, single-threaded, on whole batches of the
     workload until `seconds` of CPU time are spent (at least one request)."""
@@ -470,7 +489,8 @@ def cpu_baseline(wl, seconds):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return dict(value=rows / el, unit="rows/s", cores=1, kind="oracle",
+    return dict(value=rows / el, unit="rows/s", cores=1, kind="oracle", cpu=cpu_model(),
+                host_cores=os.cpu_count(),
                 sample=f"{i} requests ({rows} rows) of the {wl.name} workload, "
                        f"request by request, {el:.1f} s on one host core")
 
@@ -502,7 +522,7 @@ def cpu_baseline_all_cores(wl, seconds):
             el = time.perf_counter() - t0
             if el >= seconds:
                 break
-    return dict(value=rows / el, unit="rows/s", cores=cores, kind="oracle",
+    return dict(value=rows / el, unit="rows/s", cores=cores, kind="oracle", cpu=cpu_model(),
                 identical_to_single_core=same,
                 sample=f"{done} requests ({rows} rows) of the {wl.name} workload, "
                        f"one request per task on {cores} threads, {el:.1f} s")
