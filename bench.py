@@ -339,7 +339,7 @@ def bench_sparse_table(mm, torch, wl, steps, flush, stream):
     stride 4) against the plain decode, both timed the same way."""
     dev = torch.device("cuda", torch.cuda.current_device())
     d = device_inputs(wl, torch, dev)
-    attn = torch.from_numpy(W_attention_table(wl)).to(dev)
+    attn = torch.from_numpy(_attention_table(wl)).to(dev)
     st = torch.empty((wl.rows, wl.topk * 2), dtype=torch.int32, device=dev)
     ctx = torch.empty((wl.rows,), dtype=torch.int32, device=dev)
     out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
@@ -360,7 +360,7 @@ def bench_sparse_table(mm, torch, wl, steps, flush, stream):
                 pages_per_block=2, block_page_stride=4, workload=wl.name + " + sparse page table")
 
 
-def W_attention_table(wl):
+def _attention_table(wl):
     import workloads as W
     return W.attention_block_table(wl, 1)
 
