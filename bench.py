@@ -411,8 +411,16 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                                    stream=stream)
             with torch.cuda.stream(stream):
                 ms_sc = timed_steps(torch, scf, steps, warmup, flush, stream)
+                # the standalone selector (mm3idx_topk; also the path for
+                # topk > 16) on the same scores
+                self_sel = lambda: mm.topk(sc_out, d["lens"], query_len=wl.query_len,  # noqa: E731
+                                           max_seq_len=wl.max_seq_len, topk=wl.topk,
+                                           init_blocks=wl.init_blocks,
+                                           local_blocks=wl.local_blocks, out=out, stream=stream)
+                ms_sel = timed_steps(torch, self_sel, steps, warmup, flush, stream)
             t_sc = statistics.mean(ms_sc) * 1e-3
             res["scorer_ms"] = t_sc * 1e3
+            res["selector_alone_ms"] = statistics.mean(ms_sel)
             del sc_out
         t_roof = t_sc if t_sc is not None else t_all
         res["roofline"] = dict(bound="tensor", achieved=fl / t_roof / 1e12,
