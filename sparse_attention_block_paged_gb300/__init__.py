@@ -255,7 +255,15 @@ def _ids_out(out, heads, rows, topk, device):
     _need(out.dtype == torch.int32 and out.ndim == 3 and out.shape[0] == heads
           and out.shape[1] >= rows and out.shape[2] == topk and out.stride(2) == 1,
           "out must be int32 [heads, >=rows, topk] with unit inner stride")
+    _need(out.device == torch.device(device), "out must be on the inputs' GPU")
     return out
+
+
+def _on_gpu(ref, *tensors):
+    """Every tensor on ref's device, and that device a GPU (the library takes
+    the addresses as device addresses)."""
+    _need(ref.device.type == "cuda" and all(t.device == ref.device for t in tensors),
+          "all inputs must be on the same GPU")
 
 
 def topk(score_t, seq_lens, *, query_len, max_seq_len, topk, init_blocks, local_blocks,
@@ -263,6 +271,7 @@ def topk(score_t, seq_lens, *, query_len, max_seq_len, topk, init_blocks, local_
     """int32 [heads, rows, topk] ids (ascending, -1 pad) from a score tensor."""
     _need(score_t.dtype == torch.float32 and score_t.ndim == 3 and score_t.stride(2) == 1,
           "score must be fp32 [heads, rows, blocks] with unit inner stride")
+    _on_gpu(score_t, seq_lens)
     heads, rows = score_t.shape[0], seq_lens.shape[0] * query_len
     _need(score_t.shape[1] >= rows and score_t.shape[2] >= _cdiv(max_seq_len, 128),
           "score narrower than the rows or cdiv(max_seq_len,128)")
@@ -411,6 +420,7 @@ def topk_ragged(score_t, seq_lens, cu_seqlens_q, *, max_query_len, max_seq_len, 
     _need(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.ndim == 1
           and cu_seqlens_q.shape[0] == seq_lens.shape[0] + 1 and cu_seqlens_q.is_contiguous(),
           "cu_seqlens_q must be contiguous int32 [num_reqs + 1]")
+    _on_gpu(score_t, seq_lens, cu_seqlens_q)
     heads, total_q = score_t.shape[0], score_t.shape[1]
     out = _ids_out(out, heads, total_q, topk, score_t.device)
     _check(lib.mm3idx_topk_ragged(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,

@@ -229,6 +229,40 @@ def test_binding_layout_errors():
                   local_blocks=1, sm_scale=0.1)
 
 
+def test_binding_rejects_host_tensors_and_bad_shapes():
+    """Argument checks that run before any CUDA call: host tensors never reach
+    the library, whose pointers are device pointers."""
+    import torch
+    score = torch.zeros((1, 8, 8), dtype=torch.float32)
+    lens = torch.full((2,), 500, dtype=torch.int32)
+    cu = torch.tensor([0, 4, 8], dtype=torch.int32)
+    with pytest.raises(ValueError, match="same GPU"):
+        mm.topk(score, lens, query_len=4, max_seq_len=1000, topk=4, init_blocks=1,
+                local_blocks=1)
+    with pytest.raises(ValueError, match="same GPU"):
+        mm.topk_ragged(score, lens, cu, max_query_len=4, max_seq_len=1000, topk=4,
+                       init_blocks=1, local_blocks=1)
+    with pytest.raises(ValueError, match="cu_seqlens_q"):
+        mm.topk_ragged(score, lens, cu.long(), max_query_len=4, max_seq_len=1000, topk=4,
+                       init_blocks=1, local_blocks=1)
+    q = torch.zeros((8, 1, 128), dtype=torch.bfloat16)
+    cache = torch.zeros((4, 128, 128), dtype=torch.bfloat16)
+    table = torch.zeros((2, 8), dtype=torch.int32)
+    with pytest.raises(ValueError, match="more query rows"):
+        mm.prefill_ragged(q, cache, table, lens, cu, max_query_len=3, max_seq_len=1000, topk=4,
+                          init_blocks=1, local_blocks=1, sm_scale=0.1)
+    with pytest.raises(ValueError, match="same GPU"):
+        mm.prefill_ragged(q, cache, table, lens, cu, max_query_len=4, max_seq_len=1000, topk=4,
+                          init_blocks=1, local_blocks=1, sm_scale=0.1)
+    with pytest.raises(ValueError, match="same GPU"):
+        mm.decode_sparse_table(q[:2], cache, table, lens, query_len=1, max_seq_len=1000, topk=4,
+                               init_blocks=1, local_blocks=1, sm_scale=0.1,
+                               attention_block_table=table,
+                               sparse_block_table_out=torch.zeros((2, 8), dtype=torch.int32),
+                               sparse_context_lens_out=torch.zeros((2,), dtype=torch.int32),
+                               block_page_stride=2, pages_per_block=2)
+
+
 def test_workload_generator_layout():
     import workloads as W
     wl = W.make("tiny")
