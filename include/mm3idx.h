@@ -95,6 +95,7 @@ extern "C" {
 #define MM3IDX_OP_DECODE   1
 #define MM3IDX_OP_PREFILL  2
 #define MM3IDX_OP_PREFILL_NVFP4 3
+#define MM3IDX_OP_SCORE_NVFP4   4
 
 /* The problem every scoring call reads.  Host struct; the pointers in it are
  * device pointers. */
@@ -129,10 +130,29 @@ typedef struct mm3idx_problem {
  * are not touched.  Requires out_row_stride >= cdiv(max_seq_len,128) and
  * out_head_stride >= rows * out_row_stride.  Rows with heads*query_len <= 32
  * run on the streaming decode kernel, others on the tensor-core prefill
- * kernel.  bf16 cache only.
+ * kernel.  bf16 cache (NVFP4 pages: mm3idx_score_nvfp4).
  */
 int mm3idx_score(const mm3idx_problem_t *p, float *out, int64_t out_head_stride,
                  int64_t out_row_stride, void *stream);
+
+/*
+ * mm3idx_score_nvfp4 -- mm3idx_score over NVFP4 index-K pages (indexer_nvfp4,
+ * MiniMaxM3IndexerRocmNvfp4Impl.forward: the NVFP4 decode and prefill
+ * scorers write the fp32 block scores the top-k then reads; module
+ * docstring: an element is e4m3_rn_satfinite(e2m1 * scale)).  p->index_cache
+ * holds the e2m1 codes and p->index_scales the e4m3 scales (layouts in
+ * mm3idx_problem_t).  out as in mm3idx_score.  Rows with heads * query_len
+ * <= 32 run on the streaming NVFP4 decode kernel, which dequantises each
+ * page on chip (workspace may be NULL); others first dequantise every page a
+ * request can see, once, into a bf16 copy in the workspace, then run on the
+ * tensor-core scorer: workspace of mm3idx_workspace_bytes(
+ * MM3IDX_OP_SCORE_NVFP4, ...) bytes, 256-byte aligned, no initialisation
+ * needed (and num_reqs * cdiv(max_seq_len,128) <= INT_MAX / 128, else
+ * MM3IDX_ERR_UNSUPPORTED).
+ */
+int mm3idx_score_nvfp4(const mm3idx_problem_t *p, float *out, int64_t out_head_stride,
+                       int64_t out_row_stride, void *workspace, size_t workspace_bytes,
+                       void *stream);
 
 /*
  * mm3idx_topk -- top-k selection from a score tensor (index_topk,
@@ -162,6 +182,8 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
  * op = MM3IDX_OP_PREFILL_NVFP4: that (rounded up to 256 bytes), then a bf16
  * copy of the keys [num_reqs * cdiv(max_seq_len,128), 128, 128] and an
  * int32 table [num_reqs, cdiv(max_seq_len,128)].
+ * op = MM3IDX_OP_SCORE_NVFP4 (topk is not read): 0 when heads * query_len
+ * <= 32, else the bf16 copy of the keys and its table as above.
  * Writes the size to *bytes.  Reads the current device's attributes; no
  * allocation.
  */
@@ -277,7 +299,8 @@ int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
  * bf16 tensor-core scorer and the selector then run on that copy.  Workspace:
  * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL_NVFP4, ...) bytes, 256-byte
  * aligned, no initialisation needed.  A block table entry outside
- * [0, num_pages) sets MM3IDX_DEV_BAD_PAGE (its keys are taken as zero).
+ * [0, num_pages) sets MM3IDX_DEV_BAD_PAGE and its block gets no visible
+ * tokens, as in the bf16 calls.
  * Requires num_reqs * cdiv(max_seq_len, 128) <= INT_MAX / 128
  * (MM3IDX_ERR_UNSUPPORTED).  out as in mm3idx_prefill.
  */

@@ -11,6 +11,7 @@ been built: there is no CPU or PyTorch fallback.
 Entry points (names after the vLLM MiniMax-M3 ``index_topk`` page):
 
 * :func:`score`        -- fp32 block scores [heads, rows, cdiv(max_seq_len,128)]
+* :func:`score_nvfp4`  -- the same over NVFP4 index-K pages
 * :func:`topk`         -- ids from a score tensor
 * :func:`decode`       -- fused score + top-k for short query runs
 * :func:`decode_nvfp4` -- the same over NVFP4 index-K pages
@@ -31,6 +32,7 @@ OK = 0
 OP_DECODE = 1
 OP_PREFILL = 2
 OP_PREFILL_NVFP4 = 3
+OP_SCORE_NVFP4 = 4
 MAX_TOPK = 32
 MAX_DECODE_ROWS = 32
 STATIC_SCRATCH_BYTES = 8 << 20
@@ -84,6 +86,9 @@ SYMBOLS = {
     "mm3idx_workspace_bytes": (ctypes.c_int, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     "mm3idx_score": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_int64,
                                     ctypes.c_int64, ctypes.c_void_p]),
+    "mm3idx_score_nvfp4": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.c_void_p]),
     "mm3idx_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                    ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
@@ -155,9 +160,28 @@ def _check(status: int, what: str):
         raise Mm3idxError(status, what)
 
 
-def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream(device, stream=None):
+    """The stream a call launches on: `stream`, which must belong to the
+    inputs' GPU, else that GPU's current stream."""
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    _need(torch.device(stream.device) == torch.device(device),
+          "stream must belong to the inputs' GPU")
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on(device):
+    """Make the inputs' GPU current for a library call: the library takes the
+    SM count, its status word and its static scratch from the current device."""
+    return torch.cuda.device(device)
+
+
+def _ws(workspace, device):
+    """(pointer, bytes) of a caller-provided workspace on the inputs' GPU."""
+    _need(isinstance(workspace, torch.Tensor) and workspace.device == torch.device(device)
+          and workspace.is_contiguous(),
+          "workspace must be a contiguous tensor on the inputs' GPU")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
 
 def _cdiv(a, b):
@@ -241,11 +265,42 @@ def score(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, 
     width = _cdiv(max_seq_len, 128)
     if out is None:
         out = torch.empty((heads, rows, width), dtype=torch.float32, device=idx_q.device)
+    _score_out_ok(out, heads, rows, width, idx_q.device)
+    with _on(idx_q.device):
+        _check(lib.mm3idx_score(ctypes.byref(p), out.data_ptr(), out.stride(0), out.stride(1),
+                                _stream(idx_q.device, stream)), "mm3idx_score")
+    return out[:, :rows, :width]
+
+
+def _score_out_ok(out, heads, rows, width, device):
     _need(out.dtype == torch.float32 and out.ndim == 3 and out.shape[0] == heads
           and out.shape[1] >= rows and out.shape[2] >= width and out.stride(2) == 1,
           "out must be fp32 [heads, >=rows, >=cdiv(max_seq_len,128)] with unit inner stride")
-    _check(lib.mm3idx_score(ctypes.byref(p), out.data_ptr(), out.stride(0), out.stride(1),
-                            _stream(stream)), "mm3idx_score")
+    _need(out.device == torch.device(device), "out must be on the inputs' GPU")
+
+
+def score_nvfp4(idx_q, codes, scales, block_table, seq_lens, *, query_len, max_seq_len,
+                sm_scale, out=None, workspace=None, stream=None):
+    """:func:`score` over NVFP4 pages (codes uint8 [pages,128,64], scales
+    uint8 e4m3 [pages,128,8]).  Short query runs (heads * query_len <= 32)
+    dequantise on chip in the streaming kernel; longer ones first make a
+    bf16 copy of the visible pages in ``workspace`` (from
+    ``new_workspace(OP_SCORE_NVFP4, ...)``; allocated when not given)."""
+    p = _problem(idx_q, codes, block_table, seq_lens, query_len, max_seq_len, sm_scale,
+                 index_scales=scales, nvfp4=True)
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    width = _cdiv(max_seq_len, 128)
+    if out is None:
+        out = torch.empty((heads, rows, width), dtype=torch.float32, device=idx_q.device)
+    _score_out_ok(out, heads, rows, width, idx_q.device)
+    with _on(idx_q.device):
+        if workspace is None:
+            workspace = new_workspace(OP_SCORE_NVFP4, heads, seq_lens.shape[0], query_len,
+                                      max_seq_len, 1, idx_q.device)
+        wp, wn = _ws(workspace, idx_q.device)
+        _check(lib.mm3idx_score_nvfp4(ctypes.byref(p), out.data_ptr(), out.stride(0),
+                                      out.stride(1), wp, wn, _stream(idx_q.device, stream)),
+               "mm3idx_score_nvfp4")
     return out[:, :rows, :width]
 
 
@@ -276,10 +331,11 @@ def topk(score_t, seq_lens, *, query_len, max_seq_len, topk, init_blocks, local_
     _need(score_t.shape[1] >= rows and score_t.shape[2] >= _cdiv(max_seq_len, 128),
           "score narrower than the rows or cdiv(max_seq_len,128)")
     out = _ids_out(out, heads, rows, topk, score_t.device)
-    _check(lib.mm3idx_topk(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,
-                           seq_lens.data_ptr(), seq_lens.shape[0], query_len, max_seq_len, topk,
-                           init_blocks, local_blocks, out.data_ptr(), out.stride(0), out.stride(1),
-                           _stream(stream)), "mm3idx_topk")
+    with _on(score_t.device):
+        _check(lib.mm3idx_topk(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,
+                               seq_lens.data_ptr(), seq_lens.shape[0], query_len, max_seq_len,
+                               topk, init_blocks, local_blocks, out.data_ptr(), out.stride(0),
+                               out.stride(1), _stream(score_t.device, stream)), "mm3idx_topk")
     return out[:, :rows, :]
 
 
@@ -289,12 +345,13 @@ def _fused(fn, name, op, idx_q, cache, block_table, seq_lens, scales, nvfp4, que
                  index_scales=scales, nvfp4=nvfp4)
     rows, heads = idx_q.shape[0], idx_q.shape[1]
     out = _ids_out(out, heads, rows, topk, idx_q.device)
-    if workspace is None:
-        workspace = new_workspace(op, heads, seq_lens.shape[0], query_len, max_seq_len, topk,
-                                  idx_q.device)
-    _check(fn(ctypes.byref(p), topk, init_blocks, local_blocks, out.data_ptr(), out.stride(0),
-              out.stride(1), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-              _stream(stream)), name)
+    with _on(idx_q.device):
+        if workspace is None:
+            workspace = new_workspace(op, heads, seq_lens.shape[0], query_len, max_seq_len, topk,
+                                      idx_q.device)
+        wp, wn = _ws(workspace, idx_q.device)
+        _check(fn(ctypes.byref(p), topk, init_blocks, local_blocks, out.data_ptr(), out.stride(0),
+                  out.stride(1), wp, wn, _stream(idx_q.device, stream)), name)
     return out[:, :rows, :]
 
 
@@ -350,14 +407,16 @@ def decode_sparse_table(idx_q, index_cache, block_table, seq_lens, *, query_len,
     t.sparse_table_stride = st.stride(0) if st.shape[0] > 1 else max(st.shape[1], 1)
     t.sparse_context_lens_out = ctx.data_ptr()
     out = _ids_out(out, heads, rows, topk, idx_q.device)
-    if workspace is None:
-        workspace = new_workspace(OP_DECODE, heads, seq_lens.shape[0], query_len, max_seq_len,
-                                  topk, idx_q.device)
-    _check(lib.mm3idx_decode_sparse_table(ctypes.byref(p), topk, init_blocks, local_blocks,
-                                          out.data_ptr(), out.stride(0), out.stride(1),
-                                          ctypes.byref(t), workspace.data_ptr(),
-                                          workspace.numel() * workspace.element_size(),
-                                          _stream(stream)), "mm3idx_decode_sparse_table")
+    with _on(idx_q.device):
+        if workspace is None:
+            workspace = new_workspace(OP_DECODE, heads, seq_lens.shape[0], query_len,
+                                      max_seq_len, topk, idx_q.device)
+        wp, wn = _ws(workspace, idx_q.device)
+        _check(lib.mm3idx_decode_sparse_table(ctypes.byref(p), topk, init_blocks, local_blocks,
+                                              out.data_ptr(), out.stride(0), out.stride(1),
+                                              ctypes.byref(t), wp, wn,
+                                              _stream(idx_q.device, stream)),
+               "mm3idx_decode_sparse_table")
     return out[:, :rows, :]
 
 
@@ -403,12 +462,11 @@ def score_ragged(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q, *, max
     width = _cdiv(max_seq_len, 128)
     if out is None:
         out = torch.empty((heads, total_q, width), dtype=torch.float32, device=idx_q.device)
-    _need(out.dtype == torch.float32 and out.ndim == 3 and out.shape[0] == heads
-          and out.shape[1] >= total_q and out.shape[2] >= width and out.stride(2) == 1,
-          "out must be fp32 [heads, >=rows, >=cdiv(max_seq_len,128)] with unit inner stride")
-    _check(lib.mm3idx_score_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q,
-                                   out.data_ptr(), out.stride(0), out.stride(1), _stream(stream)),
-           "mm3idx_score_ragged")
+    _score_out_ok(out, heads, total_q, width, idx_q.device)
+    with _on(idx_q.device):
+        _check(lib.mm3idx_score_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q,
+                                       out.data_ptr(), out.stride(0), out.stride(1),
+                                       _stream(idx_q.device, stream)), "mm3idx_score_ragged")
     return out[:, :total_q, :width]
 
 
@@ -423,11 +481,13 @@ def topk_ragged(score_t, seq_lens, cu_seqlens_q, *, max_query_len, max_seq_len, 
     _on_gpu(score_t, seq_lens, cu_seqlens_q)
     heads, total_q = score_t.shape[0], score_t.shape[1]
     out = _ids_out(out, heads, total_q, topk, score_t.device)
-    _check(lib.mm3idx_topk_ragged(score_t.data_ptr(), score_t.stride(0), score_t.stride(1), heads,
-                                  cu_seqlens_q.data_ptr(), seq_lens.data_ptr(), seq_lens.shape[0],
-                                  total_q, max_query_len, max_seq_len, topk, init_blocks,
-                                  local_blocks, out.data_ptr(), out.stride(0), out.stride(1),
-                                  _stream(stream)), "mm3idx_topk_ragged")
+    with _on(score_t.device):
+        _check(lib.mm3idx_topk_ragged(score_t.data_ptr(), score_t.stride(0), score_t.stride(1),
+                                      heads, cu_seqlens_q.data_ptr(), seq_lens.data_ptr(),
+                                      seq_lens.shape[0], total_q, max_query_len, max_seq_len,
+                                      topk, init_blocks, local_blocks, out.data_ptr(),
+                                      out.stride(0), out.stride(1),
+                                      _stream(score_t.device, stream)), "mm3idx_topk_ragged")
     return out[:, :total_q, :]
 
 
@@ -443,14 +503,15 @@ def prefill_ragged(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q, *, m
     heads = idx_q.shape[1]
     op = OP_PREFILL_NVFP4 if index_scales is not None else OP_PREFILL
     out = _ids_out(out, heads, total_q, topk, idx_q.device)
-    if workspace is None:
-        workspace = new_workspace(op, heads, seq_lens.shape[0], max_query_len, max_seq_len, topk,
-                                  idx_q.device)
-    _check(lib.mm3idx_prefill_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q, topk,
-                                     init_blocks, local_blocks, out.data_ptr(), out.stride(0),
-                                     out.stride(1), workspace.data_ptr(),
-                                     workspace.numel() * workspace.element_size(),
-                                     _stream(stream)), "mm3idx_prefill_ragged")
+    with _on(idx_q.device):
+        if workspace is None:
+            workspace = new_workspace(op, heads, seq_lens.shape[0], max_query_len, max_seq_len,
+                                      topk, idx_q.device)
+        wp, wn = _ws(workspace, idx_q.device)
+        _check(lib.mm3idx_prefill_ragged(ctypes.byref(p), cu_seqlens_q.data_ptr(), total_q, topk,
+                                         init_blocks, local_blocks, out.data_ptr(), out.stride(0),
+                                         out.stride(1), wp, wn, _stream(idx_q.device, stream)),
+               "mm3idx_prefill_ragged")
     return out[:, :total_q, :]
 
 
@@ -462,20 +523,34 @@ def decode_static(idx_q, index_cache, block_table, seq_lens, *, query_len, max_s
     p = _problem(idx_q, index_cache, block_table, seq_lens, query_len, max_seq_len, sm_scale)
     rows, heads = idx_q.shape[0], idx_q.shape[1]
     out = _ids_out(out, heads, rows, topk, idx_q.device)
-    _check(lib.mm3idx_decode_static(ctypes.byref(p), topk, init_blocks, local_blocks,
-                                    out.data_ptr(), out.stride(0), out.stride(1), _stream(stream)),
-           "mm3idx_decode_static")
+    with _on(idx_q.device):
+        _check(lib.mm3idx_decode_static(ctypes.byref(p), topk, init_blocks, local_blocks,
+                                        out.data_ptr(), out.stride(0), out.stride(1),
+                                        _stream(idx_q.device, stream)), "mm3idx_decode_static")
     return out[:, :rows, :]
+
+
+def _stream_device(stream):
+    return (torch.device(stream.device) if stream is not None
+            else torch.device("cuda", torch.cuda.current_device()))
 
 
 def check_wait_timeout(warps: int = 4, stream=None):
     """Make the bounded on-chip wait run out on purpose (about 2 s); the
-    device status word then holds DEV_TIMEOUT (read it with get_device_error)."""
-    _check(lib.mm3idx_check_wait_timeout(warps, _stream(stream)), "mm3idx_check_wait_timeout")
+    device status word of the stream's GPU then holds DEV_TIMEOUT (read it
+    with get_device_error)."""
+    dev = _stream_device(stream)
+    with _on(dev):
+        _check(lib.mm3idx_check_wait_timeout(warps, _stream(dev, stream)),
+               "mm3idx_check_wait_timeout")
 
 
 def get_device_error(stream=None) -> int:
-    """Synchronise the stream, read and clear the device status word."""
+    """Synchronise the stream (default: the current GPU's current stream),
+    then read and clear the device status word of the stream's GPU."""
+    dev = _stream_device(stream)
     v = ctypes.c_int32(0)
-    _check(lib.mm3idx_get_device_error(_stream(stream), ctypes.byref(v)), "mm3idx_get_device_error")
+    with _on(dev):
+        _check(lib.mm3idx_get_device_error(_stream(dev, stream), ctypes.byref(v)),
+               "mm3idx_get_device_error")
     return v.value

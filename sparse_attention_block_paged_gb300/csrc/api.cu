@@ -200,15 +200,28 @@ size_t prefill_part_a(int sms, int32_t heads, int32_t num_reqs, int32_t query_le
   return static_cast<size_t>(heads) * rows * w * 4;
 }
 
-// Whole prefill workspace: part A, then for NVFP4 a bf16 copy of the keys
-// [num_reqs * cdiv(max_seq_len,128), 128, 128] and an int32 table
-// [num_reqs, cdiv(max_seq_len,128)].
+// The bf16 copy of an NVFP4 batch's visible pages: [num_reqs *
+// cdiv(max_seq_len,128), 128, 128] bf16, then its int32 table [num_reqs,
+// cdiv(max_seq_len,128)].
+size_t dequant_copy_bytes(int32_t num_reqs, int32_t max_seq_len) {
+  const size_t slots = static_cast<size_t>(num_reqs) * cdiv(max_seq_len, kBlock);
+  return slots * kBlock * kD * 2 + align256(slots * 4);
+}
+
+// Whole prefill workspace: part A, then for NVFP4 the bf16 copy of the keys.
 size_t prefill_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len,
                         int32_t max_seq_len, int32_t topk, bool nvfp4) {
   const size_t a = prefill_part_a(sms, heads, num_reqs, query_len, max_seq_len, topk);
   if (!nvfp4) return a;
-  const size_t slots = static_cast<size_t>(num_reqs) * cdiv(max_seq_len, kBlock);
-  return align256(a) + slots * kBlock * kD * 2 + align256(slots * 4);
+  return align256(a) + dequant_copy_bytes(num_reqs, max_seq_len);
+}
+
+// Score workspace of NVFP4 pages: none when the streaming decode kernel
+// dequantises on chip (heads * query_len <= 32), else the bf16 copy.
+size_t score_nvfp4_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len,
+                            int32_t max_seq_len) {
+  if (static_cast<int64_t>(heads) * query_len <= MM3IDX_MAX_DECODE_ROWS) return 0;
+  return dequant_copy_bytes(num_reqs, max_seq_len);
 }
 
 DecodeArgs decode_args(const mm3idx_problem_t* p, int* status) {
@@ -254,10 +267,13 @@ int check_sparse_table(const mm3idx_problem_t* p, int32_t topk, const mm3idx_spa
   return MM3IDX_OK;
 }
 
+// static_scratch: the workspace is the library's own array (mm3idx_decode_static):
+// a problem too large for it is MM3IDX_ERR_STATIC_SCRATCH, and its tickets are
+// cleared on the stream once every argument check has passed.
 int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init_blocks,
                int32_t local_blocks, int32_t* out, int64_t out_head_stride, int64_t out_row_stride,
                void* workspace, size_t workspace_bytes, void* stream,
-               const mm3idx_sparse_table_t* table = nullptr) {
+               const mm3idx_sparse_table_t* table = nullptr, bool static_scratch = false) {
   int rc = check_problem(p, nvfp4);
   if (rc) return rc;
   if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
@@ -271,8 +287,16 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
   const size_t need = decode_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len, topk);
+  if (static_scratch && need > workspace_bytes) return MM3IDX_ERR_STATIC_SCRATCH;
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MM3IDX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap kmap;
+  if (!nvfp4 && (rc = make_kmap(p, &kmap))) return rc;
+  // The tickets must start at zero; a completed call leaves them so, but a
+  // call that gave up part-way may not have.
+  if (static_scratch && cudaMemsetAsync(workspace, 0, decode_ws_head(p->num_reqs), s) != cudaSuccess)
+    return MM3IDX_ERR_CUDA;
   DecodeArgs a = decode_args(p, dev->status);
   a.mode = kModeSelect;
   a.topk = topk;
@@ -285,15 +309,12 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   a.tickets = reinterpret_cast<unsigned int*>(ws);
   a.partials = reinterpret_cast<uint64_t*>(ws + decode_ws_head(p->num_reqs));
   const int grid = decode_grid(p, dev->sms);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (nvfp4) {
     a.codes = static_cast<const uint8_t*>(p->index_cache);
     a.scales = static_cast<const uint8_t*>(p->index_scales);
     e = launch_decode_nvfp4(a, grid, s);
   } else {
-    CUtensorMap kmap;
-    if ((rc = make_kmap(p, &kmap))) return rc;
     e = launch_decode_bf16(kmap, a, grid, s);
   }
   if (e == cudaSuccess && table) {
@@ -425,6 +446,86 @@ int score_then_fill(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_
   return cuda_status(launch_fill_invisible(f, width, dev->sms, s));
 }
 
+// Dequantises every page an NVFP4 batch can see, once, into a bf16 copy at
+// `dst` (dequant_copy_bytes long) and points *q at it: the copy's table maps
+// (request, block) to its slot, or to -1 for a block whose page id is out of
+// range, so the bf16 scorer treats that block as it treats a bad page (no
+// visible tokens).  Requires num_reqs * cdiv(max_seq_len,128) <= INT_MAX / 128.
+int dequant_copy(const mm3idx_problem_t* p, uint8_t* dst, DeviceInfo* dev, cudaStream_t s,
+                 mm3idx_problem_t* q) {
+  const int64_t width = cdiv(p->max_seq_len, kBlock);
+  const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
+  DequantArgs d{};
+  d.codes = static_cast<const uint8_t*>(p->index_cache);
+  d.scales = static_cast<const uint8_t*>(p->index_scales);
+  d.num_pages = p->num_pages;
+  d.table = p->block_table;
+  d.table_stride = p->table_stride;
+  d.seq_lens = p->seq_lens;
+  d.num_reqs = p->num_reqs;
+  d.max_seq_len = p->max_seq_len;
+  d.width = static_cast<int32_t>(width);
+  d.pages_out = reinterpret_cast<uint16_t*>(dst);
+  d.table_out = reinterpret_cast<int32_t*>(dst + slots * kBlock * kD * 2);
+  d.status = dev->status;
+  int rc = cuda_status(launch_dequant_pages(d, dev->sms, s));
+  if (rc) return rc;
+  *q = *p;
+  q->index_cache = d.pages_out;
+  q->index_scales = nullptr;
+  q->num_pages = static_cast<int32_t>(slots);
+  q->block_table = d.table_out;
+  q->table_stride = width;
+  q->table_width = static_cast<int32_t>(width);
+  return MM3IDX_OK;
+}
+
+// Block scores of a uniform batch.  heads * query_len <= 32: the streaming
+// decode kernel in score mode (NVFP4 pages dequantised on chip); larger row
+// counts: the tensor-core scorer, on a bf16 copy of NVFP4 pages made in the
+// workspace first.
+int run_score(const mm3idx_problem_t* p, bool nvfp4, float* out, int64_t out_head_stride,
+              int64_t out_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(p, nvfp4);
+  if (rc) return rc;
+  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
+  if (rows == 0) return MM3IDX_OK;
+  const int32_t width = static_cast<int32_t>(cdiv(p->max_seq_len, kBlock));
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, width))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  const bool streaming = static_cast<int64_t>(p->heads) * p->query_len <= MM3IDX_MAX_DECODE_ROWS;
+  if (nvfp4 && !streaming) {
+    if (static_cast<int64_t>(p->num_reqs) * width > INT_MAX / kBlock) return MM3IDX_ERR_UNSUPPORTED;
+    const size_t need = score_nvfp4_ws_bytes(p->heads, p->num_reqs, p->query_len, p->max_seq_len);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return MM3IDX_ERR_WORKSPACE;
+  }
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (streaming) {
+    DecodeArgs a = decode_args(p, dev->status);
+    a.mode = kModeScore;
+    a.topk = 1;
+    a.score = out;
+    a.s_head = out_head_stride;
+    a.s_row = out_row_stride;
+    a.fill_width = width;
+    if (nvfp4) {
+      a.codes = static_cast<const uint8_t*>(p->index_cache);
+      a.scales = static_cast<const uint8_t*>(p->index_scales);
+      return cuda_status(launch_decode_nvfp4(a, decode_grid(p, dev->sms), s));
+    }
+    CUtensorMap kmap;
+    if ((rc = make_kmap(p, &kmap))) return rc;
+    return cuda_status(launch_decode_bf16(kmap, a, decode_grid(p, dev->sms), s));
+  }
+  mm3idx_problem_t q = *p;
+  if (nvfp4 && (rc = dequant_copy(p, static_cast<uint8_t*>(workspace), dev, s, &q))) return rc;
+  return score_then_fill(&q, nullptr, static_cast<int32_t>(rows), out, out_head_stride,
+                         out_row_stride, width, dev, s);
+}
+
 // Ragged batches: row offsets on the device, total_q rows, at most
 // max_query_len rows per request (the bound the workspace is sized with).
 int check_ragged(int32_t num_reqs, int32_t max_query_len, const int32_t* cu, int32_t total_q) {
@@ -496,30 +597,7 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len,
                                                 p->max_seq_len, topk));
   mm3idx_problem_t q = *p;
-  if (nvfp4) {
-    const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
-    DequantArgs d{};
-    d.codes = static_cast<const uint8_t*>(p->index_cache);
-    d.scales = static_cast<const uint8_t*>(p->index_scales);
-    d.num_pages = p->num_pages;
-    d.table = p->block_table;
-    d.table_stride = p->table_stride;
-    d.seq_lens = p->seq_lens;
-    d.num_reqs = p->num_reqs;
-    d.max_seq_len = p->max_seq_len;
-    d.width = static_cast<int32_t>(width);
-    d.pages_out = reinterpret_cast<uint16_t*>(ws + part_a);
-    d.table_out = reinterpret_cast<int32_t*>(ws + part_a + slots * kBlock * kD * 2);
-    d.status = dev->status;
-    if ((rc = cuda_status(launch_dequant_pages(d, dev->sms, s)))) return rc;
-    // the bf16 scorer then reads the copy through an identity table
-    q.index_cache = d.pages_out;
-    q.index_scales = nullptr;
-    q.num_pages = static_cast<int32_t>(slots);
-    q.block_table = d.table_out;
-    q.table_stride = width;
-    q.table_width = static_cast<int32_t>(width);
-  }
+  if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q))) return rc;
   if (topk <= kPrefillSelectTK) {
     const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
                                               static_cast<int64_t>(p->num_reqs) * p->query_len);
@@ -609,6 +687,10 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t 
     *bytes = decode_ws_bytes(dev->sms, heads, num_reqs, query_len, topk);
     return MM3IDX_OK;
   }
+  if (op == MM3IDX_OP_SCORE_NVFP4) {
+    *bytes = score_nvfp4_ws_bytes(heads, num_reqs, query_len, max_seq_len);
+    return MM3IDX_OK;
+  }
   if (op == MM3IDX_OP_PREFILL || op == MM3IDX_OP_PREFILL_NVFP4) {
     if (topk < 1 || topk > MM3IDX_MAX_TOPK) return MM3IDX_ERR_TOPK;
     int sms = 0;
@@ -627,30 +709,14 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t 
 
 int mm3idx_score(const mm3idx_problem_t* p, float* out, int64_t out_head_stride,
                  int64_t out_row_stride, void* stream) {
-  int rc = check_problem(p, false);
-  if (rc) return rc;
-  const int64_t rows = static_cast<int64_t>(p->num_reqs) * p->query_len;
-  if (rows == 0) return MM3IDX_OK;
-  const int32_t width = static_cast<int32_t>(cdiv(p->max_seq_len, kBlock));
-  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, rows, width))
-    return MM3IDX_ERR_OUT_LAYOUT;
-  DeviceInfo* dev = nullptr;
-  if ((rc = device_info(&dev))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (static_cast<int64_t>(p->heads) * p->query_len <= MM3IDX_MAX_DECODE_ROWS) {
-    DecodeArgs a = decode_args(p, dev->status);
-    a.mode = kModeScore;
-    a.topk = 1;
-    a.score = out;
-    a.s_head = out_head_stride;
-    a.s_row = out_row_stride;
-    a.fill_width = width;
-    CUtensorMap kmap;
-    if ((rc = make_kmap(p, &kmap))) return rc;
-    return cuda_status(launch_decode_bf16(kmap, a, decode_grid(p, dev->sms), s));
-  }
-  return score_then_fill(p, nullptr, static_cast<int32_t>(rows), out, out_head_stride,
-                         out_row_stride, width, dev, s);
+  return run_score(p, false, out, out_head_stride, out_row_stride, nullptr, 0, stream);
+}
+
+int mm3idx_score_nvfp4(const mm3idx_problem_t* p, float* out, int64_t out_head_stride,
+                       int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return run_score(p, true, out, out_head_stride, out_row_stride, workspace, workspace_bytes,
+                   stream);
 }
 
 int mm3idx_score_ragged(const mm3idx_problem_t* p, const int32_t* cu_seqlens_q, int32_t total_q,
@@ -753,18 +819,11 @@ int mm3idx_decode_static(const mm3idx_problem_t* p, int32_t topk, int32_t init_b
   if (static_cast<int64_t>(p->num_reqs) * p->query_len == 0) return MM3IDX_OK;
   void* scratch = nullptr;
   if ((rc = static_scratch(&scratch))) return rc;
-  DeviceInfo* dev = nullptr;
-  if ((rc = device_info(&dev))) return rc;
-  if (decode_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len, topk) >
-      MM3IDX_STATIC_SCRATCH_BYTES)
-    return MM3IDX_ERR_STATIC_SCRATCH;
-  // The tickets must start at zero; a completed call leaves them so, but a
-  // call that gave up part-way may not have.
-  if (cudaMemsetAsync(scratch, 0, decode_ws_head(p->num_reqs), static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return MM3IDX_ERR_CUDA;
+  // Every argument check runs before the tickets are cleared (inside
+  // run_decode), so a rejected call leaves the shared array untouched.
   return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
-                    out_row_stride, scratch, MM3IDX_STATIC_SCRATCH_BYTES, stream);
+                    out_row_stride, scratch, MM3IDX_STATIC_SCRATCH_BYTES, stream, nullptr,
+                    /*static_scratch=*/true);
 }
 
 int mm3idx_get_device_error(void* stream, int32_t* code) {

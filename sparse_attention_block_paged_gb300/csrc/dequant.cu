@@ -46,17 +46,19 @@ __global__ void __launch_bounds__(kThreads) dequant_pages_kernel(const DequantAr
   for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
     const int req = static_cast<int>(slot / a.width);
     const int b = static_cast<int>(slot - static_cast<int64_t>(req) * a.width);
-    if (t == 0) a.table_out[slot] = static_cast<int32_t>(slot);
     const int seq = min(max(__ldg(a.seq_lens + req), 0), a.max_seq_len);
+    const int page = b * kBlock < seq ? __ldg(a.table + req * a.table_stride + b) : 0;
+    const bool bad = page < 0 || page >= a.num_pages;
+    // A bad page's slot is marked -1 in the copy's table: the scorer then
+    // scores that block as it scores a bad page of a bf16 cache (no visible
+    // tokens) and sets the status bit.
+    if (t == 0) a.table_out[slot] = bad ? -1 : static_cast<int32_t>(slot);
     if (b * kBlock >= seq) continue;  // never read by the scorer
-    const int page = __ldg(a.table + req * a.table_stride + b);
-    uint4* dst = reinterpret_cast<uint4*>(a.pages_out + slot * (kBlock * kD) + tok * kD + half * 64);
-    if (page < 0 || page >= a.num_pages) {
+    if (bad) {
       if (t == 0) atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) dst[k] = make_uint4(0, 0, 0, 0);
       continue;
     }
+    uint4* dst = reinterpret_cast<uint4*>(a.pages_out + slot * (kBlock * kD) + tok * kD + half * 64);
     const uint4* src = reinterpret_cast<const uint4*>(a.codes + static_cast<int64_t>(page) * (kBlock * kD / 2) +
                                                       tok * (kD / 2) + half * 32);
     const uint4 c0 = __ldg(src), c1 = __ldg(src + 1);

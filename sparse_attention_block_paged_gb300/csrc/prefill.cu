@@ -369,19 +369,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         sInfo[st] = kInfoValid | (two ? kInfoTwo : 0u) | (new_tile ? kInfoNewTile : 0u);
         uint8_t* dst = sK + st * kStageBytes;
-        const bool good = pa >= 0 && pa < a.num_pages && (!two || (pb >= 0 && pb < a.num_pages));
-        if (good) {
+        // A page id out of range is not loaded (the epilogue gives its block
+        // -inf); the other page of the pair still is.
+        const bool good_a = pa >= 0 && pa < a.num_pages;
+        const bool good_b = two && pb >= 0 && pb < a.num_pages;
+        if (!good_a || (two && !good_b)) atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
+        const uint32_t bytes = (good_a ? kPage : 0) + (good_b ? kPage : 0);
+        if (bytes) {
           // Stage layout: [A cols 0-63][B cols 0-63][A cols 64-127][B cols 64-127],
           // i.e. 256 key rows per 64-column half, as the N = 256 operand.
-          mbar_arrive_expect_tx(&full[st], two ? 2 * kPage : kPage);
-          tma_load_2d(dst, &kmap, &full[st], 0, pa * 128, pol_k);
-          tma_load_2d(dst + 2 * kHalf, &kmap, &full[st], 64, pa * 128, pol_k);
-          if (two) {
+          mbar_arrive_expect_tx(&full[st], bytes);
+          if (good_a) {
+            tma_load_2d(dst, &kmap, &full[st], 0, pa * 128, pol_k);
+            tma_load_2d(dst + 2 * kHalf, &kmap, &full[st], 64, pa * 128, pol_k);
+          }
+          if (good_b) {
             tma_load_2d(dst + kHalf, &kmap, &full[st], 0, pb * 128, pol_k);
             tma_load_2d(dst + 3 * kHalf, &kmap, &full[st], 64, pb * 128, pol_k);
           }
         } else {
-          atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
           mbar_arrive(&full[st]);
         }
       }
@@ -500,6 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b0 < U.nvis) {
         const int b = b0 + team;
         const bool mine = b < U.nvis;
+        // The block's page id, read before the wait so that its latency is
+        // hidden: an id out of range means no visible tokens (-inf).
+        const int page = mine ? __ldg(a.table + static_cast<int64_t>(U.req) * a.table_stride + b) : 0;
         bool got = true;
         if (lane == 0) got = mbar_wait(&acc_full[acc], (it >> 1) & 1u, abort_flag);
         if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -541,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
         if (mine && row_ok) {
-          const float score = fmaxf(m0, m1) * a.sm_scale;
+          const float score =
+              (page >= 0 && page < a.num_pages) ? fmaxf(m0, m1) * a.sm_scale : -INFINITY;
           if constexpr (kSelect) {
             if (b >= f_lo && b < l_lo) list.offer_shallow(make_key(score, b));
           } else {

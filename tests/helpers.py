@@ -86,3 +86,38 @@ def check_ids(got, want, scores, wl, rows=None, where=""):
             c = pos // BLOCK if pos >= 0 else -1
             check_ids_row(got[h, k], want[h, k], scores[h, k], c, wl.topk, wl.init_blocks,
                           wl.local_blocks, where=f"{where} h{h} row{r}")
+
+
+def split_requests(wl, sms):
+    """Requests of a decode batch whose blocks the streaming kernel spreads
+    over more than one CTA.  The kernel gives each CTA an equal share of the
+    request-major list of positions (each request counts six extra positions
+    before its blocks); position x belongs to CTA ((x + 1) * G - 1) // total."""
+    nb = (np.minimum(np.maximum(wl.seq_lens.astype(np.int64), 0), wl.max_seq_len) + 127) // 128
+    slots = np.where(nb > 0, nb + 6, 0)
+    total = int(slots.sum())
+    grid = max(1, min(sms, wl.num_reqs * -(-wl.max_seq_len // 128)))
+    first = np.concatenate([[0], np.cumsum(slots)[:-1]]) + 6   # each request's first block
+    cta = lambda x: ((x + 1) * grid - 1) // total               # noqa: E731
+    return [i for i in range(wl.num_reqs) if nb[i] > 0 and cta(first[i]) != cta(first[i] + nb[i] - 1)]
+
+
+def decode_sample(wl, sms, n=16, seed=0):
+    """At least n requests of a decode batch: the shortest, the longest, the
+    first and last few split across CTAs, and random others."""
+    rng = np.random.default_rng(seed)
+    order = np.argsort(wl.seq_lens, kind="stable")
+    split = split_requests(wl, sms)
+    pick = {int(order[0]), int(order[1]), int(order[-1]), int(order[-2])}
+    pick |= set(split[:4]) | set(split[-4:])
+    rest = [i for i in range(wl.num_reqs) if i not in pick]
+    need = max(0, n - len(pick))
+    pick |= set(int(x) for x in rng.choice(rest, size=min(need, len(rest)), replace=False))
+    return sorted(pick), split
+
+
+def prefill_sample_rows(rows, every=61, edge=256):
+    """Rows of a long prefill checked one by one: every `every`-th row plus the
+    first and last `edge`."""
+    return sorted(set(range(0, rows, every)) | set(range(min(edge, rows)))
+                  | set(range(max(0, rows - edge), rows)))

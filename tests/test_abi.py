@@ -275,3 +275,81 @@ def test_workload_generator_layout():
     assert np.all(wl.cache[last, 300 % 128:] == W.POISON_BF16)
     again = W.make("tiny")
     assert np.array_equal(again.cache, wl.cache) and np.array_equal(again.q, wl.q)
+
+
+def test_score_nvfp4_validation_and_workspace():
+    f = mm.lib.mm3idx_score_nvfp4
+    p = problem()                                   # no scales: not an NVFP4 problem
+    assert f(ctypes.byref(p), FAKE, 1000, 8, None, 0, None) == -3
+    p = problem(index_scales=FAKE, num_reqs=0)
+    assert f(ctypes.byref(p), FAKE, 1000, 8, None, 0, None) == 0
+    # 300 rows per request: the bf16 copy needs a workspace, checked before any launch
+    p = problem(index_scales=FAKE, query_len=300)
+    assert f(ctypes.byref(p), FAKE, 1 << 20, 8, None, 0, None) == -9
+    assert f(ctypes.byref(p), FAKE, 1 << 20, 8, FAKE, 1000, None) == -9
+    assert f(ctypes.byref(p), FAKE, 1 << 20, 8, FAKE + 16, 1 << 30, None) == -9
+    assert f(ctypes.byref(p), FAKE, 1 << 20, 7, FAKE, 1 << 30, None) == -8
+    n = ctypes.c_size_t(7)
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_SCORE_NVFP4, 4, 3, 8, 1000, 1,
+                                         ctypes.byref(n)) == 0
+    assert n.value == 0                              # 4 heads x 8 rows: on chip
+    assert mm.lib.mm3idx_workspace_bytes(mm.OP_SCORE_NVFP4, 1, 3, 300, 1000, 1,
+                                         ctypes.byref(n)) == 0
+    slots = 3 * 8                                    # requests x cdiv(1000, 128)
+    assert n.value == slots * 128 * 128 * 2 + 256
+    c = header_constants()
+    assert c["MM3IDX_OP_SCORE_NVFP4"] == mm.OP_SCORE_NVFP4
+
+
+def test_binding_stream_workspace_and_out_must_be_on_the_inputs_gpu():
+    """Checks the binding makes before a library call: an explicit stream,
+    a caller's workspace and a caller's score output must all belong to the
+    inputs' GPU (the library takes their addresses as that GPU's)."""
+    import torch
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    dev0 = torch.device("cuda", 0)
+    with pytest.raises(ValueError, match="stream"):
+        mm._stream(dev0, FakeStream())
+    with pytest.raises(ValueError, match="workspace"):
+        mm._ws(torch.zeros(256, dtype=torch.uint8), dev0)
+    with pytest.raises(ValueError, match="workspace"):
+        mm._ws(None, dev0)
+    with pytest.raises(ValueError, match="out must be on"):
+        mm._score_out_ok(torch.zeros((1, 4, 8)), 1, 4, 8, dev0)
+
+
+def test_every_library_call_runs_with_the_inputs_gpu_current():
+    """The library reads the current device (SM count, status word, static
+    scratch): every call that launches work or reads the status word sits
+    inside a `with _on(device)` block, and gets its stream from _stream."""
+    import ast
+    src = open(os.path.join(ROOT, "sparse_attention_block_paged_gb300", "__init__.py")).read()
+    tree = ast.parse(src)
+    exempt = {"mm3idx_version", "mm3idx_status_string", "mm3idx_workspace_bytes"}
+    found = 0
+
+    def visit(node, guarded):
+        nonlocal found
+        if isinstance(node, ast.With):
+            guarded = guarded or any(
+                isinstance(i.context_expr, ast.Call) and getattr(i.context_expr.func, "id", "") == "_on"
+                for i in node.items)
+        lib_call = (isinstance(node, ast.Call) and isinstance(node.func, ast.Attribute)
+                    and node.func.attr.startswith("mm3idx_") and node.func.attr not in exempt
+                    and getattr(node.func.value, "id", "") == "lib")
+        # _fused calls the entry point it is given as `fn`
+        fused_call = isinstance(node, ast.Call) and getattr(node.func, "id", "") == "fn"
+        if lib_call or fused_call:
+            found += 1
+            assert guarded, f"line {node.lineno}: library call outside `with _on(...)`"
+            assert any(isinstance(a, ast.Call) and getattr(a.func, "id", "") == "_stream"
+                       for a in node.args), f"line {node.lineno}: stream not from _stream"
+        for child in ast.iter_child_nodes(node):
+            visit(child, guarded)
+
+    visit(tree, False)
+    assert found >= 11

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as W
-from helpers import check_ids, check_scores, to_device
+from helpers import check_ids, check_scores, decode_sample, prefill_sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -266,32 +266,65 @@ def _sample_rows(wl, reqs):
 
 @pytest.mark.parametrize("key", ["spec_decode", "high_batch", "nvfp4_decode"])
 def test_full_size_decode_sampled(mm, key):
+    """The named decode batches in the bench's launch configuration: ids of
+    the whole batch in one call, checked on at least 16 requests (the
+    shortest, the longest, requests split across CTAs, random others); for
+    the bf16 batches also the score call's scores on the same rows."""
+    import torch
     wl = W.make(key)
     got = run_decode(mm, wl)
     assert mm.get_device_error() == 0
-    rng = np.random.default_rng(0)
-    order = np.argsort(wl.seq_lens)
-    reqs = sorted(set([int(order[0]), int(order[-1])] +
-                      [int(x) for x in rng.choice(wl.num_reqs, size=4, replace=False)]))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    reqs, split = decode_sample(wl, sms)
+    assert len(reqs) >= 16 and any(r in split for r in reqs)
     sub = oracle.subset(wl, reqs)
     s, want = oracle.problem(sub)
     rows = _sample_rows(wl, reqs)
     check_ids(got[:, rows], want, s, sub, where=key)
+    if wl.kv_format == "bf16":
+        sc = run_scores(mm, wl)
+        assert mm.get_device_error() == 0
+        check_scores(sc[:, rows], s, f"{key} scores")
 
 
-def test_full_size_prefill_sampled(mm):
-    wl = W.make("prefill")
-    got = run_prefill(mm, wl)
-    assert mm.get_device_error() == 0
-    rows = sorted(set([0, 1, 127, 128, 129, 255, 256, 4095, 4096, 16384, 30001,
-                       wl.query_len - 129, wl.query_len - 128, wl.query_len - 1] +
-                      list(range(5, wl.query_len, 997))))
+def _prefill_rows_check(wl, rows, ids, scores=None, where=""):
+    from helpers import check_ids_row
     for r in rows:
         s, want = oracle.row(wl, r, 0)
         c = len(s) - 1
-        from helpers import check_ids_row
-        check_ids_row(got[0, r], want, s, c, wl.topk, wl.init_blocks, wl.local_blocks,
-                      where=f"prefill row {r}")
+        check_ids_row(ids[0, r], want, s, c, wl.topk, wl.init_blocks, wl.local_blocks,
+                      where=f"{where} row {r}")
+        if scores is not None:
+            full = np.full(scores.shape[2], -np.inf)
+            full[:len(s)] = s
+            check_scores(scores[0, r][None], full[None], f"{where} scores row {r}")
+
+
+def test_full_size_prefill_sampled(mm):
+    """The 32768-token causal prefill: the fused ids (scorer with selection)
+    and the score call (the score-mode kernel the prefill roofline is timed
+    on), checked on every 61st row and the first and last 256 rows."""
+    wl = W.make("prefill")
+    ids = run_prefill(mm, wl)
+    assert mm.get_device_error() == 0
+    sc = run_scores(mm, wl)
+    assert mm.get_device_error() == 0
+    _prefill_rows_check(wl, prefill_sample_rows(wl.rows), ids, sc, where="prefill")
+
+
+def test_full_size_nvfp4_prefill_sampled(mm):
+    """The 32768-token NVFP4 causal prefill (dequantised copy, then the fused
+    scorer), ids and scores checked on the same rows as the bf16 prefill."""
+    wl = W.make("nvfp4_prefill")
+    d = to_device(wl)
+    kw = dict(query_len=wl.query_len, max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale)
+    ids = mm.prefill_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"], topk=wl.topk,
+                           init_blocks=wl.init_blocks, local_blocks=wl.local_blocks,
+                           **kw).cpu().numpy()
+    sc = mm.score_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"],
+                        **kw).cpu().numpy()
+    assert mm.get_device_error() == 0
+    _prefill_rows_check(wl, prefill_sample_rows(wl.rows), ids, sc, where="nvfp4 prefill")
 
 
 def test_fused_prefill_workspace_reuse_and_graph_replay(mm):
