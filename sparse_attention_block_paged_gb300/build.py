@@ -19,8 +19,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmm3idx.so")
-SOURCES = ["api.cu", "decode.cu", "prefill.cu", "select.cu", "dequant.cu", "sparse_table.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "warp_select.cuh"]
+SOURCES = ["api.cu", "decode.cu", "decode_fp4.cu", "prefill.cu", "select.cu", "dequant.cu",
+           "sparse_table.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "warp_select.cuh", "decode_common.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
