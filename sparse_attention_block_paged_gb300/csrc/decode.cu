@@ -323,10 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
       list.clear();
+      int pg = 0;  // page ids 32 at a time, one per lane (units never straddle two 32s)
       for (int bu = b0; bu < b1; bu += 2, ++ut) {
         const int b = bu + e;
         const bool mine = b < b1;
-        const int page = mine ? __ldg(trow + b) : 0;
+        if (((bu - b0) & 31) == 0) pg = bu + lane < b1 ? __ldg(trow + bu + lane) : 0;
+        const int page = __shfl_sync(0xffffffffu, pg, (b - b0) & 31);
         const uint32_t ab = ut % kAccBufs, ar = ut / kAccBufs;
         if (!warp_wait(&acc_full[ab], ar & 1, abort_flag)) {
           ok = false;

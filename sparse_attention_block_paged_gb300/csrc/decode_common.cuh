@@ -234,22 +234,145 @@ __device__ __forceinline__ void load_q_tile(const DecodeArgs& a, int req, uint8_
   }
 }
 
-// The merge warp.  Per request, in the walker's order: wait for the NL
-// candidate lists per row that the scoring warps handed over (hand-over slot
-// seg & 1, [NL][TK][32 rows]), fold them (lane n owns row n), then either
-// write the rows (a request held by this CTA alone) or publish the lists and
-// take the request's ticket, the last of its CTAs merging every CTA's lists
-// and writing the rows.  With total >= grid every share is non-empty, so the
-// request's CTAs are first..last; with fewer blocks than CTAs every non-empty
-// share is a single block, so block k sits in cta_of(preq + k).  Afterwards,
-// requests with no blocks at all (in no share) are spread over the CTAs.
+// One request of the merge warp (below), lane n owning row n: fold the NL
+// handed-over lists of each row (H: [NL][TK][32 rows]), then either write
+// the rows (a request held by this CTA alone) or publish the lists and take
+// the request's ticket, the last of its CTAs merging every CTA's lists and
+// writing the rows.  With total >= grid every share is non-empty, so the
+// request's CTAs are first..last; with fewer blocks than CTAs every
+// non-empty share is a single block, so block k sits in cta_of(preq + k).
+//
+// The other CTAs' lists are loaded all at once, one (row, CTA) pair per lane
+// (G sources per round), and folded with a shuffle tree; 32-key lists fold
+// one source per round (a second list would not fit the registers).
+//
+// dry: the same instructions on the same path with no global access at all
+// (no loads, stores or ticket; `split` picks the path).  The merge of a split
+// request is often the last work of the last CTA of the batch; a dry run at
+// kernel start brings this code into the instruction cache, where its first
+// real run would otherwise wait on instruction fetches at every step.
+template <int TK, int NL>
+__device__ __noinline__ void merge_request(const DecodeArgs& a, int req, int nb, long long preq,
+                                           long long total, const uint64_t* H, int lane,
+                                           bool dry, bool split) {
+  const int n = lane;
+  const int R = a.rows_per_req;
+  const int G = TK <= 16 ? max(1, 32 / R) : 1;
+  const int my_row = lane % R, my_src = lane / R;
+  const int first = cta_of(preq, total, gridDim.x);
+  const int last = cta_of(preq + nb - 1, total, gridDim.x);
+  const bool dense = total >= gridDim.x;
+  const int nseg = dry ? (split ? 2 : 1) : (dense ? last - first + 1 : nb);
+  const int j = n < R ? n / a.heads : 0, h = n < R ? n - j * a.heads : 0;
+  const int pr = (dry ? a.max_seq_len : req_len(a, req)) - a.query_len + j;
+  const int cr = pr >= 0 ? (pr >> 7) : -1;
+  int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
+  const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
+  RegList<TK> list;
+  list.clear();
+  if (n < R) {
+#pragma unroll
+    for (int k = 0; k < TK; ++k) list.v[k] = H[k * kLanes + n];
+#pragma unroll
+    for (int l = 1; l < NL; ++l) {
+      uint64_t other[TK];
+#pragma unroll
+      for (int k = 0; k < TK; ++k) other[k] = H[(l * TK + k) * kLanes + n];
+      list.merge_sorted(other);
+    }
+  }
+  if (nseg == 1) {
+    // Lane n writes row n: forced blocks, the best picks in ascending id
+    // order (a sorting network over the TK candidate ids), then -1.
+    if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out, dry);
+    return;
+  }
+  // Split request: publish this CTA's lists, then take a ticket.  The
+  // ticket wraps to zero on the last arrival, ready for the next call.
+  if (n < R && !dry) {
+    ulonglong2* dst = reinterpret_cast<ulonglong2*>(
+        a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
+#pragma unroll
+    for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
+  }
+  // The warp barrier orders the lanes' list stores before lane 0's release;
+  // lane 0's acquire, then the barrier, orders the merging lanes' reads after
+  // every other CTA's release.  (Full fences around a plain atomicInc
+  // measured 1-2 us slower.)
+  __syncwarp();
+  unsigned int ticket = nseg - 1;
+  if (lane == 0 && !dry)
+    ticket = atomic_inc_acq_rel_gpu(a.tickets + req, static_cast<unsigned int>(nseg - 1));
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  __syncwarp();
+  if (ticket != static_cast<unsigned int>(nseg - 1)) return;
+  for (int base = 0; base < nseg; base += G) {
+    const int js = base + my_src;
+    int cj = -1;
+    if (lane < R * G && js < nseg) cj = dense ? first + js : cta_of(preq + js, total, gridDim.x);
+    RegList<TK> got;
+    if (cj >= 0 && cj != static_cast<int>(blockIdx.x) && !dry) {
+      const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
+          a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + my_row * TK);
+#pragma unroll
+      for (int u = 0; u < TK / 2; ++u) {
+        const ulonglong2 x = __ldcg(src + u);
+        got.v[2 * u] = x.x;
+        got.v[2 * u + 1] = x.y;
+      }
+    } else {
+      got.clear();
+    }
+    for (int w = 1; w < G; w <<= 1) {
+      uint64_t o[TK];
+#pragma unroll
+      for (int k = 0; k < TK; ++k) o[k] = __shfl_down_sync(0xffffffffu, got.v[k], R * w);
+      // Lanes whose source index is a multiple of 2w take their partner's
+      // list (sources past G hold empty lists).
+      if ((my_src & (2 * w - 1)) == 0 && my_src + w < G) got.merge_sorted(o);
+    }
+    if (n < R) list.merge_sorted(got.v);
+  }
+  if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out, dry);
+}
+
+// Requests with no blocks at all appear in no share: their rows are spread
+// over the CTAs, one warp each (-inf scores or -1 ids).
+__device__ __forceinline__ void fill_empty_requests(const DecodeArgs& a, int lane) {
+  const int R = a.rows_per_req;
+  for (int i = blockIdx.x; i < a.num_reqs; i += gridDim.x) {
+    if (req_blocks(a, i) != 0) continue;
+    if (a.mode != kModeSelect) {
+      const int w = a.fill_width;
+      for (int idx = lane; idx < R * w; idx += 32) {
+        const int rr = idx / w, bb = idx - rr * w;
+        const int j = rr / a.heads, h = rr - j * a.heads;
+        a.score[h * a.s_head + (static_cast<int64_t>(i) * a.query_len + j) * a.s_row + bb] =
+            -INFINITY;
+      }
+    } else {
+      for (int idx = lane; idx < R * a.topk; idx += 32) {
+        const int rr = idx / a.topk, k = idx - rr * a.topk;
+        const int j = rr / a.heads, h = rr - j * a.heads;
+        a.ids[h * a.i_head + (static_cast<int64_t>(i) * a.query_len + j) * a.i_row + k] = -1;
+      }
+    }
+  }
+}
+
+// The merge warp: merge_request for every request of this CTA's share, in
+// the walker's order, as the scoring warps hand their lists over (hand-over
+// slot seg & 1); afterwards, the requests with no blocks.
 template <int TK, int NL>
 __device__ void merge_warp(const DecodeArgs& a, Walker walker, long long total, uint64_t* sHand,
                            uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                            int lane) {
-  const int n = lane;
-  const int R = a.rows_per_req;
   const bool select = a.mode == kModeSelect;
+  if (select) {
+    // Dry runs of both paths while the first lists are still being scored.
+    merge_request<TK, NL>(a, 0, 1, 0, 1, sHand, lane, true, false);
+    merge_request<TK, NL>(a, 0, 1, 0, 1, sHand, lane, true, true);
+  }
   int seg = 0;
   bool ok = true;
   int req, b0, b1, nb;
@@ -260,96 +383,13 @@ __device__ void merge_warp(const DecodeArgs& a, Walker walker, long long total, 
       ok = false;
       break;
     }
-    RegList<TK> list;
-    list.clear();
-    if (n < R) {
-      const uint64_t* H = sHand + hs * NL * TK * kLanes;
-#pragma unroll
-      for (int k = 0; k < TK; ++k) list.v[k] = H[k * kLanes + n];
-#pragma unroll
-      for (int l = 1; l < NL; ++l) {
-        uint64_t other[TK];
-#pragma unroll
-        for (int k = 0; k < TK; ++k) other[k] = H[(l * TK + k) * kLanes + n];
-        list.merge_sorted(other);
-      }
-    }
-    const int first = cta_of(preq, total, gridDim.x);
-    const int last = cta_of(preq + nb - 1, total, gridDim.x);
-    const bool dense = total >= gridDim.x;
-    const int nseg = dense ? last - first + 1 : nb;
-    const int j = n < R ? n / a.heads : 0, h = n < R ? n - j * a.heads : 0;
-    const int pr = req_len(a, req) - a.query_len + j;
-    const int cr = pr >= 0 ? (pr >> 7) : -1;
-    int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
-    if (nseg == 1) {
-      // Lane n writes row n: forced blocks, the best picks in ascending id
-      // order (a sorting network over the TK candidate ids), then -1.
-      if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
-    } else {
-      // Split request: publish this CTA's lists, then take a ticket.  The
-      // ticket wraps to zero on the last arrival, ready for the next call.
-      const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
-      if (n < R) {
-        ulonglong2* dst = reinterpret_cast<ulonglong2*>(
-            a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
-#pragma unroll
-        for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
-      }
-      // The warp barrier orders the lanes' list stores before lane 0's
-      // release; lane 0's acquire, then the barrier, orders the merging
-      // lanes' reads after every other CTA's release.  (Full fences around
-      // a plain atomicInc measured 1-2 us slower.)
-      __syncwarp();
-      unsigned int ticket = 0;
-      if (lane == 0)
-        ticket = atomic_inc_acq_rel_gpu(a.tickets + req, static_cast<unsigned int>(nseg - 1));
-      ticket = __shfl_sync(0xffffffffu, ticket, 0);
-      __syncwarp();
-      if (ticket == static_cast<unsigned int>(nseg - 1)) {
-        if (n < R) {
-          for (int js = 0; js < nseg; ++js) {
-            const int cj = dense ? first + js : cta_of(preq + js, total, gridDim.x);
-            if (cj == static_cast<int>(blockIdx.x)) continue;
-            const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
-                a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + n * TK);
-            uint64_t other[TK];
-#pragma unroll
-            for (int u = 0; u < TK / 2; ++u) {
-              const ulonglong2 x = __ldcg(src + u);
-              other[2 * u] = x.x;
-              other[2 * u + 1] = x.y;
-            }
-            list.merge_sorted(other);
-          }
-          write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out);
-        }
-      }
-    }
+    merge_request<TK, NL>(a, req, nb, preq, total, sHand + hs * NL * TK * kLanes, lane, false,
+                          false);
     __syncwarp();
     if (lane == 0) mbar_arrive(&h_empty[hs]);
     ++seg;
   }
-  if (ok) {
-    for (int i = blockIdx.x; i < a.num_reqs; i += gridDim.x) {
-      if (req_blocks(a, i) != 0) continue;
-      if (!select) {
-        const int w = a.fill_width;
-        for (int idx = lane; idx < R * w; idx += 32) {
-          const int rr = idx / w, bb = idx - rr * w;
-          const int j = rr / a.heads, h = rr - j * a.heads;
-          a.score[h * a.s_head + (static_cast<int64_t>(i) * a.query_len + j) * a.s_row + bb] =
-              -INFINITY;
-        }
-      } else {
-        for (int idx = lane; idx < R * a.topk; idx += 32) {
-          const int rr = idx / a.topk, k = idx - rr * a.topk;
-          const int j = rr / a.heads, h = rr - j * a.heads;
-          a.ids[h * a.i_head + (static_cast<int64_t>(i) * a.query_len + j) * a.i_row + k] = -1;
-        }
-      }
-    }
-  }
+  if (ok) fill_empty_requests(a, lane);
 }
 
 // Score mode, once a request's last block has been scored: -inf for its

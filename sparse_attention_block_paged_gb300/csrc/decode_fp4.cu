@@ -3,41 +3,40 @@
 // the fp32 scores written out (score mode) or a fused top-k selector (select
 // mode).  Each key element is e4m3_rn_satfinite(e2m1 code * e4m3 scale), one
 // scale per 16 elements (vLLM MiniMax-M3 "indexer_nvfp4" page, module
-// docstring); the scoring and selection rules are the bf16 kernel's
-// (decode.cu), and so are the partition, walker and merge warp
-// (decode_common.cuh).
+// docstring); every such value is exact in bf16, so the page is dequantised
+// to bf16 and scored on the tensor cores against the bf16 query rows exactly
+// as the bf16 kernel (decode.cu) scores bf16 pages, with the same partition,
+// walker and merge warp (decode_common.cuh).
 //
-// The dequantised page never goes through shared memory: it is written into
-// tensor memory and is the MMA's A operand there (tokens on the 128 TMEM
-// lanes, K = 128 elements in 64 columns of bf16 pairs), with the request's
-// query rows as B (N = 16 or 32 rows, K-major in shared memory).  A page is
-// then read from shared memory once, as 9 KB of codes and scales, and the
-// accumulator holds one token per lane and one query row per column, so a
-// block's max is a max across lanes.
+// A tcgen05.mma instruction costs about the same time whatever its N, and a
+// page needs eight of them (K = 128 in steps of 16), so the instruction rate
+// bounds the kernel long before HBM does; each MMA therefore takes two pages
+// (N = 256 key tokens) with the query rows as A (M = 128).
 //
-//   * warp 4     : producer.  Per page, one TMA tiled copy of the 8 KB of
-//                  codes (64-byte swizzle, so that the dequantisers' per-token
-//                  loads hit distinct banks) and one bulk copy of the 1 KB of
-//                  scales into a ring of raw stages; the query rows of each
-//                  request into a swizzled B tile.
-//   * warps 8+   : dequantisers, in groups of four (one per TMEM lane
-//                  quadrant); group g takes the pages it % groups == g.  A
-//                  thread owns one token: 64 code bytes, 8 scale bytes, a
-//                  per-scale table lookup (eight copies of the table, so the
-//                  eight lanes of a shared-memory phase read eight distinct
-//                  banks) and byte permutes give its 128 bf16 values, stored
-//                  with tcgen05.st into one of four TMEM A buffers.
-//   * warp 5     : one thread issues tcgen05.mma, A from TMEM, B = query rows,
-//                  into one of four 32-column fp32 accumulators.
-//   * warps 0-3  : epilogue, one per lane quadrant.  Loads its 32 tokens x N
-//                  rows with tcgen05.ld, masks the causal tail per row and
-//                  reduces each row across its 32 lanes (redux max); the four
-//                  quadrant maxima go to shared memory.
-//   * warp 6     : selector.  Lane n = query row n: the row's block score is
-//                  the max of the four quadrant maxima times sm_scale; it is
-//                  stored (score mode) or offered to the row's candidate list,
-//                  handed to the merge warp at the end of each request.
-//   * warp 7     : merge warp (decode_common.cuh).
+//   * warp 2   : producer.  Per page, one TMA tiled copy of the 8 KB of codes
+//                (64-byte swizzle, so that the dequantisers' per-token loads
+//                hit distinct banks) and one bulk copy of the 1 KB of scales
+//                into a ring of raw stages, the pages further ahead pulled
+//                into L2 first; the query rows of each request into the Q
+//                tile.
+//   * warps 3+ : dequantisers, two groups of four; group g takes page g of
+//                each two-page unit.  A thread owns one token: 64 code bytes,
+//                8 scale bytes, a per-scale table lookup (copies of the table
+//                side by side spread the lanes' lookups over the banks) and
+//                byte permutes give its 128 bf16 values, stored straight into
+//                the unit's slot in the 128-byte-swizzled K-major layout of
+//                the MMA's B operand (the eight lanes of a store phase hit
+//                eight distinct 16-byte bank groups).
+//   * warp 1   : one thread issues tcgen05.mma, A = query rows, B = the
+//                unit's slot (N = 256, or 128 for a request's last odd
+//                block), into one of two 256-column fp32 accumulators.
+//   * warp 0   : epilogue: lane n = query row n takes its row's causal block
+//                max of both blocks of each unit (decode.cu's epilogue), and
+//                at the end of each request merges its candidate lists itself
+//                (decode_common.cuh, merge_request): with one or two requests
+//                per CTA this stalls the pipeline rarely, and the shared
+//                memory of a hand-over and the registers of a merge warp go
+//                to a deeper raw ring instead.
 //
 // Every wait is bounded (ptx.cuh); a wait that gives up raises the CTA's
 // abort flag and MM3IDX_DEV_TIMEOUT.
@@ -54,41 +53,55 @@ using namespace dec;
 constexpr int kCodeBytes = kBlock * kD / 2;    // 8 KB: 128 tokens x 64 B
 constexpr int kScaleBytes = kBlock * kD / 16;  // 1 KB: 128 tokens x 8 B
 constexpr int kRawStride = 10240;              // codes (1024-aligned), scales, pad
-constexpr int kABufs = 4;                      // dequantised pages in TMEM
-constexpr int kACols = 64;                     // 128 bf16 per lane
-constexpr int kDBufs = 4;                      // accumulators
-constexpr int kDCols = 32;
-constexpr int kDCol0 = kABufs * kACols;        // accumulators after the A buffers
-constexpr uint32_t kTmemCols = 512;
-constexpr int kTabCopies = 8;
-constexpr int kProdWarp = 4, kMmaWarp = 5, kSelWarp = 6, kMergeWarp = 7, kDeqWarp0 = 8;
-static_assert(kDCol0 + kDBufs * kDCols <= static_cast<int>(kTmemCols), "TMEM budget");
+constexpr int kAccBufs = 2;
+constexpr int kAccCols = 256;                  // a unit of two pages
+constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
+constexpr int kHalfPage = kBlock * 64 * 2;     // 128 rows x 64 bf16 = 16 KB
+constexpr int kSlotHalf = 2 * kHalfPage;       // one 64-column half of a two-page slot
+constexpr int kEpiWarp = 0, kMmaWarp = 1, kProdWarp = 2, kDeqWarp0 = 3;
+constexpr int kThreads = (kDeqWarp0 + 8) * 32;
+constexpr int MQ = 128;                        // query tile rows (the M = 128 layout)
+constexpr int kAhead = 16;                     // pages pulled into L2 ahead of the ring (< 32)
 
-// NQ: query rows in the B tile (16 or 32); DG: dequantiser groups.
-template <int NQ, int TK, int DG>
+// The warp pulls one page's codes (64 lines of 128 B) and scales (8 lines)
+// into L2, two or three lines per lane.
+__device__ __forceinline__ void prefetch_page_l2(const DecodeArgs& a, int page, int lane) {
+  const uint8_t* c = a.codes + static_cast<int64_t>(page) * kCodeBytes;
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + lane * 128));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + (lane + 32) * 128));
+  if (lane < kScaleBytes / 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.scales + static_cast<int64_t>(page) * kScaleBytes +
+                                                   lane * 128));
+}
+
+// Shared memory: the two-page slots as two regions, one per 64-column half
+// ([slot][page][128 rows][128 B] each), the Q tile, the raw ring, the table,
+// the epilogue's lists for its merges.  32-key lists take one raw stage less.
+template <int TK>
 struct Cfg {
-  static constexpr int kWarps = kDeqWarp0 + 4 * DG;
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kRawStages = 12;
-  static constexpr int kQBytes = NQ * kD * 2;
-  static constexpr int oRaw = 0;
-  static constexpr int oTab = oRaw + kRawStages * kRawStride;  // [256 scales][8 copies] x 16 B
-  static constexpr int oQ = oTab + 256 * kTabCopies * 16;
-  static constexpr int oPart = oQ + 2 * kQBytes;               // [kDBufs][4 quadrants][32] fp32
-  static constexpr int oHand = oPart + kDBufs * 4 * 32 * 4;    // [2 slots][TK][32] keys
-  static constexpr int oBar = oHand + 2 * TK * kLanes * 8;
-  static constexpr int kBars = 2 * kRawStages + 2 * kABufs + 4 * kDBufs + 4 + 4 + 1;
+  static constexpr int kPairs = 2;
+  static constexpr int kRawStages = TK == 16 ? 5 : 4;
+  static constexpr int kTabCopies = 2;
+  static constexpr int kQBytes = MQ * kD * 2;
+  static constexpr int oH0 = 0;
+  static constexpr int oH1 = oH0 + kPairs * kSlotHalf;
+  static constexpr int oQ = oH1 + kPairs * kSlotHalf;
+  static constexpr int oRaw = oQ + kQBytes;
+  static constexpr int oTab = oRaw + kRawStages * kRawStride;   // [256 scales][copies] x 16 B
+  static constexpr int oList = oTab + 256 * kTabCopies * 16;    // [TK][32] keys
+  static constexpr int oBar = oList + TK * kLanes * 8;
+  static constexpr int kBars = 2 * kRawStages + 2 * kPairs + 2 * kAccBufs + 2 + 1;
   static constexpr int oMisc = oBar + kBars * 8;
   static constexpr int kSmem = oMisc + 64 + 1024;
-  static_assert(oTab % 1024 == 0 && oQ % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  static_assert(oQ % 1024 == 0 && oRaw % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
 // Per-scale-byte magnitude table: for scale byte s, the bf16 bits of
 // e4m3_rn_satfinite(m * e4m3(s)) for the eight e2m1 magnitudes
 // m = 0, .5, 1, 1.5, 2, 3, 4, 6, as low bytes (words 0-1) and high bytes
-// (words 2-3) for byte-permute lookups; kTabCopies copies side by side.
-__device__ void build_fp4_table(uint4* tab, int tid, int nthreads) {
+// (words 2-3) for byte-permute lookups; `copies` copies side by side.
+__device__ void build_fp4_table(uint4* tab, int copies, int tid, int nthreads) {
   const float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
   for (int s = tid; s < 256; s += nthreads) {
     const __half_raw sh = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(s), __NV_E4M3);
@@ -104,8 +117,7 @@ __device__ void build_fp4_table(uint4* tab, int tid, int nthreads) {
       hi[k >> 2] |= ((bits >> 8) & 0xFFu) << ((k & 3) * 8);
     }
     const uint4 v = make_uint4(lo[0], lo[1], hi[0], hi[1]);
-#pragma unroll
-    for (int c = 0; c < kTabCopies; ++c) tab[s * kTabCopies + c] = v;
+    for (int c = 0; c < copies; ++c) tab[s * copies + c] = v;
   }
 }
 
@@ -124,7 +136,7 @@ __device__ __forceinline__ uint32_t xor_signs(uint32_t a, uint32_t b) {
 
 // Eight e2m1 codes (nibble k = element k, sign in bit 3) -> four bf16x2
 // words (element 2i in the low half of word i).
-__device__ __forceinline__ void dequant8(uint32_t codes, const uint4& t, uint32_t* o) {
+__device__ __forceinline__ uint4 dequant8(uint32_t codes, const uint4& t) {
   const uint32_t sel0 = codes & 0x7777u;
   const uint32_t sel1 = (codes >> 16) & 0x7777u;
   const uint32_t lo0 = prmt(t.x, t.y, sel0), hi0 = prmt(t.z, t.w, sel0);
@@ -134,38 +146,70 @@ __device__ __forceinline__ void dequant8(uint32_t codes, const uint4& t, uint32_
   const uint32_t c4 = codes << 4;
   const uint32_t s0 = prmt(c4, codes, 0x5140u), s1 = prmt(c4, codes, 0x7362u);
   const uint32_t h0 = xor_signs(hi0, s0), h1 = xor_signs(hi1, s1);
-  o[0] = prmt(lo0, h0, 0x5140u);
-  o[1] = prmt(lo0, h0, 0x7362u);
-  o[2] = prmt(lo1, h1, 0x5140u);
-  o[3] = prmt(lo1, h1, 0x7362u);
+  return make_uint4(prmt(lo0, h0, 0x5140u), prmt(lo0, h0, 0x7362u), prmt(lo1, h1, 0x5140u),
+                    prmt(lo1, h1, 0x7362u));
 }
 
-template <int NQ, int TK, int DG>
-__global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Row max of one block's 128 accumulator columns (this lane's TMEM lane),
+// with the columns past `lim` left out when lim < 127.
+__device__ __forceinline__ float acc_row_max(uint32_t taddr, int lim) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int c0 = 0; c0 < kBlock; c0 += 64) {
+    uint32_t v[32], w[32];
+    tmem_ld32(taddr + c0, v);
+    tmem_ld32(taddr + c0 + 32, w);
+    tmem_ld_wait32x2(v, w);
+    if (lim >= 127) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        m0 = fmax3(m0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+        m1 = fmax3(m1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
+        m0 = fmax3(m0, __uint_as_float(w[k]), __uint_as_float(w[k + 1]));
+        m1 = fmax3(m1, __uint_as_float(w[k + 2]), __uint_as_float(w[k + 3]));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
+        if (c0 + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(w[k]));
+      }
+    }
+  }
+  return fmaxf(m0, m1);
+}
+
+template <int TK>
+__global__ void __launch_bounds__(kThreads, 1)
     decode_fp4_kernel(const __grid_constant__ CUtensorMap cmap, const DecodeArgs a) {
-  using C = Cfg<NQ, TK, DG>;
+  using C = Cfg<TK>;
   constexpr int RS = C::kRawStages;
+  constexpr int P = C::kPairs;
+  constexpr int NC = C::kTabCopies;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
+  uint8_t* sH0 = sm + C::oH0;
+  uint8_t* sH1 = sm + C::oH1;
+  uint8_t* sQ = sm + C::oQ;
   uint8_t* sRaw = sm + C::oRaw;
   const uint4* sTab = reinterpret_cast<const uint4*>(sm + C::oTab);
-  uint8_t* sQ = sm + C::oQ;
-  float* sPart = reinterpret_cast<float*>(sm + C::oPart);
-  uint64_t* sHand = reinterpret_cast<uint64_t*>(sm + C::oHand);
+  uint64_t* sList = reinterpret_cast<uint64_t*>(sm + C::oList);
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + C::oBar);
   uint64_t* raw_empty = raw_full + RS;
-  uint64_t* a_full = raw_empty + RS;
-  uint64_t* a_empty = a_full + kABufs;
-  uint64_t* acc_full = a_empty + kABufs;
-  uint64_t* acc_empty = acc_full + kDBufs;
-  uint64_t* red_full = acc_empty + kDBufs;
-  uint64_t* red_empty = red_full + kDBufs;
-  uint64_t* q_full = red_empty + kDBufs;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* h_full = q_empty + 2;
-  uint64_t* h_empty = h_full + 2;
-  uint64_t* done_bar = h_empty + 2;
+  uint64_t* slot_full = raw_empty + RS;    // both dequantiser groups wrote the unit
+  uint64_t* slot_empty = slot_full + P;    // the unit's MMAs are done with the slot
+  uint64_t* acc_full = slot_empty + P;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* q_full = acc_empty + kAccBufs;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* done_bar = q_empty + 1;
   Misc* misc = reinterpret_cast<Misc*>(sm + C::oMisc);
   volatile int* abort_flag = &misc->abort;
 
@@ -176,22 +220,16 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], 4);
     }
-    for (int s = 0; s < kABufs; ++s) {
-      mbar_init(&a_full[s], 4);
-      mbar_init(&a_empty[s], 1);
+    for (int s = 0; s < P; ++s) {
+      mbar_init(&slot_full[s], 8);
+      mbar_init(&slot_empty[s], 1);
     }
-    for (int s = 0; s < kDBufs; ++s) {
+    for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
-      mbar_init(&red_full[s], 4);
-      mbar_init(&red_empty[s], 1);
+      mbar_init(&acc_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
-      mbar_init(&h_full[s], 1);
-      mbar_init(&h_empty[s], 1);
-    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     mbar_init(done_bar, 1);
     misc->abort = 0;
     fence_barrier_init();
@@ -200,7 +238,7 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
     tmem_alloc(&misc->tmem, kTmemCols);
     tmem_relinquish();
   }
-  build_fp4_table(reinterpret_cast<uint4*>(sm + C::oTab), threadIdx.x, C::kThreads);
+  build_fp4_table(reinterpret_cast<uint4*>(sm + C::oTab), NC, threadIdx.x, kThreads);
   // Programmatic dependent launch: the set-up above overlaps the previous
   // kernel on the stream; its results are read only after this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -208,7 +246,7 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
   if (warp == kProdWarp) {
     if (lane == 0) prefetch_tensormap(&cmap);
     partition(a, misc, lane);
-  } else if (warp == kMergeWarp) {
+  } else if (warp == kEpiWarp) {
     prefetch_table_and_queries(a, lane);
   }
   tc_fence_before();
@@ -225,30 +263,46 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     int seg = 0;
-    uint32_t it = 0;
+    uint32_t it = 0;  // pages issued
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      const int slot = seg & 1;
-      if (seg >= 2) ok = warp_wait(&q_empty[slot], ((seg >> 1) - 1) & 1, abort_flag);
-      if (!ok) break;
+      // One Q tile: it is rewritten once the previous request's MMAs are
+      // done, just before the first wait that could block, so that page
+      // loads are already in flight meanwhile.
       bool q_pending = true;
       auto put_q = [&]() {
-        load_q_tile<NQ>(a, req, sQ + slot * C::kQBytes, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full[slot]);
+        if (seg > 0) ok = warp_wait(q_empty, (seg - 1) & 1, abort_flag);
+        if (ok) {
+          load_q_tile<MQ>(a, req, sQ, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(q_full);
+        }
         q_pending = false;
       };
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
+      // Page ids 32 at a time (one per lane), the next 32 read one chunk
+      // early.  The request's first kAhead pages are pulled into L2 here,
+      // and page k + kAhead when page k is issued, so that the copies into
+      // the ring mostly find their pages in L2.
+      int pg_next = b0 + lane < b1 ? __ldg(trow + b0 + lane) : -1;
+      for (int k = 0; k < kAhead; ++k) {
+        const int p = __shfl_sync(0xffffffffu, pg_next, k);
+        if (p >= 0 && p < a.num_pages) prefetch_page_l2(a, p, lane);
+      }
       for (int bc = b0; bc < b1 && ok; bc += 32) {
-        const int mine = bc + lane;
-        const int pg = mine < b1 ? __ldg(trow + mine) : 0;
+        const int pg = pg_next;
+        pg_next = bc + 32 + lane < b1 ? __ldg(trow + bc + 32 + lane) : -1;
         const int nblk = min(32, b1 - bc);
         for (int k = 0; k < nblk; ++k) {
           const int page = __shfl_sync(0xffffffffu, pg, k);
+          const int ka = k + kAhead;
+          const int ahead = __shfl_sync(0xffffffffu, ka < 32 ? pg : pg_next, ka & 31);
+          if (ahead >= 0 && ahead < a.num_pages) prefetch_page_l2(a, ahead, lane);
           const bool good = page >= 0 && page < a.num_pages;
           const uint32_t st = it % RS, rnd = it / RS;
           if (rnd > 0 && q_pending) put_q();
+          if (!ok) break;
           if (rnd > 0) ok = warp_wait(&raw_empty[st], (rnd - 1) & 1, abort_flag);
           if (!ok) break;
           if (lane == 0) {
@@ -260,7 +314,7 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
                         kScaleBytes, &raw_full[st], pol);
             } else {
               // Not loaded: the stage's stale bytes are dequantised and
-              // scored, and the selector gives the block -inf.
+              // scored, and the epilogue gives the block -inf.
               atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
               mbar_arrive(&raw_full[st]);
             }
@@ -269,7 +323,7 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
           ++it;
         }
       }
-      if (q_pending) put_q();
+      if (ok && q_pending) put_q();
       ++seg;
     }
     // Let every copy this warp started land before the CTA can exit.
@@ -284,100 +338,103 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
     __syncwarp();
   } else if (warp >= kDeqWarp0) {
     // --------------------------------------------------------- dequantisers
-    const int group = (warp - kDeqWarp0) >> 2;
-    const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
-    const int tok = quad * 32 + lane;    // this thread's token of the page
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    const int swz = (tok >> 1) & 3;      // 64-byte swizzle of the code rows
-    const int copy = lane & (kTabCopies - 1);
-    uint32_t it = 0;
+    const int group = (warp - kDeqWarp0) >> 2;   // which page of each unit
+    const int tok = ((warp - kDeqWarp0) & 3) * 32 + lane;
+    const int swz = (tok >> 1) & 3;                // 64-byte swizzle of the code rows
+    const int copy = lane % NC;
+    // This token's rows in the two halves of a slot (128-byte swizzle).
+    const uint32_t row_off = group * kHalfPage + (tok >> 3) * 1024 + (tok & 7) * 128;
+    uint32_t it = 0, ut = 0;  // pages and units so far
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      for (int b = b0; b < b1; ++b, ++it) {
-        if (static_cast<int>(it % DG) != group) continue;
-        const uint32_t rs = it % RS, rr = it / RS;
-        const uint32_t ab = it % kABufs, ar = it / kABufs;
+      for (int bu = b0; bu < b1; bu += 2, ++ut) {
+        const bool two = bu + 1 < b1;
+        const bool mine = group == 0 || two;
+        const uint32_t pit = it + group;           // this group's page of the unit
+        it += two ? 2 : 1;
+        const uint32_t st = ut % P, sr = ut / P;
+        const uint32_t rs = pit % RS, rr = pit / RS;
         bool got = true;
         if (lane == 0) {
-          got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
-          if (got && ar > 0) got = mbar_wait(&a_empty[ab], (ar - 1) & 1, abort_flag);
+          if (mine) got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
+          // The slot's previous unit must be consumed before this group
+          // writes it or counts towards its next phase.
+          if (got && sr > 0) got = mbar_wait(&slot_empty[st], (sr - 1) & 1, abort_flag);
         }
         if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
-        // Every lane observes the completed phase itself before reading what
-        // the copies wrote (the stage cannot move on before this warp frees it).
-        mbar_try_wait(&raw_full[rs], rr & 1);
-        tc_fence_after();
-        const uint8_t* raw = sRaw + rs * kRawStride;
-        const uint8_t* crow = raw + tok * 64;
-        uint4 cw[4];
+        if (mine) {
+          // Every lane observes the completed phase itself before reading
+          // what the copies wrote.
+          mbar_try_wait(&raw_full[rs], rr & 1);
+          const uint8_t* raw = sRaw + rs * kRawStride;
+          const uint8_t* crow = raw + tok * 64;
+          uint4 cw[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cw[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ swz) << 4));
-        const uint2 scw = *reinterpret_cast<const uint2*>(raw + kCodeBytes + tok * 8);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+          for (int c = 0; c < 4; ++c) cw[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ swz) << 4));
+          const uint2 scw = *reinterpret_cast<const uint2*>(raw + kCodeBytes + tok * 8);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[rs]);
+          uint8_t* h0 = sH0 + st * kSlotHalf + row_off;
+          uint8_t* h1 = sH1 + st * kSlotHalf + row_off;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          // Elements 64*half .. +63: scale groups 4*half .. +3, code chunks
-          // 2*half, 2*half+1 (two groups, i.e. 16 code bytes, each).
-          const uint32_t sw = half ? scw.y : scw.x;
-          uint4 t[4];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) t[g] = sTab[((sw >> (8 * g)) & 0xFFu) * kTabCopies + copy];
-          uint32_t o[32];
-          const uint4 c0 = cw[2 * half], c1 = cw[2 * half + 1];
-          dequant8(c0.x, t[0], o + 0);
-          dequant8(c0.y, t[0], o + 4);
-          dequant8(c0.z, t[1], o + 8);
-          dequant8(c0.w, t[1], o + 12);
-          dequant8(c1.x, t[2], o + 16);
-          dequant8(c1.y, t[2], o + 20);
-          dequant8(c1.z, t[3], o + 24);
-          dequant8(c1.w, t[3], o + 28);
-          tmem_st32(t_lane + ab * kACols + 32 * half, o);
+          for (int g = 0; g < 8; ++g) {
+            // Scale group g: elements 16g .. 16g+15, code words 2g, 2g+1,
+            // output chunks 2g, 2g+1 (8 elements each) of the 16 in the row.
+            const uint32_t sb = ((g < 4 ? scw.x : scw.y) >> (8 * (g & 3))) & 0xFFu;
+            const uint4 t = sTab[sb * NC + copy];
+            const uint4 c = cw[g >> 1];
+            const uint32_t w0 = (g & 1) ? c.z : c.x, w1 = (g & 1) ? c.w : c.y;
+            uint8_t* hb = g < 4 ? h0 : h1;
+            const int c0 = (2 * g) & 7, c1 = (2 * g + 1) & 7;
+            *reinterpret_cast<uint4*>(hb + ((c0 ^ (tok & 7)) << 4)) = dequant8(w0, t);
+            *reinterpret_cast<uint4*>(hb + ((c1 ^ (tok & 7)) << 4)) = dequant8(w1, t);
+          }
+          fence_proxy_async_smem();
         }
-        tmem_st_wait();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[ab]);
+        if (lane == 0) mbar_arrive(&slot_full[st]);
       }
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, NQ);
+      constexpr uint32_t idesc2 = idesc_bf16_f32(MQ, 2 * kBlock);
+      constexpr uint32_t idesc1 = idesc_bf16_f32(MQ, kBlock);
+      const uint32_t qaddr = smem_u32(sQ);
       int seg = 0;
-      uint32_t it = 0;
+      uint32_t ut = 0;
       bool ok = true;
       while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-        const int slot = seg & 1;
-        ok = mbar_wait(&q_full[slot], (seg >> 1) & 1, abort_flag);
+        ok = mbar_wait(q_full, seg & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qaddr = smem_u32(sQ + slot * C::kQBytes);
-        for (int b = b0; b < b1; ++b) {
-          const uint32_t aa = it % kABufs, ar = it / kABufs;
-          ok = mbar_wait(&a_full[aa], ar & 1, abort_flag);
+        for (int b = b0; b < b1; b += 2) {
+          const bool two = b + 1 < b1;
+          const uint32_t st = ut % P, rnd = ut / P;
+          ok = mbar_wait(&slot_full[st], rnd & 1, abort_flag);
           if (!ok) break;
-          const uint32_t db = it % kDBufs, dr = it / kDBufs;
-          if (dr > 0) ok = mbar_wait(&acc_empty[db], (dr - 1) & 1, abort_flag);
+          const uint32_t ab = ut % kAccBufs, ar = ut / kAccBufs;
+          if (ar > 0) ok = mbar_wait(&acc_empty[ab], (ar - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d = tmem_base + kDCol0 + db * kDCols;
-          const uint32_t at = tmem_base + aa * kACols;
+          const uint32_t k0 = smem_u32(sH0 + st * kSlotHalf), k1 = smem_u32(sH1 + st * kSlotHalf);
+          const uint32_t d = tmem_base + ab * kAccCols;
+          const uint32_t idesc = two ? idesc2 : idesc1;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint64_t bd = sdesc_kmajor_sw128(qaddr + (k >> 2) * (NQ * 128) + (k & 3) * 32);
-            mma_bf16_ts(d, at + 8 * k, bd, idesc, k > 0 ? 1u : 0u);
+            const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (MQ * 128) + (k & 3) * 32);
+            const uint64_t bd = sdesc_kmajor_sw128((k < 4 ? k0 : k1) + (k & 3) * 32);
+            mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
           }
-          mma_commit(&a_empty[aa]);
-          mma_commit(&acc_full[db]);
-          ++it;
+          mma_commit(&slot_empty[st]);
+          mma_commit(&acc_full[ab]);
+          ++ut;
         }
         if (!ok) break;
-        mma_commit(&q_empty[slot]);
+        mma_commit(q_empty);
         ++seg;
       }
       // Wait until every MMA issued above has finished before TMEM is freed.
@@ -386,75 +443,21 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
       mbar_wait(done_bar, 0, &dummy);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp == kEpiWarp) {
     // ------------------------------------------------------------- epilogue
-    const int quad = warp;
-    const int tok = quad * 32 + lane;
-    const int R = a.rows_per_req;
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    uint32_t it = 0;
-    bool ok = true;
-    while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      // Row n (query j = n / heads) sees token t of block b iff
-      // 128 b + t <= seq - query_len + j.
-      const int first_pos = req_len(a, req) - a.query_len;
-      for (int b = b0; b < b1; ++b, ++it) {
-        const uint32_t db = it % kDBufs, dr = it / kDBufs;
-        if (!warp_wait(&acc_full[db], dr & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t v[NQ];
-        if constexpr (NQ == 16) {
-          tmem_ld16(t_lane + kDCol0 + db * kDCols, v);
-          tmem_ld_wait16(v);
-        } else {
-          tmem_ld32(t_lane + kDCol0 + db * kDCols, v);
-          tmem_ld_wait32(v);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[db]);
-        const int lim = first_pos - b * kBlock;  // row n sees tokens 0 .. lim + n / heads
-        float mine = -INFINITY;
-        if (lim >= kBlock - 1) {
-#pragma unroll
-          for (int n = 0; n < NQ; ++n) {
-            if (n < R) {
-              const float m = warp_max_f32(__uint_as_float(v[n]));
-              if (lane == n) mine = m;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int n = 0; n < NQ; ++n) {
-            if (n < R) {
-              const bool vis = tok <= lim + n / a.heads;
-              const float m = warp_max_f32(vis ? __uint_as_float(v[n]) : -INFINITY);
-              if (lane == n) mine = m;
-            }
-          }
-        }
-        if (dr > 0 && !warp_wait(&red_empty[db], (dr - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        sPart[(db * 4 + quad) * 32 + lane] = mine;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&red_full[db]);
-      }
-    }
-  } else if (warp == kSelWarp) {
-    // ------------------------------------------------------------- selector
-    const int n = lane;  // query row
+    const int n = lane;                   // query row (TMEM lane)
     const int R = a.rows_per_req;
     const int my_j = n < R ? n / a.heads : 0;
     const int my_h = n < R ? n - my_j * a.heads : 0;
     const bool select = a.mode == kModeSelect;
+    if (select) {
+      // Dry runs of both merge paths (decode_common.cuh) before the first
+      // accumulator is ready.
+      merge_request<TK, 1>(a, 0, 1, 0, 1, sList, lane, true, false);
+      merge_request<TK, 1>(a, 0, 1, 0, 1, sList, lane, true, true);
+    }
     RegList<TK> list;
-    uint32_t it = 0;
-    int seg = 0;
+    uint32_t ut = 0;
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
       const int pos = req_len(a, req) - a.query_len + my_j;
@@ -462,42 +465,51 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
       list.clear();
-      for (int b = b0; b < b1; ++b, ++it) {
-        const int page = __ldg(trow + b);
-        const uint32_t db = it % kDBufs, dr = it / kDBufs;
-        if (!warp_wait(&red_full[db], dr & 1, abort_flag)) {
+      int pg = 0;  // page ids 32 at a time, one per lane (units never straddle two 32s)
+      for (int bu = b0; bu < b1; bu += 2, ++ut) {
+        const bool two = bu + 1 < b1;
+        if (((bu - b0) & 31) == 0) pg = bu + lane < b1 ? __ldg(trow + bu + lane) : 0;
+        const int page0 = __shfl_sync(0xffffffffu, pg, (bu - b0) & 31);
+        const int page1 = __shfl_sync(0xffffffffu, pg, (bu + 1 - b0) & 31);
+        const uint32_t ab = ut % kAccBufs, ar = ut / kAccBufs;
+        if (!warp_wait(&acc_full[ab], ar & 1, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_try_wait(&red_full[db], dr & 1);  // each lane's own acquire of the maxima
-        const float* P = sPart + db * 4 * 32 + n;
-        const float m = fmaxf(fmaxf(P[0], P[32]), fmaxf(P[64], P[96]));
+        tc_fence_after();
+        const float m0 = acc_row_max(tmem_base + ab * kAccCols, pos - bu * kBlock);
+        const float m1 =
+            two ? acc_row_max(tmem_base + ab * kAccCols + kBlock, pos - (bu + 1) * kBlock) : -INFINITY;
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&red_empty[db]);
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
         if (n < R) {
-          const float s = (page >= 0 && page < a.num_pages) ? m * a.sm_scale : -INFINITY;
-          if (!select) {
-            a.score[my_h * a.s_head + row * a.s_row + b] = s;
-          } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
-            list.offer(make_key(s, b));
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int b = bu + e;
+            if (e == 1 && !two) break;
+            const int page = e ? page1 : page0;
+            const float s =
+                (page >= 0 && page < a.num_pages) ? (e ? m1 : m0) * a.sm_scale : -INFINITY;
+            if (!select) {
+              a.score[my_h * a.s_head + row * a.s_row + b] = s;
+            } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
+              list.offer(make_key(s, b));
+            }
           }
         }
       }
       if (!ok) break;
       if (select) {
-        const int hs = seg & 1;
-        if (seg >= 2 && !warp_wait(&h_empty[hs], ((seg >> 1) - 1) & 1, abort_flag)) break;
-        if (n < R) list.store_cols(sHand + hs * TK * kLanes, n);
+        if (n < R) list.store_cols(sList, n);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&h_full[hs]);
+        merge_request<TK, 1>(a, req, nb, preq, total, sList, lane, false, false);
+        __syncwarp();
       } else if (b1 == nb && a.fill_width > nb) {
         fill_past_blocks(a, req, nb, lane);
       }
-      ++seg;
     }
-  } else if (warp == kMergeWarp) {
-    // ------------------------------------------------------------ merge warp
-    merge_warp<TK, 1>(a, walker, total, sHand, h_full, h_empty, abort_flag, lane);
+    if (ok) fill_empty_requests(a, lane);
   }
 
   tc_fence_before();
@@ -509,15 +521,15 @@ __global__ void __launch_bounds__(Cfg<NQ, TK, DG>::kThreads, 1)
   }
 }
 
-template <int NQ, int TK, int DG>
+template <int TK>
 cudaError_t launch_t(const CUtensorMap& cmap, const DecodeArgs& a, int grid, cudaStream_t s) {
-  using C = Cfg<NQ, TK, DG>;
-  cudaError_t e = cudaFuncSetAttribute(decode_fp4_kernel<NQ, TK, DG>,
+  using C = Cfg<TK>;
+  cudaError_t e = cudaFuncSetAttribute(decode_fp4_kernel<TK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(C::kThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -525,20 +537,15 @@ cudaError_t launch_t(const CUtensorMap& cmap, const DecodeArgs& a, int grid, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fp4_kernel<NQ, TK, DG>, cmap, a);
+  return cudaLaunchKernelEx(&cfg, decode_fp4_kernel<TK>, cmap, a);
 }
 
 }  // namespace
 
-// 32-key lists need more registers per thread, so they keep one group of
-// dequantisers (384 threads); 16-key lists take two (512 threads).
 cudaError_t launch_decode_nvfp4(const CUtensorMap& cmap, const DecodeArgs& a, int grid,
                                 cudaStream_t s) {
-  const bool small = a.rows_per_req <= 16, tk16 = decode_tk(a.topk) == 16;
-  if (small && tk16) return launch_t<16, 16, 2>(cmap, a, grid, s);
-  if (small) return launch_t<16, 32, 1>(cmap, a, grid, s);
-  if (tk16) return launch_t<32, 16, 2>(cmap, a, grid, s);
-  return launch_t<32, 32, 1>(cmap, a, grid, s);
+  if (decode_tk(a.topk) == 16) return launch_t<16>(cmap, a, grid, s);
+  return launch_t<32>(cmap, a, grid, s);
 }
 
 }  // namespace mm3idx

@@ -94,12 +94,15 @@ struct RegList {
 
 // One thread writes one output row from its candidate list (keys sorted
 // descending, 0 = none): forced blocks [0, f_lo) and [l_lo, c] around the best
-// topk - |forced| picks, picks in ascending id order, then -1.
+// topk - |forced| picks, picks in ascending id order, then -1.  dry: the same
+// work without the stores.
 template <int TK>
 __device__ __forceinline__ void write_row_lane(const uint64_t (&v)[TK], int c, int init_blocks,
-                                               int local_blocks, int topk, int32_t* out) {
+                                               int local_blocks, int topk, int32_t* out,
+                                               bool dry = false) {
   if (c < 0) {
-    for (int k = 0; k < topk; ++k) out[k] = -1;
+    if (!dry)
+      for (int k = 0; k < topk; ++k) out[k] = -1;
     return;
   }
   const Forced F(c, init_blocks, local_blocks);
@@ -129,6 +132,7 @@ __device__ __forceinline__ void write_row_lane(const uint64_t (&v)[TK], int c, i
       }
     }
   }
+  if (dry) return;
   int o = 0;
   for (int b = 0; b < F.f_lo; ++b) out[o++] = b;
 #pragma unroll
