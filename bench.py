@@ -44,7 +44,9 @@ BLOCK = 128
 L2_BYTES = 129 * 1024 * 1024
 # kernel sources whose hash a committed ncu summary must match for its
 # dram traffic to be reported
-DECODE_SOURCES = ["decode.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
+DECODE_SOURCES = ["decode.cu", "decode_common.cuh", "ptx.cuh", "internal.h", "warp_select.cuh"]
+NVFP4_DECODE_SOURCES = ["decode_fp4.cu", "decode_common.cuh", "ptx.cuh", "internal.h",
+                        "warp_select.cuh"]
 PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
 
 
@@ -58,7 +60,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the CPU oracle sample")
     ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill", "nvfp4_prefill",
-                                       "chunked_prefill"],
+                                       "chunked_prefill", "mixed_batch"],
                     help="run just this extra workload and print its result (for profiling)")
     return ap.parse_args()
 
@@ -209,7 +211,7 @@ def bench_decode(mm, torch, wl, steps, warmup, flush, stream, pk, min_warm_s=0.0
         sources = DECODE_SOURCES
     else:
         fn = lambda: mm.decode_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"], **kw)  # noqa: E731
-        sources = DECODE_SOURCES
+        sources = NVFP4_DECODE_SOURCES
     with torch.cuda.stream(stream):
         ms = timed_steps(torch, fn, steps, warmup, flush, stream, min_warm_s)
     assert mm.get_device_error(stream) == 0, "device status word set"
@@ -463,6 +465,48 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                               peak_source=pk["source"] + " cuBLAS bf16 burst"))
 
 
+def bench_forward(mm, torch, wl, steps, warmup, flush, stream, pk):
+    """A mixed batch through mm3idx_forward (decode rows first, then two
+    chunked prefills, one call) against the same work as two calls (the
+    decode, then the ragged prefill) on the same stream."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = device_inputs(wl, torch, dev)
+    nd = int(np.sum(np.diff(wl.cu_seqlens) == 4))           # the leading 4-row requests
+    dec_rows = nd * 4
+    cu = wl.cu_seqlens
+    pcu = torch.from_numpy((cu[nd:] - cu[nd]).astype(np.int32)).to(dev)
+    pmax = int(np.diff(cu[nd:]).max())
+    out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
+    n = mm.forward_workspace_bytes(wl.heads, nd, 4, wl.num_reqs - nd, pmax, wl.max_seq_len, wl.topk)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    kw = dict(max_seq_len=wl.max_seq_len, topk=wl.topk, init_blocks=wl.init_blocks,
+              local_blocks=wl.local_blocks, sm_scale=wl.sm_scale)
+    fn = lambda: mm.forward(d["q"], d["cache"], d["table"], d["lens"], pcu, num_decodes=nd,  # noqa: E731
+                            decode_query_len=4, prefill_max_query_len=pmax, out=out,
+                            workspace=ws, stream=stream, **kw)
+    # the same work as two calls
+    dws = mm.new_workspace(mm.OP_DECODE, wl.heads, nd, 4, wl.max_seq_len, wl.topk, dev)
+    pws = mm.new_workspace(mm.OP_PREFILL, wl.heads, wl.num_reqs - nd, pmax, wl.max_seq_len,
+                           wl.topk, dev)
+    qd, qp = d["q"][:dec_rows], d["q"][dec_rows:]
+
+    def two():
+        mm.decode(qd, d["cache"], d["table"][:nd], d["lens"][:nd], query_len=4, out=out[:, :dec_rows],
+                  workspace=dws, stream=stream, **kw)
+        mm.prefill_ragged(qp, d["cache"], d["table"][nd:], d["lens"][nd:], pcu,
+                          max_query_len=pmax, out=out[:, dec_rows:], workspace=pws, stream=stream,
+                          **kw)
+
+    with torch.cuda.stream(stream):
+        ms = timed_steps(torch, fn, steps, warmup, flush, stream)
+        ms2 = timed_steps(torch, two, steps, warmup, flush, stream)
+    assert mm.get_device_error(stream) == 0, "device status word set"
+    t = statistics.mean(ms) * 1e-3
+    return dict(value=wl.rows / t, unit="rows/s", ms_per_step=t * 1e3,
+                two_calls_ms=statistics.mean(ms2), decode_requests=nd,
+                prefill_rows=int(wl.rows - dec_rows), steps=steps)
+
+
 def cpu_model():
     """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
     try:
@@ -579,6 +623,8 @@ def run_ours(args):
         w = W.make(args.only)
         if args.only in ("prefill", "nvfp4_prefill", "chunked_prefill"):
             r = bench_prefill(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
+        elif args.only == "mixed_batch":
+            r = bench_forward(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
         else:
             r = bench_decode(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)[0]
         r["workload"] = w.name
@@ -607,8 +653,9 @@ def run_ours(args):
     if not args.no_extra and rank == 0:
         for key in ("high_batch", "nvfp4_decode"):
             w2 = W.make(key)
-            r2 = bench_decode(mm, torch, w2, max(20, args.steps // 4), 3, flush, stream, pk)[0]
-            r2["roofline"]["traffic"] = profiled_traffic(f"decode_{key}.md", sources)
+            r2, _, _, _, _, src2 = bench_decode(mm, torch, w2, max(20, args.steps // 4), 3, flush,
+                                                stream, pk)
+            r2["roofline"]["traffic"] = profiled_traffic(f"decode_{key}.md", src2)
             r2["workload"] = w2.name
             extra[key] = r2
             del w2
@@ -632,6 +679,11 @@ def run_ours(args):
         del w6
         extra["sparse_table"] = bench_sparse_table(mm, torch, wl, max(20, args.steps // 4), flush,
                                                    stream)
+        w7 = W.make("mixed_batch")
+        r7 = bench_forward(mm, torch, w7, max(20, args.steps // 4), 3, flush, stream, pk)
+        r7["workload"] = w7.name
+        extra["mixed_batch"] = r7
+        del w7
     clk = clocks.stop()
     if rank != 0:
         torch.distributed.destroy_process_group()

@@ -277,10 +277,9 @@ int mm3idx_decode_sparse_table(const mm3idx_problem_t *p, int32_t topk,
  * mm3idx_prefill -- prefill scoring on the tensor cores and top-k selection
  * (index_topk, minimax_m3_index_score then minimax_m3_index_topk).  For
  * topk <= 16 the scorer selects as it goes: each row's best candidates stay
- * in registers and the CTAs that share a query tile merge them at its end,
- * so no score tensor is written; the call clears the workspace's ticket
- * words first (cudaMemsetAsync on `stream`).  For larger topk the fp32
- * scores go to the workspace and the selector follows.  Workspace:
+ * in registers and a small dependent kernel merges the lists of the CTAs
+ * that shared a query tile, so no score tensor is written.  For larger topk
+ * the fp32 scores go to the workspace and the selector follows.  Workspace:
  * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL, ...) bytes, 256-byte aligned, no
  * initialisation needed.  out as in mm3idx_decode.  Any heads/query_len.
  */
@@ -344,6 +343,48 @@ int mm3idx_prefill_ragged(const mm3idx_problem_t *p, const int32_t *cu_seqlens_q
                           int32_t local_blocks, int32_t *out, int64_t out_head_stride,
                           int64_t out_row_stride, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * mm3idx_forward -- one batch of decode requests followed by prefill
+ * requests, scored and selected in one call (indexer_nvfp4,
+ * MiniMaxM3IndexerRocmNvfp4Impl.forward: the batch's first
+ * num_decode_tokens rows go through the decode scorer and its top-k, the
+ * other rows through the prefill scorer and its top-k, into one output).
+ * p describes all num_reqs requests (bf16 cache, or NVFP4 pages with
+ * p->index_scales set).  Requests 0 .. num_decodes-1 are decode requests of
+ * p->query_len rows each (rows 0 .. num_decodes*query_len-1; requires
+ * heads * query_len <= 32 when num_decodes > 0, else MM3IDX_ERR_UNSUPPORTED).
+ * Requests num_decodes .. num_reqs-1 are prefill requests whose rows follow
+ * those: prefill_cu_seqlens_q, an int32 device array
+ * [num_reqs - num_decodes + 1], runs from 0 to prefill_total_q (offsets
+ * counted from the first prefill row, as in the ragged calls), at most
+ * prefill_max_query_len rows per request.  idx_q holds
+ * num_decodes*query_len + prefill_total_q rows; out as in mm3idx_decode,
+ * one row per query row of the whole batch.  Workspace:
+ * mm3idx_forward_workspace_bytes(...) bytes, 256-byte aligned, zero-filled
+ * before its first use (its decode part follows mm3idx_decode's rules).
+ * The decode kernel runs first; the prefill's first kernel is launched as a
+ * programmatic dependent of it, so that it starts on the SMs the decode
+ * frees, and completes only after the decode has.
+ */
+int mm3idx_forward(const mm3idx_problem_t *p, int32_t num_decodes,
+                   const int32_t *prefill_cu_seqlens_q, int32_t prefill_total_q,
+                   int32_t prefill_max_query_len, int32_t topk, int32_t init_blocks,
+                   int32_t local_blocks, int32_t *out, int64_t out_head_stride,
+                   int64_t out_row_stride, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * mm3idx_forward_workspace_bytes -- workspace of mm3idx_forward: the decode
+ * workspace of num_decodes requests (MM3IDX_OP_DECODE), rounded up to 256
+ * bytes, then the prefill workspace of num_prefills requests of at most
+ * prefill_max_query_len rows (MM3IDX_OP_PREFILL, or MM3IDX_OP_PREFILL_NVFP4
+ * when nvfp4 != 0).  Reads the current device's SM count; no allocation.
+ */
+int mm3idx_forward_workspace_bytes(int32_t heads, int32_t num_decodes, int32_t decode_query_len,
+                                   int32_t num_prefills, int32_t prefill_max_query_len,
+                                   int32_t max_seq_len, int32_t topk, int32_t nvfp4,
+                                   size_t *bytes);
 
 /*
  * mm3idx_get_device_error -- synchronises `stream`, then reads and clears the

@@ -16,6 +16,7 @@ Entry points (names after the vLLM MiniMax-M3 ``index_topk`` page):
 * :func:`decode`       -- fused score + top-k for short query runs
 * :func:`decode_nvfp4` -- the same over NVFP4 index-K pages
 * :func:`prefill`      -- tensor-core scores + selector for long query runs
+* :func:`forward`      -- a batch of decode requests followed by prefill requests
 """
 
 from __future__ import annotations
@@ -128,6 +129,13 @@ SYMBOLS = {
                                                   ctypes.POINTER(SparseTable), ctypes.c_void_p,
                                                   ctypes.c_size_t, ctypes.c_void_p]),
     "mm3idx_check_wait_timeout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_void_p]),
+    "mm3idx_forward": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_size_t, ctypes.c_void_p]),
+    "mm3idx_forward_workspace_bytes": (ctypes.c_int, [ctypes.c_int32] * 8 +
+                                       [ctypes.POINTER(ctypes.c_size_t)]),
     "mm3idx_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
@@ -513,6 +521,56 @@ def prefill_ragged(idx_q, index_cache, block_table, seq_lens, cu_seqlens_q, *, m
                                          out.stride(1), wp, wn, _stream(idx_q.device, stream)),
                "mm3idx_prefill_ragged")
     return out[:, :total_q, :]
+
+
+def forward_workspace_bytes(heads: int, num_decodes: int, decode_query_len: int,
+                            num_prefills: int, prefill_max_query_len: int, max_seq_len: int,
+                            topk: int, nvfp4: bool = False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.mm3idx_forward_workspace_bytes(heads, num_decodes, decode_query_len, num_prefills,
+                                              prefill_max_query_len, max_seq_len, topk,
+                                              1 if nvfp4 else 0, ctypes.byref(n)),
+           "mm3idx_forward_workspace_bytes")
+    return n.value
+
+
+def forward(idx_q, index_cache, block_table, seq_lens, prefill_cu_seqlens_q, *, num_decodes,
+            decode_query_len, prefill_max_query_len, max_seq_len, topk, init_blocks, local_blocks,
+            sm_scale, index_scales=None, out=None, workspace=None, stream=None):
+    """A batch of ``num_decodes`` decode requests (``decode_query_len`` rows
+    each) followed by prefill requests whose rows are given by
+    ``prefill_cu_seqlens_q`` (int32 [num_prefills + 1], from 0, counted from
+    the first prefill row), scored and selected in one call: int32
+    [heads, rows, topk] ids for every row of the batch.  NVFP4 pages when
+    ``index_scales`` is given.  ``workspace`` (zero-filled, reusable) from
+    :func:`forward_workspace_bytes`; allocated when not given."""
+    num_reqs = seq_lens.shape[0]
+    num_prefills = num_reqs - num_decodes
+    _need(0 <= num_decodes <= num_reqs, "num_decodes must be within the batch")
+    _need(prefill_cu_seqlens_q.dtype == torch.int32 and prefill_cu_seqlens_q.ndim == 1
+          and prefill_cu_seqlens_q.shape[0] == num_prefills + 1
+          and prefill_cu_seqlens_q.is_contiguous() and prefill_cu_seqlens_q.device == idx_q.device,
+          "prefill_cu_seqlens_q must be contiguous int32 [num_prefills + 1] on the query device")
+    dec_rows = num_decodes * decode_query_len
+    total_q = idx_q.shape[0] - dec_rows
+    _need(total_q >= 0 and total_q <= num_prefills * prefill_max_query_len,
+          "rows after the decode rows exceed num_prefills * prefill_max_query_len")
+    nvfp4 = index_scales is not None
+    p = _problem(idx_q, index_cache, block_table, seq_lens, decode_query_len, max_seq_len, sm_scale,
+                 index_scales=index_scales, nvfp4=nvfp4, rows=idx_q.shape[0])
+    rows, heads = idx_q.shape[0], idx_q.shape[1]
+    out = _ids_out(out, heads, rows, topk, idx_q.device)
+    with _on(idx_q.device):
+        if workspace is None:
+            n = forward_workspace_bytes(heads, num_decodes, decode_query_len, num_prefills,
+                                        prefill_max_query_len, max_seq_len, topk, nvfp4)
+            workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=idx_q.device)
+        wp, wn = _ws(workspace, idx_q.device)
+        _check(lib.mm3idx_forward(ctypes.byref(p), num_decodes, prefill_cu_seqlens_q.data_ptr(),
+                                  total_q, prefill_max_query_len, topk, init_blocks, local_blocks,
+                                  out.data_ptr(), out.stride(0), out.stride(1), wp, wn,
+                                  _stream(idx_q.device, stream)), "mm3idx_forward")
+    return out[:, :rows, :]
 
 
 def decode_static(idx_q, index_cache, block_table, seq_lens, *, query_len, max_seq_len, topk,

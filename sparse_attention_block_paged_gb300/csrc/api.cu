@@ -240,6 +240,19 @@ size_t score_nvfp4_ws_bytes(int32_t heads, int32_t num_reqs, int32_t query_len,
   return dequant_copy_bytes(num_reqs, max_seq_len);
 }
 
+// Workspace of a mixed batch: the decode part (256-aligned), then the
+// prefill part.
+size_t forward_ws_bytes(int sms, int32_t heads, int32_t num_decodes, int32_t decode_query_len,
+                        int32_t num_prefills, int32_t prefill_max_query_len, int32_t max_seq_len,
+                        int32_t topk, bool nvfp4) {
+  const size_t d = num_decodes > 0
+      ? align256(decode_ws_bytes(sms, heads, num_decodes, decode_query_len, topk)) : 0;
+  const size_t f = num_prefills > 0
+      ? prefill_ws_bytes(sms, heads, num_prefills, prefill_max_query_len, max_seq_len, topk, nvfp4)
+      : 0;
+  return d + f;
+}
+
 DecodeArgs decode_args(const mm3idx_problem_t* p, int* status) {
   DecodeArgs a{};
   a.q = static_cast<const uint16_t*>(p->idx_q);
@@ -368,8 +381,9 @@ struct PrefillSelect {
 
 int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q, float* out,
                    int64_t head_stride, int64_t row_stride, int sms, int32_t* status,
-                   cudaStream_t s, const PrefillSelect* sel = nullptr) {
+                   cudaStream_t s, const PrefillSelect* sel = nullptr, bool overlap = false) {
   PrefillArgs a{};
+  a.overlap = overlap ? 1 : 0;
   if (sel) {
     a.topk = sel->topk;
     a.init_blocks = sel->init_blocks;
@@ -468,7 +482,7 @@ int score_then_fill(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_
 // range, so the bf16 scorer treats that block as it treats a bad page (no
 // visible tokens).  Requires num_reqs * cdiv(max_seq_len,128) <= INT_MAX / 128.
 int dequant_copy(const mm3idx_problem_t* p, uint8_t* dst, DeviceInfo* dev, cudaStream_t s,
-                 mm3idx_problem_t* q) {
+                 mm3idx_problem_t* q, bool overlap = false) {
   const int64_t width = cdiv(p->max_seq_len, kBlock);
   const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
   DequantArgs d{};
@@ -484,6 +498,7 @@ int dequant_copy(const mm3idx_problem_t* p, uint8_t* dst, DeviceInfo* dev, cudaS
   d.pages_out = reinterpret_cast<uint16_t*>(dst);
   d.table_out = reinterpret_cast<int32_t*>(dst + slots * kBlock * kD * 2);
   d.status = dev->status;
+  d.overlap = overlap ? 1 : 0;
   int rc = cuda_status(launch_dequant_pages(d, dev->sms, s));
   if (rc) return rc;
   *q = *p;
@@ -581,11 +596,12 @@ int run_topk(const float* score, int64_t sh, int64_t sr, int32_t heads, const in
 // score tensor); larger topk: scores to the workspace, then the selector.
 // NVFP4 keys are first dequantised, once per page, into a bf16 copy in the
 // workspace.  cu == nullptr: query_len rows per request; else ragged
-// (total_q rows).
+// (total_q rows).  overlap: the first kernel is launched as a programmatic
+// dependent of the one before it (see PrefillArgs::overlap).
 int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_t total_q,
                 int32_t topk, int32_t init_blocks, int32_t local_blocks, int32_t* out,
                 int64_t out_head_stride, int64_t out_row_stride, void* workspace,
-                size_t workspace_bytes, void* stream) {
+                size_t workspace_bytes, void* stream, bool overlap = false) {
   int rc = check_problem(p, nvfp4);
   if (rc) return rc;
   if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
@@ -615,7 +631,8 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len,
                                                 p->max_seq_len, topk));
   mm3idx_problem_t q = *p;
-  if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q))) return rc;
+  if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q, overlap))) return rc;
+  const bool scorer_overlap = overlap && !nvfp4;   // after a dequant, the scorer reads its output
   if (topk <= kPrefillSelectTK) {
     const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
                                               static_cast<int64_t>(p->num_reqs) * p->query_len);
@@ -630,11 +647,13 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
     sel.tiles = tiles;
     sel.partials = reinterpret_cast<uint64_t*>(
         ws + align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4));
-    return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel);
+    return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel,
+                          scorer_overlap);
   }
   const int64_t w = (width + 3) / 4 * 4;
   float* score = reinterpret_cast<float*>(ws);
-  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, dev->sms, dev->status, s)))
+  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, dev->sms, dev->status, s,
+                           nullptr, scorer_overlap)))
     return rc;
   SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
                              cu, total_q, p->max_seq_len, topk, init_blocks, local_blocks, out,
@@ -842,6 +861,80 @@ int mm3idx_decode_static(const mm3idx_problem_t* p, int32_t topk, int32_t init_b
   return run_decode(p, false, topk, init_blocks, local_blocks, out, out_head_stride,
                     out_row_stride, scratch, MM3IDX_STATIC_SCRATCH_BYTES, stream, nullptr,
                     /*static_scratch=*/true);
+}
+
+int mm3idx_forward_workspace_bytes(int32_t heads, int32_t num_decodes, int32_t decode_query_len,
+                                   int32_t num_prefills, int32_t prefill_max_query_len,
+                                   int32_t max_seq_len, int32_t topk, int32_t nvfp4,
+                                   size_t* bytes) {
+  if (!bytes || heads < 1 || num_decodes < 0 || num_prefills < 0 || decode_query_len < 1 ||
+      prefill_max_query_len < 1 || max_seq_len < 1)
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (topk < 1 || topk > MM3IDX_MAX_TOPK) return MM3IDX_ERR_TOPK;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  *bytes = forward_ws_bytes(dev->sms, heads, num_decodes, decode_query_len, num_prefills,
+                            prefill_max_query_len, max_seq_len, topk, nvfp4 != 0);
+  return MM3IDX_OK;
+}
+
+int mm3idx_forward(const mm3idx_problem_t* p, int32_t num_decodes,
+                   const int32_t* prefill_cu_seqlens_q, int32_t prefill_total_q,
+                   int32_t prefill_max_query_len, int32_t topk, int32_t init_blocks,
+                   int32_t local_blocks, int32_t* out, int64_t out_head_stride,
+                   int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (!p) return MM3IDX_ERR_INVALID_ARGUMENT;
+  const bool nvfp4 = p->index_scales != nullptr;
+  int rc = check_problem(p, nvfp4);
+  if (rc) return rc;
+  if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
+  if (num_decodes < 0 || num_decodes > p->num_reqs || prefill_max_query_len < 1)
+    return MM3IDX_ERR_INVALID_ARGUMENT;
+  const int32_t num_prefills = p->num_reqs - num_decodes;
+  if ((rc = check_ragged(num_prefills, prefill_max_query_len, prefill_cu_seqlens_q,
+                         prefill_total_q)))
+    return rc;
+  if (prefill_max_query_len > p->max_seq_len) return MM3IDX_ERR_QUERY_LEN;
+  if (num_decodes > 0 && p->heads * static_cast<int64_t>(p->query_len) > MM3IDX_MAX_DECODE_ROWS)
+    return MM3IDX_ERR_UNSUPPORTED;
+  const int64_t dec_rows = static_cast<int64_t>(num_decodes) * p->query_len;
+  if (dec_rows + prefill_total_q >= INT_MAX) return MM3IDX_ERR_INVALID_ARGUMENT;
+  if (dec_rows + prefill_total_q == 0) return MM3IDX_OK;
+  if (!out || !out_ok(out_head_stride, out_row_stride, p->heads, dec_rows + prefill_total_q, topk))
+    return MM3IDX_ERR_OUT_LAYOUT;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  const size_t dec_ws = num_decodes > 0
+      ? align256(decode_ws_bytes(dev->sms, p->heads, num_decodes, p->query_len, topk)) : 0;
+  const size_t need = forward_ws_bytes(dev->sms, p->heads, num_decodes, p->query_len,
+                                       num_prefills, prefill_max_query_len, p->max_seq_len, topk,
+                                       nvfp4);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MM3IDX_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // The decode part: requests 0 .. num_decodes-1, rows 0 .. dec_rows-1.
+  if (num_decodes > 0) {
+    mm3idx_problem_t d = *p;
+    d.num_reqs = num_decodes;
+    if ((rc = run_decode(&d, nvfp4, topk, init_blocks, local_blocks, out, out_head_stride,
+                         out_row_stride, ws, dec_ws, stream)))
+      return rc;
+  }
+  if (num_prefills == 0 || prefill_total_q == 0) return MM3IDX_OK;
+  // The prefill part: the remaining requests and rows, launched to start on
+  // the SMs the decode frees.
+  mm3idx_problem_t f = *p;
+  f.num_reqs = num_prefills;
+  f.query_len = prefill_max_query_len;
+  f.idx_q = static_cast<const uint16_t*>(p->idx_q) + dec_rows * p->q_token_stride;
+  f.block_table = p->block_table + static_cast<int64_t>(num_decodes) * p->table_stride;
+  f.seq_lens = p->seq_lens + num_decodes;
+  return run_prefill(&f, nvfp4, prefill_cu_seqlens_q, prefill_total_q, topk, init_blocks,
+                     local_blocks, out + dec_rows * out_row_stride, out_head_stride,
+                     out_row_stride, ws + dec_ws, workspace_bytes - dec_ws, stream,
+                     /*overlap=*/num_decodes > 0);
 }
 
 int mm3idx_get_device_error(void* stream, int32_t* code) {

@@ -84,6 +84,9 @@ __global__ void __launch_bounds__(kThreads) dequant_pages_kernel(const DequantAr
       dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
+  // Overlapping launch (DequantArgs::overlap): complete only once the kernel
+  // before it has.
+  if (a.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -93,8 +96,16 @@ cudaError_t launch_dequant_pages(const DequantArgs& a, int num_sms, cudaStream_t
   int64_t grid = static_cast<int64_t>(num_sms) * 8;
   if (slots < grid) grid = slots;
   if (grid < 1) return cudaSuccess;
-  dequant_pages_kernel<<<static_cast<int>(grid), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, dequant_pages_kernel, a);
 }
 
 }  // namespace mm3idx

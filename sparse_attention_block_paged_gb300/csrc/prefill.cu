@@ -604,6 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // Overlapping launch: complete only once the kernel before it has.
+  if (a.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -685,8 +687,17 @@ cudaError_t launch_prefill_t(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kSelect>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<kSelect><<<grid, kThreads, kSmem, s>>>(qmap, kmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<kSelect>, qmap, kmap, a);
 }
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,

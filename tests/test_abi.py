@@ -329,7 +329,8 @@ def test_every_library_call_runs_with_the_inputs_gpu_current():
     import ast
     src = open(os.path.join(ROOT, "sparse_attention_block_paged_gb300", "__init__.py")).read()
     tree = ast.parse(src)
-    exempt = {"mm3idx_version", "mm3idx_status_string", "mm3idx_workspace_bytes"}
+    exempt = {"mm3idx_version", "mm3idx_status_string", "mm3idx_workspace_bytes",
+              "mm3idx_forward_workspace_bytes"}
     found = 0
 
     def visit(node, guarded):
@@ -353,3 +354,31 @@ def test_every_library_call_runs_with_the_inputs_gpu_current():
 
     visit(tree, False)
     assert found >= 11
+
+
+def test_forward_validation():
+    """mm3idx_forward rejects bad splits and layouts before any device work."""
+    f = mm.lib.mm3idx_forward
+    p = problem(query_len=4, num_reqs=3)             # 3 requests of at most 4 decode rows
+    # num_decodes outside 0..num_reqs
+    assert f(ctypes.byref(p), 4, FAKE, 8, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), -1, FAKE, 8, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -1
+    # prefill rows beyond num_prefills * max_query_len, missing or misaligned offsets
+    assert f(ctypes.byref(p), 1, FAKE, 601, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), 1, None, 8, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -1
+    assert f(ctypes.byref(p), 1, FAKE + 2, 8, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30,
+             None) == -1
+    # prefill query rows longer than max_seq_len
+    assert f(ctypes.byref(p), 1, FAKE, 8, 2000, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -6
+    # decode rows per request over 32
+    q = problem(query_len=16, heads=4, num_reqs=3)
+    assert f(ctypes.byref(q), 1, FAKE, 8, 300, 16, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -10
+    # topk and output layout
+    assert f(ctypes.byref(p), 1, FAKE, 8, 300, 40, 1, 2, FAKE, 1 << 20, 16, FAKE, 1 << 30, None) == -7
+    assert f(ctypes.byref(p), 1, FAKE, 8, 300, 16, 1, 2, FAKE, 1 << 20, 8, FAKE, 1 << 30, None) == -8
+    # an empty batch is a no-op
+    e = problem(num_reqs=0)
+    assert f(ctypes.byref(e), 0, None, 0, 1, 16, 1, 2, None, 0, 16, None, 0, None) == 0
+    n = ctypes.c_size_t(0)
+    assert mm.lib.mm3idx_forward_workspace_bytes(1, 2, 4, 1, 300, 1000, 40, 0, ctypes.byref(n)) == -7
+    assert mm.lib.mm3idx_forward_workspace_bytes(0, 2, 4, 1, 300, 1000, 16, 0, ctypes.byref(n)) == -1

@@ -317,6 +317,19 @@ def _chunked_prefill(seed=6, num_reqs=8):
                        local_blocks=2, max_seq_len=32768)
 
 
+def _mixed_batch(seed=8):
+    """The spec-decode batch's 64 decode requests (4 rows each, 4K-32K tokens)
+    followed by two chunked prefills of 4096 new tokens after 8192 and 16384
+    earlier ones, as one ragged batch (decode rows first); not one of the
+    five named configurations."""
+    rng = np.random.default_rng(1000 + 1)
+    seq = rng.integers(4096, 32768, size=64, endpoint=True)
+    ql = [4] * 64 + [4096, 4096]
+    pre = [int(x) - 4 for x in seq] + [8192, 16384]
+    return ragged_case(seed, query_lens=ql, prefix_lens=pre, heads=1, topk=16, init_blocks=1,
+                       local_blocks=2, max_seq_len=32768)
+
+
 # The five named workloads, by short key, the NVFP4 prefill and a chunked
 # (ragged) prefill batch.  The second argument of each maker
 # (request count / sequence length) lets tests draw a smaller case with the
@@ -329,6 +342,7 @@ WORKLOADS = {
     "nvfp4_decode": _nvfp4_decode,
     "nvfp4_prefill": _nvfp4_prefill,
     "chunked_prefill": _chunked_prefill,
+    "mixed_batch": _mixed_batch,
 }
 
 
