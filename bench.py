@@ -59,8 +59,8 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bound on the CPU oracle sample")
-    ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill", "nvfp4_prefill",
-                                       "chunked_prefill", "mixed_batch"],
+    ap.add_argument("--only", choices=["high_batch", "nvfp4_decode", "prefill", "prefill_topk32",
+                                       "nvfp4_prefill", "chunked_prefill", "mixed_batch"],
                     help="run just this extra workload and print its result (for profiling)")
     return ap.parse_args()
 
@@ -367,7 +367,7 @@ def _attention_table(wl):
     return W.attention_block_table(wl, 1)
 
 
-def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
+def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk, time_scorer=True):
     dev = torch.device("cuda", torch.cuda.current_device())
     d = device_inputs(wl, torch, dev)
     out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
@@ -390,79 +390,49 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk):
                                       query_len=wl.query_len, **kw)
     else:
         fn = lambda: mm.prefill(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len, **kw)  # noqa: E731
-    fused = wl.topk <= 16
     with torch.cuda.stream(stream):
         ms_all = timed_steps(torch, fn, steps, warmup, flush, stream)
-    if fused:
-        # topk <= 16: the scorer keeps each row's candidates and a small merge
-        # kernel writes the ids (after the dequant pass for NVFP4); `value` is
-        # the whole step's rate.  The roofline is the scorer kernel's: the
-        # same kernel in score mode, timed alone through the score call
-        # (bf16, uniform rows), which also writes -inf past each row's block.
-        assert mm.get_device_error(stream) == 0, "device status word set"
-        t_all = statistics.mean(ms_all) * 1e-3
-        fl = prefill_flops(wl)
-        res = dict(value=fl / t_all / 1e12, unit="TFLOP/s (scores + top-k)",
-                   rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3)
-        t_sc = None
-        if not nvfp4 and not ragged:
-            width = -(-wl.max_seq_len // BLOCK)
-            sc_out = torch.empty((wl.heads, wl.rows, width), dtype=torch.float32, device=dev)
-            scf = lambda: mm.score(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len,  # noqa: E731
-                                   max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale, out=sc_out,
-                                   stream=stream)
-            with torch.cuda.stream(stream):
-                ms_sc = timed_steps(torch, scf, steps, warmup, flush, stream)
-                # the standalone selector (mm3idx_topk; also the path for
-                # topk > 16) on the same scores
-                self_sel = lambda: mm.topk(sc_out, d["lens"], query_len=wl.query_len,  # noqa: E731
-                                           max_seq_len=wl.max_seq_len, topk=wl.topk,
-                                           init_blocks=wl.init_blocks,
-                                           local_blocks=wl.local_blocks, out=out, stream=stream)
-                ms_sel = timed_steps(torch, self_sel, steps, warmup, flush, stream)
-            t_sc = statistics.mean(ms_sc) * 1e-3
-            res["scorer_ms"] = t_sc * 1e3
-            res["selector_alone_ms"] = statistics.mean(ms_sel)
-            del sc_out
-        t_roof = t_sc if t_sc is not None else t_all
-        res["roofline"] = dict(bound="tensor", achieved=fl / t_roof / 1e12,
-                               peak=pk["bf16_tflops"], unit="TFLOP/s",
-                               frac=fl / t_roof / 1e12 / pk["bf16_tflops"],
-                               traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
-                                                        PREFILL_SOURCES) if t_sc else None,
-                               algorithmic_flops=fl,
-                               kernel="score-mode prefill kernel alone" if t_sc
-                               else "whole step (scores + top-k)",
-                               peak_source=pk["source"] + " cuBLAS bf16 burst")
-        return res
-    with torch.cuda.stream(stream):
-        w = (-(-wl.max_seq_len // BLOCK) + 3) // 4 * 4
-        sc = ws.view(torch.float32)[: wl.heads * wl.rows * w].view(wl.heads, wl.rows, w)
-        if ragged:
-            sel = lambda: mm.topk_ragged(sc, d["lens"], cu, max_query_len=wl.query_len,  # noqa: E731
-                                         max_seq_len=wl.max_seq_len, topk=wl.topk,
-                                         init_blocks=wl.init_blocks,
-                                         local_blocks=wl.local_blocks, out=out, stream=stream)
-        else:
-            sel = lambda: mm.topk(sc, d["lens"], query_len=wl.query_len,  # noqa: E731
-                                  max_seq_len=wl.max_seq_len, topk=wl.topk,
-                                  init_blocks=wl.init_blocks, local_blocks=wl.local_blocks,
-                                  out=out, stream=stream)
-        ms_sel = timed_steps(torch, sel, steps, warmup, flush, stream)
+    # The scorer keeps each row's candidates and a small merge kernel writes
+    # the ids (after the dequant pass for NVFP4); `value` is the whole step's
+    # rate.  The roofline is the scorer kernel's: the same kernel in score
+    # mode, timed alone through the score call (bf16, uniform rows), which
+    # also writes -inf past each row's block.  time_scorer=False: the whole
+    # step is the roofline's kernel time.
     assert mm.get_device_error(stream) == 0, "device status word set"
     t_all = statistics.mean(ms_all) * 1e-3
-    t_sel = statistics.mean(ms_sel) * 1e-3
-    t_score = max(t_all - t_sel, 1e-9)
     fl = prefill_flops(wl)
-    return dict(value=fl / t_score / 1e12, unit="TFLOP/s (scorer)",
-                rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3, scorer_ms=t_score * 1e3,
-                selector_ms=t_sel * 1e3,
-                roofline=dict(bound="tensor", achieved=fl / t_score / 1e12, peak=pk["bf16_tflops"],
-                              unit="TFLOP/s", frac=fl / t_score / 1e12 / pk["bf16_tflops"],
-                              traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
-                                                       PREFILL_SOURCES),
-                              algorithmic_flops=fl,
-                              peak_source=pk["source"] + " cuBLAS bf16 burst"))
+    res = dict(value=fl / t_all / 1e12, unit="TFLOP/s (scores + top-k)",
+               rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3)
+    t_sc = None
+    if time_scorer and not nvfp4 and not ragged:
+        width = -(-wl.max_seq_len // BLOCK)
+        sc_out = torch.empty((wl.heads, wl.rows, width), dtype=torch.float32, device=dev)
+        scf = lambda: mm.score(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len,  # noqa: E731
+                               max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale, out=sc_out,
+                               stream=stream)
+        with torch.cuda.stream(stream):
+            ms_sc = timed_steps(torch, scf, steps, warmup, flush, stream)
+            # the standalone selector (mm3idx_topk) on the same scores
+            self_sel = lambda: mm.topk(sc_out, d["lens"], query_len=wl.query_len,  # noqa: E731
+                                       max_seq_len=wl.max_seq_len, topk=wl.topk,
+                                       init_blocks=wl.init_blocks,
+                                       local_blocks=wl.local_blocks, out=out, stream=stream)
+            ms_sel = timed_steps(torch, self_sel, steps, warmup, flush, stream)
+        t_sc = statistics.mean(ms_sc) * 1e-3
+        res["scorer_ms"] = t_sc * 1e3
+        res["selector_alone_ms"] = statistics.mean(ms_sel)
+        del sc_out
+    t_roof = t_sc if t_sc is not None else t_all
+    res["roofline"] = dict(bound="tensor", achieved=fl / t_roof / 1e12,
+                           peak=pk["bf16_tflops"], unit="TFLOP/s",
+                           frac=fl / t_roof / 1e12 / pk["bf16_tflops"],
+                           traffic=profiled_traffic("prefill_scorer_causal_prefill.md",
+                                                    PREFILL_SOURCES) if t_sc else None,
+                           algorithmic_flops=fl,
+                           kernel="score-mode prefill kernel alone" if t_sc
+                           else "whole step (scores + top-k)",
+                           peak_source=pk["source"] + " cuBLAS bf16 burst")
+    return res
 
 
 def bench_forward(mm, torch, wl, steps, warmup, flush, stream, pk):
@@ -621,7 +591,7 @@ def run_ours(args):
 
     if args.only:
         w = W.make(args.only)
-        if args.only in ("prefill", "nvfp4_prefill", "chunked_prefill"):
+        if args.only in ("prefill", "prefill_topk32", "nvfp4_prefill", "chunked_prefill"):
             r = bench_prefill(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
         elif args.only == "mixed_batch":
             r = bench_forward(mm, torch, w, args.steps, max(args.warmup, 3), flush, stream, pk)
@@ -664,6 +634,12 @@ def run_ours(args):
         r4["workload"] = w4.name
         extra["prefill"] = r4
         del w4
+        w8 = W.make("prefill_topk32")
+        r8 = bench_prefill(mm, torch, w8, max(10, args.steps // 10), 3, flush, stream, pk,
+                           time_scorer=False)
+        r8["workload"] = w8.name
+        extra["prefill_topk32"] = r8
+        del w8
         w5 = W.make("nvfp4_prefill")
         r5 = bench_prefill(mm, torch, w5, max(10, args.steps // 10), 3, flush, stream, pk)
         r5["workload"] = w5.name

@@ -174,11 +174,10 @@ int mm3idx_topk(const float *score, int64_t score_head_stride,
  * op = MM3IDX_OP_DECODE: one ticket counter per request plus the partial
  * top-k candidate lists of requests split across CTAs (depends on the
  * current device's SM count).
- * op = MM3IDX_OP_PREFILL: topk <= 16 (selection inside the scorer): one
- * ticket word per (tile of 128 query rows, lane quadrant) and two candidate
- * lists per row of each tile a CTA touches (depends on the current device's
- * SM count); topk > 16: the fp32 score scratch
- * [heads, rows, roundup(cdiv(max_seq_len,128), 4)] for the selector.
+ * op = MM3IDX_OP_PREFILL (selection inside the scorer): a 64-byte record
+ * per tile of 128 query rows, then two candidate lists (16 keys for
+ * topk <= 16, else 32; 8 bytes a key) per row of each tile a CTA touches
+ * (depends on the current device's SM count); max_seq_len is not read.
  * op = MM3IDX_OP_PREFILL_NVFP4: that (rounded up to 256 bytes), then a bf16
  * copy of the keys [num_reqs * cdiv(max_seq_len,128), 128, 128] and an
  * int32 table [num_reqs, cdiv(max_seq_len,128)].
@@ -275,11 +274,11 @@ int mm3idx_decode_sparse_table(const mm3idx_problem_t *p, int32_t topk,
 
 /*
  * mm3idx_prefill -- prefill scoring on the tensor cores and top-k selection
- * (index_topk, minimax_m3_index_score then minimax_m3_index_topk).  For
- * topk <= 16 the scorer selects as it goes: each row's best candidates stay
- * in registers and a small dependent kernel merges the lists of the CTAs
- * that shared a query tile, so no score tensor is written.  For larger topk
- * the fp32 scores go to the workspace and the selector follows.  Workspace:
+ * (index_topk, minimax_m3_index_score then minimax_m3_index_topk).  The
+ * scorer selects as it goes: each row's best candidates (a list of 16 keys
+ * for topk <= 16, else 32) stay in registers and a small dependent kernel
+ * merges the lists of the CTAs that shared a query tile, so no score tensor
+ * is written.  Workspace:
  * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL, ...) bytes, 256-byte aligned, no
  * initialisation needed.  out as in mm3idx_decode.  Any heads/query_len.
  */
@@ -295,7 +294,7 @@ int mm3idx_prefill(const mm3idx_problem_t *p, int32_t topk, int32_t init_blocks,
  * codes and p->index_scales the e4m3 scales, as for mm3idx_decode_nvfp4.
  * Every page a request can see is first dequantised, once, to bf16
  * (e4m3_rn_satfinite(e2m1 * scale), exact in bf16) into the workspace; the
- * bf16 tensor-core scorer and the selector then run on that copy.  Workspace:
+ * bf16 tensor-core scorer with its selection then runs on that copy.  Workspace:
  * mm3idx_workspace_bytes(MM3IDX_OP_PREFILL_NVFP4, ...) bytes, 256-byte
  * aligned, no initialisation needed.  A block table entry outside
  * [0, num_pages) sets MM3IDX_DEV_BAD_PAGE and its block gets no visible

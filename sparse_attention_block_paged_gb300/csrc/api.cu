@@ -194,26 +194,20 @@ size_t decode_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_l
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Prefill workspace, part A.  topk <= kPrefillSelectTK (selection fused into
-// the scorer): tile records [tiles][kTileRecInts] (256-aligned), then
-// 2 * (grid + tiles) list slots of 128 rows x kPrefillSelectTK keys.  Larger topk: the fp32
-// scores [heads, rows, roundup(cdiv(max_seq_len,128), 4)] for the selector.
-// `rows` bounds the batch's query rows; tiles are bounded by
-// heads * (cdiv(rows, 128) + num_reqs).
+// Prefill workspace, part A (selection fused into the scorer): tile records
+// [tiles + 1][kTileRecInts] (256-aligned), then 2 * (grid + tiles) list
+// slots of 128 rows x prefill_tk(topk) keys.  `rows` bounds the batch's
+// query rows; tiles are bounded by heads * (cdiv(rows, 128) + num_reqs).
 int64_t prefill_tiles_bound(int32_t heads, int32_t num_reqs, int64_t rows) {
   return static_cast<int64_t>(heads) * (cdiv(rows, 128) + num_reqs);
 }
 
 size_t prefill_part_a(int sms, int32_t heads, int32_t num_reqs, int32_t query_len,
-                      int32_t max_seq_len, int32_t topk) {
+                      int32_t topk) {
   const int64_t rows = static_cast<int64_t>(num_reqs) * query_len;
-  if (topk <= kPrefillSelectTK) {
-    const int64_t tiles = prefill_tiles_bound(heads, num_reqs, rows);
-    return align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4) +
-           static_cast<size_t>(2 * (sms + tiles)) * 128 * kPrefillSelectTK * 8;
-  }
-  const int64_t w = (cdiv(max_seq_len, kBlock) + 3) / 4 * 4;
-  return static_cast<size_t>(heads) * rows * w * 4;
+  const int64_t tiles = prefill_tiles_bound(heads, num_reqs, rows);
+  return align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4) +
+         static_cast<size_t>(2 * (sms + tiles)) * 128 * prefill_tk(topk) * 8;
 }
 
 // The bf16 copy of an NVFP4 batch's visible pages: [num_reqs *
@@ -227,7 +221,7 @@ size_t dequant_copy_bytes(int32_t num_reqs, int32_t max_seq_len) {
 // Whole prefill workspace: part A, then for NVFP4 the bf16 copy of the keys.
 size_t prefill_ws_bytes(int sms, int32_t heads, int32_t num_reqs, int32_t query_len,
                         int32_t max_seq_len, int32_t topk, bool nvfp4) {
-  const size_t a = prefill_part_a(sms, heads, num_reqs, query_len, max_seq_len, topk);
+  const size_t a = prefill_part_a(sms, heads, num_reqs, query_len, topk);
   if (!nvfp4) return a;
   return align256(a) + dequant_copy_bytes(num_reqs, max_seq_len);
 }
@@ -369,7 +363,7 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
 
 // Scores of a batch on the tensor-core scorer; cu == nullptr: query_len
 // rows per request, else the ragged row offsets (total_q rows).
-// Selection fused into the prefill scorer (topk <= kPrefillSelectTK).
+// Selection fused into the prefill scorer.
 struct PrefillSelect {
   int32_t* ids;
   int64_t i_head, i_row;
@@ -592,12 +586,12 @@ int run_topk(const float* score, int64_t sh, int64_t sr, int32_t heads, const in
   return cuda_status(launch_select(a, dev->sms, static_cast<cudaStream_t>(stream)));
 }
 
-// Prefill.  topk <= kPrefillSelectTK: the scorer selects as it goes (no
-// score tensor); larger topk: scores to the workspace, then the selector.
-// NVFP4 keys are first dequantised, once per page, into a bf16 copy in the
-// workspace.  cu == nullptr: query_len rows per request; else ragged
-// (total_q rows).  overlap: the first kernel is launched as a programmatic
-// dependent of the one before it (see PrefillArgs::overlap).
+// Prefill: the scorer selects as it goes (no score tensor), a dependent
+// kernel merges its lists.  NVFP4 keys are first dequantised, once per
+// page, into a bf16 copy in the workspace.  cu == nullptr: query_len rows
+// per request; else ragged (total_q rows).  overlap: the first kernel is
+// launched as a programmatic dependent of the one before it (see
+// PrefillArgs::overlap).
 int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_t total_q,
                 int32_t topk, int32_t init_blocks, int32_t local_blocks, int32_t* out,
                 int64_t out_head_stride, int64_t out_row_stride, void* workspace,
@@ -617,48 +611,38 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   const int64_t width = cdiv(p->max_seq_len, kBlock);
   if (nvfp4 && static_cast<int64_t>(p->num_reqs) * width > INT_MAX / kBlock)
     return MM3IDX_ERR_UNSUPPORTED;
-  // The fused selection's workspace depends on the grid (the SM count); the
-  // two-kernel one does not, so it is checked before any CUDA call.
-  DeviceInfo* dev = nullptr;
-  if (topk <= kPrefillSelectTK && (rc = device_info(&dev))) return rc;
-  const size_t need = prefill_ws_bytes(dev ? dev->sms : 0, p->heads, p->num_reqs, p->query_len,
-                                       p->max_seq_len, topk, nvfp4);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  // The list slots depend on the grid (the SM count): a workspace short of
+  // the size for a grid of none is refused before any CUDA call.
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < prefill_ws_bytes(0, p->heads, p->num_reqs, p->query_len, p->max_seq_len,
+                                         topk, nvfp4))
     return MM3IDX_ERR_WORKSPACE;
-  if (!dev && (rc = device_info(&dev))) return rc;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  if (workspace_bytes < prefill_ws_bytes(dev->sms, p->heads, p->num_reqs, p->query_len,
+                                         p->max_seq_len, topk, nvfp4))
+    return MM3IDX_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len,
-                                                p->max_seq_len, topk));
+  const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len, topk));
   mm3idx_problem_t q = *p;
   if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q, overlap))) return rc;
   const bool scorer_overlap = overlap && !nvfp4;   // after a dequant, the scorer reads its output
-  if (topk <= kPrefillSelectTK) {
-    const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
-                                              static_cast<int64_t>(p->num_reqs) * p->query_len);
-    PrefillSelect sel{};
-    sel.ids = out;
-    sel.i_head = out_head_stride;
-    sel.i_row = out_row_stride;
-    sel.topk = topk;
-    sel.init_blocks = init_blocks;
-    sel.local_blocks = local_blocks;
-    sel.tile_rec = reinterpret_cast<int32_t*>(ws);
-    sel.tiles = tiles;
-    sel.partials = reinterpret_cast<uint64_t*>(
-        ws + align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4));
-    return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel,
-                          scorer_overlap);
-  }
-  const int64_t w = (width + 3) / 4 * 4;
-  float* score = reinterpret_cast<float*>(ws);
-  if ((rc = prefill_scores(&q, cu, total_q, score, rows * w, w, dev->sms, dev->status, s,
-                           nullptr, scorer_overlap)))
-    return rc;
-  SelectArgs a = select_args(score, rows * w, w, p->heads, p->seq_lens, p->num_reqs, p->query_len,
-                             cu, total_q, p->max_seq_len, topk, init_blocks, local_blocks, out,
-                             out_head_stride, out_row_stride, dev->status);
-  return cuda_status(launch_select(a, dev->sms, s));
+  const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
+                                            static_cast<int64_t>(p->num_reqs) * p->query_len);
+  PrefillSelect sel{};
+  sel.ids = out;
+  sel.i_head = out_head_stride;
+  sel.i_row = out_row_stride;
+  sel.topk = topk;
+  sel.init_blocks = init_blocks;
+  sel.local_blocks = local_blocks;
+  sel.tile_rec = reinterpret_cast<int32_t*>(ws);
+  sel.tiles = tiles;
+  sel.partials = reinterpret_cast<uint64_t*>(
+      ws + align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4));
+  return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel,
+                        scorer_overlap);
 }
 
 // Every warp waits on the first phase of a barrier that nothing arrives at,
@@ -730,14 +714,10 @@ int mm3idx_workspace_bytes(int32_t op, int32_t heads, int32_t num_reqs, int32_t 
   }
   if (op == MM3IDX_OP_PREFILL || op == MM3IDX_OP_PREFILL_NVFP4) {
     if (topk < 1 || topk > MM3IDX_MAX_TOPK) return MM3IDX_ERR_TOPK;
-    int sms = 0;
-    if (topk <= kPrefillSelectTK) {   // the list slots depend on the grid
-      DeviceInfo* dev = nullptr;
-      int rc = device_info(&dev);
-      if (rc) return rc;
-      sms = dev->sms;
-    }
-    *bytes = prefill_ws_bytes(sms, heads, num_reqs, query_len, max_seq_len, topk,
+    DeviceInfo* dev = nullptr;   // the list slots depend on the grid
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    *bytes = prefill_ws_bytes(dev->sms, heads, num_reqs, query_len, max_seq_len, topk,
                               op == MM3IDX_OP_PREFILL_NVFP4);
     return MM3IDX_OK;
   }

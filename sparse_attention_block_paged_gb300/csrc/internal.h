@@ -58,10 +58,10 @@ struct PrefillArgs {
   int64_t s_head, s_row;
   const int32_t* cu;          // ragged: [num_reqs + 1] query-row offsets; nullptr: query_len each
   int32_t total_q;            // rows of the batch
-  // fused selection (partials != nullptr; topk <= 16): candidate lists
-  // instead of scores, merged into ids by launch_prefill_merge
+  // fused selection (partials != nullptr): candidate lists instead of
+  // scores, merged into ids by launch_prefill_merge
   int32_t topk, init_blocks, local_blocks;
-  uint64_t* partials;         // [2 * (grid + tiles)] slots of [128 rows][16 keys]
+  uint64_t* partials;         // [2 * (grid + tiles)] slots of [128 rows][prefill_tk(topk) keys]
   int32_t* tile_rec;          // [1 + tiles][kTileRecInts]: [0][0] = tile count, then one per tile
   int32_t* status;
   // Launched as a programmatic dependent of the kernel before it (a decode
@@ -145,7 +145,6 @@ cudaError_t launch_decode_nvfp4(const CUtensorMap& cmap, const DecodeArgs& a, in
                                 cudaStream_t s);
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
-constexpr int kPrefillSelectTK = 16;  // list length of the fused prefill selection (topk <= 16)
 // The merge of the selecting prefill's lists; a programmatic dependent of it.
 cudaError_t launch_prefill_merge(const PrefillMergeArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int num_sms, cudaStream_t s);
@@ -159,5 +158,7 @@ cudaError_t launch_sparse_table(const SparseTableArgs& a, cudaStream_t s);
 int decode_ctas_per_sm();
 // Keys per (slot, row) in the decode workspace for a given topk.
 inline int decode_tk(int topk) { return topk <= 16 ? 16 : 32; }
+// List length of the prefill scorer's fused selection.
+inline int prefill_tk(int topk) { return topk <= 16 ? 16 : 32; }
 
 }  // namespace mm3idx

@@ -266,9 +266,9 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// kSelect: instead of the scores, the top-k ids (topk <= 16), see the
-// epilogue.
-template <bool kSelect>
+// kSelect: instead of the scores, the top-k ids, kept in lists of TK keys
+// (TK = 16 for topk <= 16, else 32), see the epilogue.
+template <bool kSelect, int TK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap, const PrefillArgs a) {
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pos = 0;
     float* srow = nullptr;   // score mode: the row's scores
     int f_lo = 0, l_lo = 0;  // select mode: the row's forced blocks [0, f_lo), [l_lo, c]
-    RegList<kPrefillSelectTK> list;  // select mode: best non-forced keys of the tile so far
+    RegList<TK> list;  // select mode: best non-forced keys of the tile so far
     bool new_tile = true;
     for (; ok && U.valid(); new_tile = U.advance(a)) {
       if (new_tile) {
@@ -571,7 +571,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // holds the tile's first unit also leaves the tile's record.  A
         // dependent kernel merges the lists after this one.
         if (U.p == U.np - 1 || U.left == 1) {
-          constexpr int TK = kPrefillSelectTK;
           if (U.nvis > a.topk) {
             const int64_t slot = 2 * (static_cast<int64_t>(blockIdx.x) + U.tile) + team;
             ulonglong2* dst = reinterpret_cast<ulonglong2*>(a.partials + (slot * 128 + r) * TK);
@@ -618,12 +617,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // waits for on the GPU.
 constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const PrefillMergeArgs a) {
+template <int TK>
+__global__ void __launch_bounds__(kMergeWarps * 32, 1) prefill_merge_kernel(const PrefillMergeArgs a) {
   // Each warp builds its 32 rows in shared memory (lane = row) and writes
-  // them out row by row, so the stores are contiguous.
-  __shared__ int32_t s_rows[kMergeWarps][32][kPrefillSelectTK];
+  // them out row by row, so the stores are contiguous.  Rows are TK + 1
+  // words apart, so that the lanes' stores fall in distinct banks.
+  __shared__ int32_t s_rows[kMergeWarps][32][TK + 1];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int TK = kPrefillSelectTK;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kMergeWarps + wib;
   const int64_t tile = item >> 2;
@@ -681,10 +681,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
   }
 }
 
-template <bool kSelect>
+template <bool kSelect, int TK>
 cudaError_t launch_prefill_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                      int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kSelect>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kSelect, TK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -697,13 +697,14 @@ cudaError_t launch_prefill_t(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<kSelect>, qmap, kmap, a);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<kSelect, TK>, qmap, kmap, a);
 }
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s) {
-  return a.partials != nullptr ? launch_prefill_t<true>(qmap, kmap, a, grid, s)
-                               : launch_prefill_t<false>(qmap, kmap, a, grid, s);
+  if (a.partials == nullptr) return launch_prefill_t<false, 16>(qmap, kmap, a, grid, s);
+  return prefill_tk(a.topk) == 16 ? launch_prefill_t<true, 16>(qmap, kmap, a, grid, s)
+                                  : launch_prefill_t<true, 32>(qmap, kmap, a, grid, s);
 }
 
 cudaError_t launch_prefill_merge(const PrefillMergeArgs& a, cudaStream_t s) {
@@ -718,7 +719,8 @@ cudaError_t launch_prefill_merge(const PrefillMergeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_merge_kernel, a);
+  return prefill_tk(a.topk) == 16 ? cudaLaunchKernelEx(&cfg, prefill_merge_kernel<16>, a)
+                                  : cudaLaunchKernelEx(&cfg, prefill_merge_kernel<32>, a);
 }
 
 }  // namespace mm3idx

@@ -169,12 +169,26 @@ def test_nvfp4_prefill_validation_and_workspace():
     assert f(ctypes.byref(p), 4, 1, 1, FAKE, 1000, 4, FAKE, 1 << 30, None) == 0
     p = problem(index_scales=FAKE)
     assert f(ctypes.byref(p), 32, 1, 1, FAKE, 1000, 32, FAKE, 1000, None) == -9
+
+
+@pytest.mark.gpu
+def test_prefill_workspace_sizes(cuda_device):
+    """Tile records and two candidate lists (16 or 32 keys) per row of each
+    tile a CTA touches; NVFP4 adds the bf16 copy of the pages and its table."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     n = ctypes.c_size_t(0)
-    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL_NVFP4, 2, 3, 300, 1000, 32,
-                                         ctypes.byref(n)) == 0
-    scores = 2 * 3 * 300 * 8 * 4                     # as OP_PREFILL, 256-byte multiple here
-    slots = 3 * 8                                    # requests x cdiv(1000, 128)
-    assert n.value == scores + slots * 128 * 128 * 2 + 256
+    up = lambda x: -(-x // 256) * 256                # noqa: E731
+    tiles = 2 * (-(-3 * 300 // 128) + 3)             # heads x (cdiv(rows, 128) + requests)
+    for topk, tk in ((16, 16), (17, 32), (32, 32)):
+        part_a = up((tiles + 1) * 64) + 2 * (sms + tiles) * 128 * tk * 8
+        assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, topk,
+                                             ctypes.byref(n)) == 0
+        assert n.value == part_a
+        assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL_NVFP4, 2, 3, 300, 1000, topk,
+                                             ctypes.byref(n)) == 0
+        slots = 3 * 8                                # requests x cdiv(1000, 128)
+        assert n.value == up(part_a) + slots * 128 * 128 * 2 + up(slots * 4)
 
 
 def test_ragged_validation():
@@ -205,9 +219,7 @@ def test_workspace_query_validation():
     n = ctypes.c_size_t(0)
     assert mm.lib.mm3idx_workspace_bytes(9, 1, 1, 1, 128, 4, ctypes.byref(n)) == -1
     assert mm.lib.mm3idx_workspace_bytes(mm.OP_DECODE, 1, 1, 1, 128, 40, ctypes.byref(n)) == -7
-    # topk > 16: the two-kernel prefill's score scratch (no device needed)
-    assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 32, ctypes.byref(n)) == 0
-    assert n.value == 2 * 3 * 300 * 8 * 4      # [heads, rows, roundup(cdiv(1000,128), 4)] fp32
+    # topk is checked before the device is queried
     assert mm.lib.mm3idx_workspace_bytes(mm.OP_PREFILL, 2, 3, 300, 1000, 33, ctypes.byref(n)) == -7
 
 

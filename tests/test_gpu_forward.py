@@ -51,7 +51,7 @@ CASES = [
     # seed, decodes, decode qlen, prefill rows, prefill prefixes, heads, topk, format
     (1, 6, 4, [300, 700], [1000, 0], 1, 16, "bf16"),
     (2, 5, 2, [257], [3000], 2, 8, "bf16"),
-    (3, 4, 4, [400, 129], [500, 2000], 1, 32, "bf16"),     # 32-key lists: two-kernel prefill
+    (3, 4, 4, [400, 129], [6000, 9000], 1, 32, "bf16"),    # 32-key lists
     (4, 6, 4, [300, 700], [1000, 0], 1, 16, "nvfp4"),
     (5, 0, 4, [600], [900], 1, 16, "bf16"),                 # prefill only
     (6, 7, 4, [], [], 1, 16, "bf16"),                       # decode only

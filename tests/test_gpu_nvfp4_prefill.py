@@ -72,7 +72,6 @@ def test_nvfp4_dequantised_pages_bit_exact(mm):
     """Every (code, scale byte) pair except the two NaN scales, read back from
     the workspace's bf16 copy and compared with the oracle's value."""
     import torch
-    # topk 32: the two-kernel prefill, whose workspace starts with the scores
     wl = W.random_case(8, num_reqs=1, query_len=256, heads=1, topk=32, init_blocks=1,
                        local_blocks=1, min_len=256, max_len=256, kv_format="nvfp4")
     pages = wl.block_table[0, :2]
@@ -83,17 +82,19 @@ def test_nvfp4_dequantised_pages_bit_exact(mm):
         nib = np.tile(np.arange(16, dtype=np.uint8), 128 * 8).reshape(128, 128)
         nib = np.roll(nib, k, axis=1)
         wl.codes[pg] = nib[:, 0::2] | (nib[:, 1::2] << 4)
-    ws = torch.zeros(mm.workspace_bytes(mm.OP_PREFILL_NVFP4, 1, 1, 256, 256, 32),
-                     dtype=torch.uint8, device="cuda")
+    n = mm.workspace_bytes(mm.OP_PREFILL_NVFP4, 1, 1, 256, 256, 32)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     run_prefill_nvfp4(mm, wl, workspace=ws)
     assert mm.get_device_error() == 0
+    # The workspace ends with the bf16 copy [1 * 2 pages, 128, 128] and its
+    # int32 table [1, 2] (rounded up to 256 bytes).
     width = 2
-    score_bytes = -(-(1 * 256 * 4 * 4) // 256) * 256          # [1, 256, roundup(2, 4)] fp32
-    got = ws[score_bytes:score_bytes + width * 128 * 128 * 2].cpu().numpy().view(np.uint16)
+    copy = n - (width * 128 * 128 * 2 + 256)
+    got = ws[copy:copy + width * 128 * 128 * 2].cpu().numpy().view(np.uint16)
     got = got.reshape(width, 128, 128)
     want = oracle.nvfp4_dequant_bf16(wl.codes[pages], wl.scales[pages])
     np.testing.assert_array_equal(got, want)
-    table = ws[score_bytes + width * 32768:score_bytes + width * 32768 + 8].cpu().numpy().view(np.int32)
+    table = ws[copy + width * 32768:copy + width * 32768 + 8].cpu().numpy().view(np.int32)
     assert table.tolist() == [0, 1]
 
 

@@ -148,13 +148,15 @@ def test_prefill_matches_oracle(mm, case):
     assert mm.get_device_error() == 0
 
 
-@pytest.mark.parametrize("topk,init,local", [(16, 1, 2), (4, 0, 0), (9, 3, 2)])
+@pytest.mark.parametrize("topk,init,local", [(16, 1, 2), (4, 0, 0), (9, 3, 2), (32, 1, 2),
+                                             (17, 0, 0), (25, 4, 3)])
 def test_fused_prefill_selection_equals_two_kernels(mm, topk, init, local):
-    """topk <= 16: the prefill kernel selects as it scores.  Its ids must be
-    those of the score kernel followed by the selector, bit for bit (the
-    same fp32 scores and the same keys)."""
+    """The prefill kernel selects as it scores (16-key lists for topk <= 16,
+    else 32).  Its ids must be those of the score kernel followed by the
+    selector, bit for bit (the same fp32 scores and the same keys)."""
     wl = W.random_case(70 + topk, num_reqs=3, query_len=700, heads=2, topk=topk,
-                       init_blocks=init, local_blocks=local, min_len=700, max_len=5000)
+                       init_blocks=init, local_blocks=local, min_len=700,
+                       max_len=5000 if topk <= 16 else 12000)
     d = to_device(wl)
     fused = run_prefill(mm, wl)
     sc = mm.score(d["q"], d["cache"], d["table"], d["lens"], query_len=wl.query_len,
@@ -312,6 +314,15 @@ def test_full_size_prefill_sampled(mm):
     _prefill_rows_check(wl, prefill_sample_rows(wl.rows), ids, sc, where="prefill")
 
 
+def test_full_size_prefill_topk32_sampled(mm):
+    """The 32768-token causal prefill at topk 32 (32-key lists in the
+    scorer), ids checked on the bf16 prefill's sample rows."""
+    wl = W.make("prefill_topk32")
+    ids = run_prefill(mm, wl)
+    assert mm.get_device_error() == 0
+    _prefill_rows_check(wl, prefill_sample_rows(wl.rows), ids, where="prefill topk32")
+
+
 def test_full_size_nvfp4_prefill_sampled(mm):
     """The 32768-token NVFP4 causal prefill (dequantised copy, then the fused
     scorer), ids and scores checked on the same rows as the bf16 prefill."""
@@ -328,7 +339,7 @@ def test_full_size_nvfp4_prefill_sampled(mm):
 
 
 def test_fused_prefill_workspace_reuse_and_graph_replay(mm):
-    """topk <= 16 keeps tile records and candidate lists in the workspace.
+    """The fused selection keeps tile records and candidate lists in the workspace.
     A larger batch, then a smaller one, then a graph replay of the smaller
     one on the same workspace: each must match the oracle (records and
     lists of the earlier call must not leak into the later one)."""

@@ -290,6 +290,14 @@ def _causal_prefill(seed=3, seq=32768):
                  max_seq_len=seq)
 
 
+def _causal_prefill_topk32(seed=3, seq=32768):
+    """The causal prefill's inputs with 32 selected blocks a row; not one of
+    the five named configurations."""
+    return build("causal prefill, topk 32", seed=seed, seq_lens=[seq], query_len=seq,
+                 heads=1, topk=32, init_blocks=1, local_blocks=2,
+                 max_seq_len=seq)
+
+
 def _nvfp4_decode(seed=4, num_reqs=128):
     rng = np.random.default_rng(1000 + seed)
     seq = rng.integers(32768, 131072, size=num_reqs, endpoint=True)
@@ -330,8 +338,8 @@ def _mixed_batch(seed=8):
                        local_blocks=2, max_seq_len=32768)
 
 
-# The five named workloads, by short key, the NVFP4 prefill and a chunked
-# (ragged) prefill batch.  The second argument of each maker
+# The five named workloads, by short key, the NVFP4 prefill, the causal
+# prefill at topk 32, a chunked (ragged) prefill batch and a mixed batch.  The second argument of each maker
 # (request count / sequence length) lets tests draw a smaller case with the
 # same recipe.
 WORKLOADS = {
@@ -339,6 +347,7 @@ WORKLOADS = {
     "spec_decode": _spec_decode,
     "high_batch": _high_batch,
     "prefill": _causal_prefill,
+    "prefill_topk32": _causal_prefill_topk32,
     "nvfp4_decode": _nvfp4_decode,
     "nvfp4_prefill": _nvfp4_prefill,
     "chunked_prefill": _chunked_prefill,
