@@ -61,7 +61,7 @@ struct PrefillArgs {
   // fused selection (partials != nullptr): candidate lists instead of
   // scores, merged into ids by launch_prefill_merge
   int32_t topk, init_blocks, local_blocks;
-  uint64_t* partials;         // [2 * (grid + tiles)] slots of [128 rows][prefill_tk(topk) keys]
+  uint64_t* partials;         // [2 * (grid + tiles)] slots of [prefill_tk(topk) keys][128 rows]
   int32_t* tile_rec;          // [1 + tiles][kTileRecInts]: [0][0] = tile count, then one per tile
   int32_t* status;
   // Launched as a programmatic dependent of the kernel before it (a decode

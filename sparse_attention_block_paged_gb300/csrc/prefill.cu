@@ -572,10 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dependent kernel merges the lists after this one.
         if (U.p == U.np - 1 || U.left == 1) {
           if (U.nvis > a.topk) {
+            // Key-major slot [TK][128 rows]: a warp's 32 rows store 256
+            // contiguous bytes per key.
             const int64_t slot = 2 * (static_cast<int64_t>(blockIdx.x) + U.tile) + team;
-            ulonglong2* dst = reinterpret_cast<ulonglong2*>(a.partials + (slot * 128 + r) * TK);
+            uint64_t* dst = a.partials + slot * 128 * TK + r;
 #pragma unroll
-            for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
+            for (int k = 0; k < TK; ++k) dst[k * 128] = list.v[k];
           }
           const int64_t tfirst = U.u - U.p, tlast = tfirst + U.np - 1;
           if (warp == 2 && lane == 0 && tfirst >= share_lo) {
@@ -656,17 +658,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 1) prefill_merge_kernel(cons
     const bool dense = total >= a.grid;
     for (int cj = c0; cj <= c1; ++cj) {
       if (!dense && !has_units(cj, total, a.grid)) continue;
+      // The two teams' slots, key-major: the warp's 32 rows read 256
+      // contiguous bytes per key.
       uint64_t l0[TK], l1[TK];
-      const ulonglong2* s0 = reinterpret_cast<const ulonglong2*>(
-          a.partials + ((2 * (static_cast<int64_t>(cj) + tile)) * 128 + r) * TK);
-      const ulonglong2* s1 = s0 + 128 * TK / 2;
+      const uint64_t* s0 = a.partials + 2 * (static_cast<int64_t>(cj) + tile) * 128 * TK + r;
+      const uint64_t* s1 = s0 + 128 * TK;
 #pragma unroll
-      for (int j = 0; j < TK / 2; ++j) {
-        const ulonglong2 x = __ldcg(s0 + j), y = __ldcg(s1 + j);
-        l0[2 * j] = x.x;
-        l0[2 * j + 1] = x.y;
-        l1[2 * j] = y.x;
-        l1[2 * j + 1] = y.y;
+      for (int k = 0; k < TK; ++k) {
+        l0[k] = __ldcg(s0 + k * 128);
+        l1[k] = __ldcg(s1 + k * 128);
       }
       m.merge_sorted(l0);
       m.merge_sorted(l1);
