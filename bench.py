@@ -172,6 +172,17 @@ def prefill_flops(wl):
     return 2.0 * 128 * float(sum(pos)) * wl.heads
 
 
+def graph_of(torch, fn, stream):
+    """fn() (which launches on `stream`) run once, then captured once in a
+    CUDA graph; returns the graph's replay."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g.replay
+
+
 def timed_steps(torch, fn, steps, warmup, flush, stream, min_warm_s=0.0):
     """Per-step CUDA-event times (ms) of fn() on `stream`, L2 flushed (untimed)
     before each step."""
@@ -390,8 +401,14 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk, time_scorer=T
                                       query_len=wl.query_len, **kw)
     else:
         fn = lambda: mm.prefill(d["q"], cache, d["table"], d["lens"], query_len=wl.query_len, **kw)  # noqa: E731
+    # Each step is a CUDA-graph replay of the same call (the calls are
+    # capturable): eagerly, the binding's marshalling and the launches (tens
+    # of microseconds of host time) can outlast the untimed L2 flush before
+    # the step and leave the GPU idle inside the timed region.  The eager
+    # step time is reported beside it.
     with torch.cuda.stream(stream):
-        ms_all = timed_steps(torch, fn, steps, warmup, flush, stream)
+        ms_eager = timed_steps(torch, fn, steps, warmup, flush, stream)
+        ms_all = timed_steps(torch, graph_of(torch, fn, stream), steps, warmup, flush, stream)
     # The scorer keeps each row's candidates and a small merge kernel writes
     # the ids (after the dequant pass for NVFP4); `value` is the whole step's
     # rate.  The roofline is the scorer kernel's: the same kernel in score
@@ -402,7 +419,9 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk, time_scorer=T
     t_all = statistics.mean(ms_all) * 1e-3
     fl = prefill_flops(wl)
     res = dict(value=fl / t_all / 1e12, unit="TFLOP/s (scores + top-k)",
-               rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3)
+               rows_per_s=wl.rows / t_all, ms_per_step=t_all * 1e3,
+               timing="CUDA-graph replay of the call",
+               eager_ms_per_step=statistics.mean(ms_eager))
     t_sc = None
     if time_scorer and not nvfp4 and not ragged:
         width = -(-wl.max_seq_len // BLOCK)
@@ -411,7 +430,7 @@ def bench_prefill(mm, torch, wl, steps, warmup, flush, stream, pk, time_scorer=T
                                max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale, out=sc_out,
                                stream=stream)
         with torch.cuda.stream(stream):
-            ms_sc = timed_steps(torch, scf, steps, warmup, flush, stream)
+            ms_sc = timed_steps(torch, graph_of(torch, scf, stream), steps, warmup, flush, stream)
             # the standalone selector (mm3idx_topk) on the same scores
             self_sel = lambda: mm.topk(sc_out, d["lens"], query_len=wl.query_len,  # noqa: E731
                                        max_seq_len=wl.max_seq_len, topk=wl.topk,

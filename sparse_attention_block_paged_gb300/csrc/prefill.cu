@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m0 = fmax3(m0, __uint_as_float(v1[k]), __uint_as_float(v1[k + 1]));
                 m1 = fmax3(m1, __uint_as_float(v1[k + 2]), __uint_as_float(v1[k + 3]));
               }
-            } else {
+            } else if (lim >= 0) {   // rows past the request's end (lim < 0) are never read
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
                 if (64 * h + k <= lim) m0 = fmaxf(m0, __uint_as_float(v0[k]));

@@ -322,7 +322,7 @@ def _chunked_prefill(seed=6, num_reqs=8):
     ql = rng.integers(1000, 8000, size=num_reqs, endpoint=True)
     pre = rng.integers(0, 24000, size=num_reqs, endpoint=True)
     return ragged_case(seed, query_lens=ql, prefix_lens=pre, heads=1, topk=16, init_blocks=1,
-                       local_blocks=2, max_seq_len=32768)
+                       local_blocks=2, max_seq_len=32768, name="chunked prefill batch")
 
 
 def _mixed_batch(seed=8):
@@ -335,7 +335,7 @@ def _mixed_batch(seed=8):
     ql = [4] * 64 + [4096, 4096]
     pre = [int(x) - 4 for x in seq] + [8192, 16384]
     return ragged_case(seed, query_lens=ql, prefix_lens=pre, heads=1, topk=16, init_blocks=1,
-                       local_blocks=2, max_seq_len=32768)
+                       local_blocks=2, max_seq_len=32768, name="mixed decode + prefill batch")
 
 
 # The five named workloads, by short key, the NVFP4 prefill, the causal
@@ -376,13 +376,13 @@ def random_case(seed, *, num_reqs, query_len, heads, topk, init_blocks,
 
 
 def ragged_case(seed, *, query_lens, prefix_lens, heads, topk, init_blocks, local_blocks,
-                max_seq_len=None, kv_format="bf16", sm_scale=None):
+                max_seq_len=None, kv_format="bf16", sm_scale=None, name=None):
     """A ragged batch: request i has query_lens[i] new tokens after
     prefix_lens[i] earlier ones (seq_len = prefix + count)."""
     ql = np.asarray(query_lens, dtype=np.int64)
     seq = (np.asarray(prefix_lens, dtype=np.int64) + ql).astype(np.int32)
     msl = max_seq_len or int(max(1, seq.max()))
-    return build(f"ragged-{seed}", seed=seed, seq_lens=seq, query_len=1, heads=heads,
+    return build(name or f"ragged-{seed}", seed=seed, seq_lens=seq, query_len=1, heads=heads,
                  topk=topk, init_blocks=init_blocks, local_blocks=local_blocks,
                  max_seq_len=msl,
                  sm_scale=sm_scale if sm_scale is not None else 1.0 / math.sqrt(128.0),
