@@ -234,66 +234,203 @@ __device__ __forceinline__ void load_q_tile(const DecodeArgs& a, int req, uint8_
   }
 }
 
-// One request of the merge warp (below), lane n owning row n: fold the NL
-// handed-over lists of each row (H: [NL][TK][32 rows]), then either write
-// the rows (a request held by this CTA alone) or publish the lists and take
-// the request's ticket, the last of its CTAs merging every CTA's lists and
-// writing the rows.  With total >= grid every share is non-empty, so the
-// request's CTAs are first..last; with fewer blocks than CTAs every
-// non-empty share is a single block, so block k sits in cta_of(preq + k).
-//
-// The other CTAs' lists are loaded all at once, one (row, CTA) pair per lane
-// (G sources per round), and folded with a shuffle tree; 32-key lists fold
-// one source per round (a second list would not fit the registers).
+// The merge works in a spread layout: four rows per pass, row g of the pass
+// on lanes 8g..8g+7, lane 8g+s holding list positions s, s+8, ... (TK/8 keys,
+// descending over positions).  A bitonic step at a stride below 8 pairs a
+// lane with lane ^ stride, at 8 or more two registers of one lane, so all 32
+// lanes share a merge of two TK-key lists (about 6*TK/8 instructions a lane
+// a step).  With one lane per row, four rows left 28 lanes idle and each
+// 64-bit merge took one lane 1000-1600 cycles of dependent integer work.
+template <int TK>
+__device__ __forceinline__ void spread_clean_desc(uint64_t (&v)[TK / 8], int s) {
+  constexpr int KL = TK / 8;
+#pragma unroll
+  for (int d = KL / 2; d > 0; d >>= 1) {       // strides TK/2 .. 8: registers i, i + d
+#pragma unroll
+    for (int i = 0; i < KL; ++i) {
+      if ((i & d) == 0) {
+        const uint64_t x = v[i], y = v[i + d];
+        v[i] = x > y ? x : y;
+        v[i + d] = x > y ? y : x;
+      }
+    }
+  }
+#pragma unroll
+  for (int st = 4; st > 0; st >>= 1) {         // strides 4, 2, 1: lanes s, s ^ st
+    const bool lower = (s & st) == 0;
+#pragma unroll
+    for (int i = 0; i < KL; ++i) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v[i], st);
+      v[i] = (v[i] > o) == lower ? v[i] : o;
+    }
+  }
+}
+
+// a := the best TK keys of a and b (both descending), descending: the
+// elementwise max of a and reversed b is a bitonic sequence holding exactly
+// those keys, which a half-cleaner cascade orders.
+template <int TK>
+__device__ __forceinline__ void spread_merge(uint64_t (&a)[TK / 8], const uint64_t (&b)[TK / 8],
+                                             int lane) {
+  constexpr int KL = TK / 8;
+  const int s = lane & 7;
+  const int src = (lane & ~7) | (7 - s);     // holds position TK-1-p in register KL-1-i
+#pragma unroll
+  for (int i = 0; i < KL; ++i) {
+    const uint64_t r = __shfl_sync(0xffffffffu, b[KL - 1 - i], src);
+    a[i] = a[i] > r ? a[i] : r;
+  }
+  spread_clean_desc<TK>(a, s);
+}
+
+// Ascending bitonic sort of TK ids in the spread layout.
+template <int TK>
+__device__ __forceinline__ void spread_sort_asc(int (&id)[TK / 8], int s) {
+  constexpr int KL = TK / 8;
+#pragma unroll
+  for (int size = 2; size <= TK; size <<= 1) {
+#pragma unroll
+    for (int st = size / 2; st > 0; st >>= 1) {
+      if (st >= 8) {
+        const int d = st / 8;
+#pragma unroll
+        for (int i = 0; i < KL; ++i) {
+          if ((i & d) == 0) {
+            const bool up = ((8 * i) & size) == 0;
+            const int x = id[i], y = id[i + d];
+            id[i] = up ? min(x, y) : max(x, y);
+            id[i + d] = up ? max(x, y) : min(x, y);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < KL; ++i) {
+          const int p = s + 8 * i;
+          const bool up = (p & size) == 0, lower = (p & st) == 0;
+          const int o = __shfl_xor_sync(0xffffffffu, id[i], st);
+          id[i] = (lower == up) ? min(id[i], o) : max(id[i], o);
+        }
+      }
+    }
+  }
+}
+
+// Writes one row from its spread list (every lane of the warp takes part;
+// write = false for lanes whose row does not exist): forced blocks [0, f_lo),
+// the best topk - |forced| picks in ascending id order, the local blocks
+// [l_lo, c], then -1.  c < 0 (no visible block): -1 throughout.
+template <int TK>
+__device__ __forceinline__ void spread_write_row(const uint64_t (&v)[TK / 8], int c,
+                                                 int init_blocks, int local_blocks, int topk,
+                                                 int32_t* out, int s, bool write) {
+  constexpr int KL = TK / 8;
+  const Forced F(c, init_blocks, local_blocks);
+  const int m = c < 0 ? 0 : topk - F.nf;
+  const int nlocal = c < 0 ? 0 : c + 1 - F.l_lo;
+  const int f_lo = c < 0 ? 0 : F.f_lo;
+  int id[KL];
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < KL; ++i) {
+    const bool take = s + 8 * i < m && v[i] != 0ull;
+    id[i] = take ? key_block(v[i]) : 0x7fffffff;
+    cnt += take;
+  }
+  cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+  cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+  cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
+  spread_sort_asc<TK>(id, s);
+  if (!write) return;
+#pragma unroll
+  for (int i = 0; i < KL; ++i)
+    if (s + 8 * i < cnt) out[f_lo + s + 8 * i] = id[i];
+  for (int o = s; o < topk; o += 8) {
+    if (o < f_lo) {
+      out[o] = o;
+    } else if (o >= f_lo + cnt) {
+      const int t = o - f_lo - cnt;
+      out[o] = t < nlocal ? F.l_lo + t : -1;
+    }
+  }
+}
+
+// Where a request's lists are: its first and last CTA (with total >= grid
+// every share is non-empty, so they are first..last; with fewer blocks than
+// CTAs every non-empty share is a single block, and block k sits in
+// cta_of(preq + k)) and how many CTAs hold part of it.  Computed before the
+// lists are handed over (64-bit divisions).
+struct MergeGeom {
+  int first, nseg;
+  bool dense;
+};
+
+__device__ __forceinline__ MergeGeom merge_geom(int nb, long long preq, long long total) {
+  MergeGeom m;
+  m.dense = total >= gridDim.x;
+  m.first = cta_of(preq, total, gridDim.x);
+  const int last = cta_of(preq + nb - 1, total, gridDim.x);
+  m.nseg = m.dense ? last - m.first + 1 : nb;
+  return m;
+}
+
+// One request of the merge warp: fold the NL handed-over lists of each row
+// (H: [NL][TK][32 rows]), then either write the rows (a request held by this
+// CTA alone) or publish the lists ([slot][32 rows][TK]) and take the
+// request's ticket, the last of its CTAs merging every CTA's lists and
+// writing the rows.  Rows are taken four per pass in the spread layout.
 //
 // dry: the same instructions on the same path with no global access at all
 // (no loads, stores or ticket; `split` picks the path).  The merge of a split
 // request is often the last work of the last CTA of the batch; a dry run at
 // kernel start brings this code into the instruction cache, where its first
-// real run would otherwise wait on instruction fetches at every step.
+// real run would otherwise wait on instruction fetches.
 template <int TK, int NL>
-__device__ __noinline__ void merge_request(const DecodeArgs& a, int req, int nb, long long preq,
-                                           long long total, const uint64_t* H, int lane,
-                                           bool dry, bool split) {
-  const int n = lane;
+__device__ __noinline__ void merge_request(const DecodeArgs& a, int req, long long preq, int seq,
+                                           MergeGeom geo, long long total, const uint64_t* H,
+                                           int lane, bool dry, bool split) {
+  constexpr int KL = TK / 8;
   const int R = a.rows_per_req;
-  const int G = TK <= 16 ? max(1, 32 / R) : 1;
-  const int my_row = lane % R, my_src = lane / R;
-  const int first = cta_of(preq, total, gridDim.x);
-  const int last = cta_of(preq + nb - 1, total, gridDim.x);
-  const bool dense = total >= gridDim.x;
-  const int nseg = dry ? (split ? 2 : 1) : (dense ? last - first + 1 : nb);
-  const int j = n < R ? n / a.heads : 0, h = n < R ? n - j * a.heads : 0;
-  const int pr = (dry ? a.max_seq_len : req_len(a, req)) - a.query_len + j;
-  const int cr = pr >= 0 ? (pr >> 7) : -1;
-  int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
+  const int g = lane >> 3, s = lane & 7;
+  const int nseg = dry ? (split ? 2 : 1) : geo.nseg;
   const int64_t slot_stride = static_cast<int64_t>(kLanes) * TK;
-  RegList<TK> list;
-  list.clear();
-  if (n < R) {
+  auto fold = [&](int r, uint64_t (&v)[KL]) {
 #pragma unroll
-    for (int k = 0; k < TK; ++k) list.v[k] = H[k * kLanes + n];
+    for (int i = 0; i < KL; ++i) v[i] = r < R ? H[(s + 8 * i) * kLanes + r] : 0ull;
 #pragma unroll
     for (int l = 1; l < NL; ++l) {
-      uint64_t other[TK];
+      uint64_t o[KL];
 #pragma unroll
-      for (int k = 0; k < TK; ++k) other[k] = H[(l * TK + k) * kLanes + n];
-      list.merge_sorted(other);
+      for (int i = 0; i < KL; ++i) o[i] = r < R ? H[(l * TK + s + 8 * i) * kLanes + r] : 0ull;
+      spread_merge<TK>(v, o, lane);
     }
-  }
+  };
+  auto write_rows = [&](int r, const uint64_t (&v)[KL]) {
+    const int rr = r < R ? r : 0;
+    const int j = rr / a.heads, h = rr - j * a.heads;
+    const int pr = (dry ? a.max_seq_len : seq) - a.query_len + j;
+    const int cr = pr >= 0 ? (pr >> 7) : -1;
+    int32_t* out = a.ids + h * a.i_head + (static_cast<int64_t>(req) * a.query_len + j) * a.i_row;
+    spread_write_row<TK>(v, cr, a.init_blocks, a.local_blocks, a.topk, out, s, r < R && !dry);
+  };
   if (nseg == 1) {
-    // Lane n writes row n: forced blocks, the best picks in ascending id
-    // order (a sorting network over the TK candidate ids), then -1.
-    if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out, dry);
+    for (int r0 = 0; r0 < R; r0 += 4) {
+      uint64_t v[KL];
+      fold(r0 + g, v);
+      write_rows(r0 + g, v);
+    }
     return;
   }
   // Split request: publish this CTA's lists, then take a ticket.  The
   // ticket wraps to zero on the last arrival, ready for the next call.
-  if (n < R && !dry) {
-    ulonglong2* dst = reinterpret_cast<ulonglong2*>(
-        a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + n * TK);
+  for (int r0 = 0; r0 < R; r0 += 4) {
+    const int r = r0 + g;
+    uint64_t v[KL];
+    fold(r, v);
+    if (r < R && !dry) {
+      uint64_t* dst = a.partials + (static_cast<int64_t>(blockIdx.x) + req) * slot_stride + r * TK;
 #pragma unroll
-    for (int k = 0; k < TK; k += 2) dst[k / 2] = make_ulonglong2(list.v[k], list.v[k + 1]);
+      for (int i = 0; i < KL; ++i) dst[s + 8 * i] = v[i];
+    }
   }
   // The warp barrier orders the lanes' list stores before lane 0's release;
   // lane 0's acquire, then the barrier, orders the merging lanes' reads after
@@ -306,34 +443,32 @@ __device__ __noinline__ void merge_request(const DecodeArgs& a, int req, int nb,
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   __syncwarp();
   if (ticket != static_cast<unsigned int>(nseg - 1)) return;
-  for (int base = 0; base < nseg; base += G) {
-    const int js = base + my_src;
-    int cj = -1;
-    if (lane < R * G && js < nseg) cj = dense ? first + js : cta_of(preq + js, total, gridDim.x);
-    RegList<TK> got;
-    if (cj >= 0 && cj != static_cast<int>(blockIdx.x) && !dry) {
-      const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
-          a.partials + (static_cast<int64_t>(cj) + req) * slot_stride + my_row * TK);
+  // The last arrival: its own lists again from the hand-over, then every
+  // other CTA's, four sources' loads in flight at a time.
+  constexpr int kBatch = 4;
+  for (int r0 = 0; r0 < R; r0 += 4) {
+    const int r = r0 + g;
+    uint64_t v[KL];
+    fold(r, v);
+    for (int base = 0; base < nseg; base += kBatch) {
+      uint64_t o[kBatch][KL];
 #pragma unroll
-      for (int u = 0; u < TK / 2; ++u) {
-        const ulonglong2 x = __ldcg(src + u);
-        got.v[2 * u] = x.x;
-        got.v[2 * u + 1] = x.y;
+      for (int b = 0; b < kBatch; ++b) {
+        const int js = base + b;
+        int cj = -1;
+        if (js < nseg) cj = geo.dense ? geo.first + js : cta_of(preq + js, total, gridDim.x);
+        const bool load = cj >= 0 && cj != static_cast<int>(blockIdx.x) && r < R && !dry;
+        const uint64_t* src = a.partials + (static_cast<int64_t>(load ? cj : 0) + req) * slot_stride +
+                              r * TK;
+#pragma unroll
+        for (int i = 0; i < KL; ++i) o[b][i] = load ? __ldcg(src + s + 8 * i) : 0ull;
       }
-    } else {
-      got.clear();
-    }
-    for (int w = 1; w < G; w <<= 1) {
-      uint64_t o[TK];
 #pragma unroll
-      for (int k = 0; k < TK; ++k) o[k] = __shfl_down_sync(0xffffffffu, got.v[k], R * w);
-      // Lanes whose source index is a multiple of 2w take their partner's
-      // list (sources past G hold empty lists).
-      if ((my_src & (2 * w - 1)) == 0 && my_src + w < G) got.merge_sorted(o);
+      for (int b = 0; b < kBatch; ++b)
+        if (base + b < nseg) spread_merge<TK>(v, o[b], lane);
     }
-    if (n < R) list.merge_sorted(got.v);
+    write_rows(r, v);
   }
-  if (n < R) write_row_lane<TK>(list.v, cr, a.init_blocks, a.local_blocks, a.topk, out, dry);
 }
 
 // Requests with no blocks at all appear in no share: their rows are spread
@@ -360,36 +495,45 @@ __device__ __forceinline__ void fill_empty_requests(const DecodeArgs& a, int lan
   }
 }
 
-// The merge warp: merge_request for every request of this CTA's share, in
-// the walker's order, as the scoring warps hand their lists over (hand-over
-// slot seg & 1); afterwards, the requests with no blocks.
+// The merge warp: first the requests with no blocks; then merge_request for
+// every request of this CTA's share, in the walker's order, as the scoring
+// warps hand their lists over (hand-over slot seg & 1).  The walker steps to
+// the next segment (and reads its length) before the wait for the current
+// one's lists, so that after the share's last hand-over no global read is
+// left on the way to the CTA's exit.
 template <int TK, int NL>
 __device__ void merge_warp(const DecodeArgs& a, Walker walker, long long total, uint64_t* sHand,
                            uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                            int lane) {
-  const bool select = a.mode == kModeSelect;
-  if (select) {
-    // Dry runs of both paths while the first lists are still being scored.
-    merge_request<TK, NL>(a, 0, 1, 0, 1, sHand, lane, true, false);
-    merge_request<TK, NL>(a, 0, 1, 0, 1, sHand, lane, true, true);
-  }
-  int seg = 0;
-  bool ok = true;
+  fill_empty_requests(a, lane);
+  if (a.mode != kModeSelect) return;
+  // Dry runs of both paths while the first lists are still being scored.
+  const MergeGeom none{0, 1, true};
+  merge_request<TK, NL>(a, 0, 0, 1, none, 1, sHand, lane, true, false);
+  merge_request<TK, NL>(a, 0, 0, 1, none, 1, sHand, lane, true, true);
   int req, b0, b1, nb;
   long long preq;
-  while (select && ok && walker.next(a, req, b0, b1, nb, preq)) {
+  bool have = walker.next(a, req, b0, b1, nb, preq);
+  int seq = have ? req_len(a, req) : 0;
+  MergeGeom geo = have ? merge_geom(nb, preq, total) : none;
+  for (int seg = 0; have; ++seg) {
+    int nreq, nb0, nb1, nnb;
+    long long npreq;
+    const bool nhave = walker.next(a, nreq, nb0, nb1, nnb, npreq);
+    const int nseq = nhave ? req_len(a, nreq) : 0;
+    const MergeGeom ngeo = nhave ? merge_geom(nnb, npreq, total) : none;
     const int hs = seg & 1;
-    if (!warp_wait(&h_full[hs], (seg >> 1) & 1, abort_flag)) {
-      ok = false;
-      break;
-    }
-    merge_request<TK, NL>(a, req, nb, preq, total, sHand + hs * NL * TK * kLanes, lane, false,
-                          false);
+    if (!warp_wait(&h_full[hs], (seg >> 1) & 1, abort_flag)) break;
+    merge_request<TK, NL>(a, req, preq, seq, geo, total, sHand + hs * NL * TK * kLanes, lane,
+                          false, false);
     __syncwarp();
     if (lane == 0) mbar_arrive(&h_empty[hs]);
-    ++seg;
+    req = nreq;
+    preq = npreq;
+    seq = nseq;
+    geo = ngeo;
+    have = nhave;
   }
-  if (ok) fill_empty_requests(a, lane);
 }
 
 // Score mode, once a request's last block has been scored: -inf for its

@@ -450,17 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_j = n < R ? n / a.heads : 0;
     const int my_h = n < R ? n - my_j * a.heads : 0;
     const bool select = a.mode == kModeSelect;
+    // Requests with no blocks first, then dry runs of both merge paths
+    // (decode_common.cuh), all before the first accumulator is ready.
+    fill_empty_requests(a, lane);
     if (select) {
-      // Dry runs of both merge paths (decode_common.cuh) before the first
-      // accumulator is ready.
-      merge_request<TK, 1>(a, 0, 1, 0, 1, sList, lane, true, false);
-      merge_request<TK, 1>(a, 0, 1, 0, 1, sList, lane, true, true);
+      const MergeGeom none{0, 1, true};
+      merge_request<TK, 1>(a, 0, 0, 1, none, 1, sList, lane, true, false);
+      merge_request<TK, 1>(a, 0, 0, 1, none, 1, sList, lane, true, true);
     }
     RegList<TK> list;
     uint32_t ut = 0;
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      const int pos = req_len(a, req) - a.query_len + my_j;
+      const int seq = req_len(a, req);
+      const int pos = seq - a.query_len + my_j;
+      const MergeGeom geo = merge_geom(nb, preq, total);
       const int c = pos >= 0 ? (pos >> 7) : -1;
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
@@ -503,13 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (select) {
         if (n < R) list.store_cols(sList, n);
         __syncwarp();
-        merge_request<TK, 1>(a, req, nb, preq, total, sList, lane, false, false);
+        merge_request<TK, 1>(a, req, preq, seq, geo, total, sList, lane, false, false);
         __syncwarp();
       } else if (b1 == nb && a.fill_width > nb) {
         fill_past_blocks(a, req, nb, lane);
       }
     }
-    if (ok) fill_empty_requests(a, lane);
   }
 
   tc_fence_before();
