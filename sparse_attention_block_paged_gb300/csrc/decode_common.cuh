@@ -51,8 +51,8 @@ __device__ __forceinline__ int req_blocks(const DecodeArgs& a, int i) {
 // CTAs share out: each request a CTA serves costs it a query tile and, when
 // split, a cross-CTA merge, which the blocks alone do not count.  The extra
 // positions come first and hold no work.  Measured on one GB300 over 0-20:
-// 6 gave high-batch 171 -> 163 us and kept spec-decode at its faster 60.6 us;
-// larger values lose again.
+// 6 gave high-batch 171 -> 163 us; the spec-decode batch is within noise
+// over 0-12 (57.3-58.6 us, graph replays); larger values lose again.
 constexpr int kSegCost = 6;
 
 __device__ __forceinline__ int req_slots(const DecodeArgs& a, int i) {
@@ -444,8 +444,9 @@ __device__ __noinline__ void merge_request(const DecodeArgs& a, int req, long lo
   __syncwarp();
   if (ticket != static_cast<unsigned int>(nseg - 1)) return;
   // The last arrival: its own lists again from the hand-over, then every
-  // other CTA's, four sources' loads in flight at a time.
-  constexpr int kBatch = 4;
+  // other CTA's, eight sources' loads in flight at a time (a request of the
+  // named batches spans at most eight CTAs, so one round trip).
+  constexpr int kBatch = 8;
   for (int r0 = 0; r0 < R; r0 += 4) {
     const int r = r0 + g;
     uint64_t v[KL];
