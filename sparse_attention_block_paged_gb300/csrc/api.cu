@@ -84,22 +84,6 @@ int make_kmap(const mm3idx_problem_t* p, CUtensorMap* m) {
   return r == CUDA_SUCCESS ? MM3IDX_OK : MM3IDX_ERR_CACHE_LAYOUT;
 }
 
-// NVFP4 codes as [pages*128, 64] bytes: boxes of one page (128 rows of 64 B),
-// 64-byte swizzle.
-int make_cmap(const mm3idx_problem_t* p, CUtensorMap* m) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return MM3IDX_ERR_CUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD / 2),
-                              static_cast<cuuint64_t>(p->num_pages) * kBlock};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD / 2)};
-  const cuuint32_t box[2] = {kD / 2, 128};
-  const cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(p->index_cache), dims,
-                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MM3IDX_OK : MM3IDX_ERR_CACHE_LAYOUT;
-}
-
 // [rows, heads, 128] bf16 queries, boxes of 64 columns x 1 head x 128 rows.
 int make_qmap(const mm3idx_problem_t* p, int64_t rows, CUtensorMap* m) {
   EncodeTiledFn enc = encode_fn();
@@ -314,8 +298,8 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MM3IDX_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap kmap;
-  if ((rc = nvfp4 ? make_cmap(p, &kmap) : make_kmap(p, &kmap))) return rc;
+  CUtensorMap kmap;   // bf16 pages only: the NVFP4 kernel copies whole pages untiled
+  if (!nvfp4 && (rc = make_kmap(p, &kmap))) return rc;
   // The tickets must start at zero; a completed call leaves them so, but a
   // call that gave up part-way may not have.
   if (static_scratch && cudaMemsetAsync(workspace, 0, decode_ws_head(p->num_reqs), s) != cudaSuccess)
@@ -336,7 +320,7 @@ int run_decode(const mm3idx_problem_t* p, bool nvfp4, int32_t topk, int32_t init
   if (nvfp4) {
     a.codes = static_cast<const uint8_t*>(p->index_cache);
     a.scales = static_cast<const uint8_t*>(p->index_scales);
-    e = launch_decode_nvfp4(kmap, a, grid, s);
+    e = launch_decode_nvfp4(a, grid, s);
   } else {
     e = launch_decode_bf16(kmap, a, grid, s);
   }
@@ -539,9 +523,7 @@ int run_score(const mm3idx_problem_t* p, bool nvfp4, float* out, int64_t out_hea
     if (nvfp4) {
       a.codes = static_cast<const uint8_t*>(p->index_cache);
       a.scales = static_cast<const uint8_t*>(p->index_scales);
-      CUtensorMap cmap;
-      if ((rc = make_cmap(p, &cmap))) return rc;
-      return cuda_status(launch_decode_nvfp4(cmap, a, decode_grid(p, dev->sms), s));
+      return cuda_status(launch_decode_nvfp4(a, decode_grid(p, dev->sms), s));
     }
     CUtensorMap kmap;
     if ((rc = make_kmap(p, &kmap))) return rc;

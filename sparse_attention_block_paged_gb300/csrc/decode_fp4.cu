@@ -3,40 +3,36 @@
 // the fp32 scores written out (score mode) or a fused top-k selector (select
 // mode).  Each key element is e4m3_rn_satfinite(e2m1 code * e4m3 scale), one
 // scale per 16 elements (vLLM MiniMax-M3 "indexer_nvfp4" page, module
-// docstring); every such value is exact in bf16, so the page is dequantised
-// to bf16 and scored on the tensor cores against the bf16 query rows exactly
-// as the bf16 kernel (decode.cu) scores bf16 pages, with the same partition,
-// walker and merge warp (decode_common.cuh).
+// docstring); every such value is exact in bf16, and the products with the
+// bf16 query rows are exact in the fp32 accumulators, as in the bf16 kernel
+// (decode.cu).  The partition, walker and merge are decode_common.cuh's.
 //
-// A tcgen05.mma instruction costs about the same time whatever its N, and a
-// page needs eight of them (K = 128 in steps of 16), so the instruction rate
-// bounds the kernel long before HBM does; each MMA therefore takes two pages
-// (N = 256 key tokens) with the query rows as A (M = 128).
+// Why not tcgen05 here: its B operand (or A) must sit in shared memory, so a
+// page's 32 KB of dequantised bf16 is written to and read back from shared
+// memory -- with the TMA copy and the code reads, about 100 KB of
+// shared-memory traffic per 9 KB page from HBM, which bounds the kernel near
+// half of the HBM rate.  With a handful of query rows the contraction itself
+// is small (rows x 128 x 128 per page), so the dequantised keys instead go
+// straight from registers into warp-level mma.sync (m16n8k16, bf16 in, fp32
+// accumulate): keys as A (16 tokens x 16 dims), the query rows as B
+// (16 dims x 8 rows, up to four row tiles), held in registers per request.
+// The 128 dims of a product are taken in an order (the same for keys and
+// queries) that gives each thread one 16-byte run of a token's codes and two
+// of its scales.
 //
-//   * warp 2   : producer.  Per page, one TMA tiled copy of the 8 KB of codes
-//                (64-byte swizzle, so that the dequantisers' per-token loads
-//                hit distinct banks) and one bulk copy of the 1 KB of scales
-//                into a ring of raw stages, the pages further ahead pulled
-//                into L2 first; the query rows of each request into the Q
-//                tile.
-//   * warps 3+ : dequantisers, two groups of four; group g takes page g of
-//                each two-page unit.  A thread owns one token: 64 code bytes,
-//                8 scale bytes, a per-scale table lookup (copies of the table
-//                side by side spread the lanes' lookups over the banks) and
-//                byte permutes give its 128 bf16 values, stored straight into
-//                the unit's slot in the 128-byte-swizzled K-major layout of
-//                the MMA's B operand (the eight lanes of a store phase hit
-//                eight distinct 16-byte bank groups).
-//   * warp 1   : one thread issues tcgen05.mma, A = query rows, B = the
-//                unit's slot (N = 256, or 128 for a request's last odd
-//                block), into one of two 256-column fp32 accumulators.
-//   * warp 0   : epilogue: lane n = query row n takes its row's causal block
-//                max of both blocks of each unit (decode.cu's epilogue), and
-//                at the end of each request merges its candidate lists itself
-//                (decode_common.cuh, merge_request): with one or two requests
-//                per CTA this stalls the pipeline rarely, and the shared
-//                memory of a hand-over and the registers of a merge warp go
-//                to a deeper raw ring instead.
+//   * warp 1   : producer.  Per page, bulk copies of the 8 KB of codes and
+//                the 1 KB of scales into a ring of raw stages, the pages
+//                further ahead pulled into L2 first.
+//   * warps 2-9: compute.  Warp w takes pages w, w+8, ... of the CTA's
+//                stream: eight slabs of 16 tokens, each eight mma.sync per
+//                row tile over the dequantised codes, then the causal row
+//                max of the block (masked only in a request's last blocks),
+//                written to the stage's score slot.
+//   * warp 0   : selector.  Takes the score slots in page order, scales them
+//                (a block with an out-of-range page gets -inf), offers them
+//                to its rows' candidate lists (lane n = row n) or writes the
+//                scores, frees the stage, and at the end of each request
+//                writes or merges the rows (merge_request).
 //
 // Every wait is bounded (ptx.cuh); a wait that gives up raises the CTA's
 // abort flag and MM3IDX_DEV_TIMEOUT.
@@ -52,16 +48,17 @@ using namespace dec;
 
 constexpr int kCodeBytes = kBlock * kD / 2;    // 8 KB: 128 tokens x 64 B
 constexpr int kScaleBytes = kBlock * kD / 16;  // 1 KB: 128 tokens x 8 B
-constexpr int kRawStride = 10240;              // codes (1024-aligned), scales, pad
-constexpr int kAccBufs = 2;
-constexpr int kAccCols = 256;                  // a unit of two pages
-constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
-constexpr int kHalfPage = kBlock * 64 * 2;     // 128 rows x 64 bf16 = 16 KB
-constexpr int kSlotHalf = 2 * kHalfPage;       // one 64-column half of a two-page slot
-constexpr int kEpiWarp = 0, kMmaWarp = 1, kProdWarp = 2, kDeqWarp0 = 3;
-constexpr int kThreads = (kDeqWarp0 + 8) * 32;
-constexpr int MQ = 128;                        // query tile rows (the M = 128 layout)
+constexpr int kStageBytes = kCodeBytes + kScaleBytes;
+constexpr int kSelWarp = 0, kProdWarp = 1, kCompWarp0 = 2;
+// Compute warps.  Measured on the 128-request NVFP4 batch: twelve (under
+// the 128-register cap of 14 warps) 0.328 ms, eight 0.305 ms.
+template <int NT>
+constexpr int comp_warps() { return 8; }
+template <int NT>
+constexpr int threads_of() { return (kCompWarp0 + comp_warps<NT>()) * 32; }
 constexpr int kAhead = 16;                     // pages pulled into L2 ahead of the ring (< 32)
+constexpr int kStages = 18;                    // raw ring depth (pages)
+constexpr int kTabCopies = 8;                  // lane & 7 picks a copy: a quarter-warp's lookups hit distinct banks
 
 // The warp pulls one page's codes (64 lines of 128 B) and scales (8 lines)
 // into L2, two or three lines per lane.
@@ -74,26 +71,20 @@ __device__ __forceinline__ void prefetch_page_l2(const DecodeArgs& a, int page, 
                                                    lane * 128));
 }
 
-// Shared memory: the two-page slots as two regions, one per 64-column half
-// ([slot][page][128 rows][128 B] each), the Q tile, the raw ring, the table,
-// the epilogue's lists for its merges.  32-key lists take one raw stage less.
+// Shared memory: the raw ring (codes then scales per stage), the magnitude
+// table, the score slots (32 rows per stage), the selector's lists for its
+// merges, the barriers.
 template <int TK>
 struct Cfg {
-  static constexpr int kPairs = 2;
-  static constexpr int kRawStages = TK == 16 ? 5 : 4;
-  static constexpr int kTabCopies = 2;
-  static constexpr int kQBytes = MQ * kD * 2;
-  static constexpr int oH0 = 0;
-  static constexpr int oH1 = oH0 + kPairs * kSlotHalf;
-  static constexpr int oQ = oH1 + kPairs * kSlotHalf;
-  static constexpr int oRaw = oQ + kQBytes;
-  static constexpr int oTab = oRaw + kRawStages * kRawStride;   // [256 scales][copies] x 16 B
-  static constexpr int oList = oTab + 256 * kTabCopies * 16;    // [TK][32] keys
+  static constexpr int oRaw = 0;
+  static constexpr int oTab = oRaw + kStages * kStageBytes;       // [256 scales][copies] x 16 B
+  static constexpr int oScore = oTab + 256 * kTabCopies * 16;      // [stages][32] fp32
+  static constexpr int oList = oScore + kStages * kLanes * 4;      // [TK][32] keys
   static constexpr int oBar = oList + TK * kLanes * 8;
-  static constexpr int kBars = 2 * kRawStages + 2 * kPairs + 2 * kAccBufs + 2 + 1;
+  static constexpr int kBars = 3 * kStages;
   static constexpr int oMisc = oBar + kBars * 8;
-  static constexpr int kSmem = oMisc + 64 + 1024;
-  static_assert(oQ % 1024 == 0 && oRaw % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+  static constexpr int kSmem = oMisc + 64 + 128;
+  static_assert(kStageBytes % 128 == 0 && oTab % 128 == 0 && oBar % 8 == 0, "alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -150,93 +141,60 @@ __device__ __forceinline__ uint4 dequant8(uint32_t codes, const uint4& t) {
                     prmt(lo1, h1, 0x7362u));
 }
 
+// D += A * B on the legacy warp-level tensor path: A 16x16 bf16 (row), B
+// 16x8 bf16 (col), D 16x8 fp32, fragments in registers.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// Row max of one block's 128 accumulator columns (this lane's TMEM lane),
-// with the columns past `lim` left out when lim < 127.
-__device__ __forceinline__ float acc_row_max(uint32_t taddr, int lim) {
-  float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-  for (int c0 = 0; c0 < kBlock; c0 += 64) {
-    uint32_t v[32], w[32];
-    tmem_ld32(taddr + c0, v);
-    tmem_ld32(taddr + c0 + 32, w);
-    tmem_ld_wait32x2(v, w);
-    if (lim >= 127) {
-#pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        m0 = fmax3(m0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-        m1 = fmax3(m1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
-        m0 = fmax3(m0, __uint_as_float(w[k]), __uint_as_float(w[k + 1]));
-        m1 = fmax3(m1, __uint_as_float(w[k + 2]), __uint_as_float(w[k + 3]));
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        if (c0 + k <= lim) m0 = fmaxf(m0, __uint_as_float(v[k]));
-        if (c0 + 32 + k <= lim) m1 = fmaxf(m1, __uint_as_float(w[k]));
-      }
-    }
-  }
-  return fmaxf(m0, m1);
-}
-
-template <int TK>
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_fp4_kernel(const __grid_constant__ CUtensorMap cmap, const DecodeArgs a) {
+// ------------------------------------------------------------------ kernel
+//
+// Fragment layout (thread t of a warp, j = t & 3, g = t >> 2): in k-step ks
+// (0..7) of slab sl the thread's A registers are tokens 16*sl + g and +8,
+// dims 32j + 4ks + {0,1} (a0, a1) and 32j + 4ks + {2,3} (a2, a3) -- bytes
+// 16j + 2ks and 16j + 2ks + 1 of the token's codes, so its k-steps walk one
+// 16-byte run, and scale groups 2j (k-steps 0-3) and 2j+1 (4-7); its B
+// registers are query row 8*nt + g, the same dims.  D: rows = tokens
+// 16*sl + g (c0, c1) and +8 (c2, c3), columns = query rows 8*nt + 2j, +1.
+template <int TK, int NT>
+__global__ void __launch_bounds__(threads_of<NT>(), 1) decode_fp4_kernel(const DecodeArgs a) {
   using C = Cfg<TK>;
-  constexpr int RS = C::kRawStages;
-  constexpr int P = C::kPairs;
-  constexpr int NC = C::kTabCopies;
+  constexpr int S = kStages, NC = kTabCopies;
+  constexpr int kCompWarps = comp_warps<NT>(), kThreads = threads_of<NT>();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  uint8_t* sH0 = sm + C::oH0;
-  uint8_t* sH1 = sm + C::oH1;
-  uint8_t* sQ = sm + C::oQ;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~static_cast<uintptr_t>(127));
   uint8_t* sRaw = sm + C::oRaw;
   const uint4* sTab = reinterpret_cast<const uint4*>(sm + C::oTab);
+  float* sScore = reinterpret_cast<float*>(sm + C::oScore);
   uint64_t* sList = reinterpret_cast<uint64_t*>(sm + C::oList);
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + C::oBar);
-  uint64_t* raw_empty = raw_full + RS;
-  uint64_t* slot_full = raw_empty + RS;    // both dequantiser groups wrote the unit
-  uint64_t* slot_empty = slot_full + P;    // the unit's MMAs are done with the slot
-  uint64_t* acc_full = slot_empty + P;
-  uint64_t* acc_empty = acc_full + kAccBufs;
-  uint64_t* q_full = acc_empty + kAccBufs;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* done_bar = q_empty + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::oBar);   // the copies landed
+  uint64_t* done = full + S;                                     // the stage's scores are written
+  uint64_t* empty = done + S;                                    // the selector is done with the stage
   Misc* misc = reinterpret_cast<Misc*>(sm + C::oMisc);
   volatile int* abort_flag = &misc->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RS; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&done[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < P; ++s) {
-      mbar_init(&slot_full[s], 8);
-      mbar_init(&slot_empty[s], 1);
-    }
-    for (int s = 0; s < kAccBufs; ++s) {
-      mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 1);
-    }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    mbar_init(done_bar, 1);
     misc->abort = 0;
     fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&misc->tmem, kTmemCols);
-    tmem_relinquish();
   }
   build_fp4_table(reinterpret_cast<uint4*>(sm + C::oTab), NC, threadIdx.x, kThreads);
   // Programmatic dependent launch: the set-up above overlaps the previous
@@ -244,15 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kProdWarp) {
-    if (lane == 0) prefetch_tensormap(&cmap);
     partition(a, misc, lane);
-  } else if (warp == kEpiWarp) {
+  } else if (warp == kSelWarp) {
     prefetch_table_and_queries(a, lane);
   }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = misc->tmem;
   const long long total = misc->total;
   Walker walker = make_walker(misc);
 
@@ -262,24 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
-    int seg = 0;
     uint32_t it = 0;  // pages issued
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      // One Q tile: it is rewritten once the previous request's MMAs are
-      // done, just before the first wait that could block, so that page
-      // loads are already in flight meanwhile.
-      bool q_pending = true;
-      auto put_q = [&]() {
-        if (seg > 0) ok = warp_wait(q_empty, (seg - 1) & 1, abort_flag);
-        if (ok) {
-          load_q_tile<MQ>(a, req, sQ, lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(q_full);
-        }
-        q_pending = false;
-      };
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
       // Page ids 32 at a time (one per lane), the next 32 read one chunk
       // early.  The request's first kAhead pages are pulled into L2 here,
@@ -300,158 +239,179 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ahead = __shfl_sync(0xffffffffu, ka < 32 ? pg : pg_next, ka & 31);
           if (ahead >= 0 && ahead < a.num_pages) prefetch_page_l2(a, ahead, lane);
           const bool good = page >= 0 && page < a.num_pages;
-          const uint32_t st = it % RS, rnd = it / RS;
-          if (rnd > 0 && q_pending) put_q();
-          if (!ok) break;
-          if (rnd > 0) ok = warp_wait(&raw_empty[st], (rnd - 1) & 1, abort_flag);
+          const uint32_t st = it % S, rnd = it / S;
+          if (rnd > 0) ok = warp_wait(&empty[st], (rnd - 1) & 1, abort_flag);
           if (!ok) break;
           if (lane == 0) {
             if (good) {
-              uint8_t* dst = sRaw + st * kRawStride;
-              mbar_arrive_expect_tx(&raw_full[st], kCodeBytes + kScaleBytes);
-              tma_load_2d(dst, &cmap, &raw_full[st], 0, page * kBlock, pol);
+              uint8_t* dst = sRaw + st * kStageBytes;
+              mbar_arrive_expect_tx(&full[st], kStageBytes);
+              bulk_load(dst, a.codes + static_cast<int64_t>(page) * kCodeBytes, kCodeBytes,
+                        &full[st], pol);
               bulk_load(dst + kCodeBytes, a.scales + static_cast<int64_t>(page) * kScaleBytes,
-                        kScaleBytes, &raw_full[st], pol);
+                        kScaleBytes, &full[st], pol);
             } else {
-              // Not loaded: the stage's stale bytes are dequantised and
-              // scored, and the epilogue gives the block -inf.
+              // Not loaded: the stage's stale bytes are scored, and the
+              // selector gives the block -inf.
               atomicOr(a.status, MM3IDX_DEV_BAD_PAGE);
-              mbar_arrive(&raw_full[st]);
+              mbar_arrive(&full[st]);
             }
           }
           __syncwarp();
           ++it;
         }
       }
-      if (ok && q_pending) put_q();
-      ++seg;
     }
     // Let every copy this warp started land before the CTA can exit.
     if (lane == 0) {
-      const uint32_t pending = it < static_cast<uint32_t>(RS) ? it : RS;
+      const uint32_t pending = it < static_cast<uint32_t>(S) ? it : S;
       for (uint32_t k = 0; k < pending; ++k) {
         const uint32_t idx = it - 1 - k;
         int dummy = 0;
-        mbar_wait(&raw_full[idx % RS], (idx / RS) & 1, &dummy);
+        mbar_wait(&full[idx % S], (idx / S) & 1, &dummy);
       }
     }
     __syncwarp();
-  } else if (warp >= kDeqWarp0) {
-    // --------------------------------------------------------- dequantisers
-    const int group = (warp - kDeqWarp0) >> 2;   // which page of each unit
-    const int tok = ((warp - kDeqWarp0) & 3) * 32 + lane;
-    const int swz = (tok >> 1) & 3;                // 64-byte swizzle of the code rows
-    const int copy = lane % NC;
-    // This token's rows in the two halves of a slot (128-byte swizzle).
-    const uint32_t row_off = group * kHalfPage + (tok >> 3) * 1024 + (tok & 7) * 128;
-    uint32_t it = 0, ut = 0;  // pages and units so far
+  } else if (warp >= kCompWarp0) {
+    // -------------------------------------------------------------- compute
+    const int w = warp - kCompWarp0;
+    const int j = lane & 3, g = lane >> 2;
+    const int R = a.rows_per_req;
+    const int copy = lane & (NC - 1);
+    uint32_t pi = 0;  // pages of the stream so far
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-      for (int bu = b0; bu < b1; bu += 2, ++ut) {
-        const bool two = bu + 1 < b1;
-        const bool mine = group == 0 || two;
-        const uint32_t pit = it + group;           // this group's page of the unit
-        it += two ? 2 : 1;
-        const uint32_t st = ut % P, sr = ut / P;
-        const uint32_t rs = pit % RS, rr = pit / RS;
-        bool got = true;
-        if (lane == 0) {
-          if (mine) got = mbar_wait(&raw_full[rs], rr & 1, abort_flag);
-          // The slot's previous unit must be consumed before this group
-          // writes it or counts towards its next phase.
-          if (got && sr > 0) got = mbar_wait(&slot_empty[st], (sr - 1) & 1, abort_flag);
+      const uint32_t nseg = static_cast<uint32_t>(b1 - b0);
+      // This warp's first page of the segment.
+      const uint32_t first = (static_cast<uint32_t>(w) + kCompWarps - pi % kCompWarps) % kCompWarps;
+      if (first < nseg) {
+        // The request's query rows as B fragments: row 8*nt + g, dims
+        // 32j .. 32j+31 (word 2ks: dims 32j+4ks, +1; word 2ks+1: +2, +3).
+        uint32_t bq[NT][16];
+        const int seq = req_len(a, req);
+        int lim0[NT][2];  // pos - 0 for the D columns (query rows 8*nt + 2j + e) of this lane
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int n = nt * 8 + g;
+          if (n < R) {
+            const int jj = n / a.heads, h = n - jj * a.heads;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + (static_cast<int64_t>(req) * a.query_len + jj) * a.q_tok +
+                static_cast<int64_t>(h) * a.q_head + 32 * j);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 x = __ldg(src + v);
+              bq[nt][4 * v] = x.x;
+              bq[nt][4 * v + 1] = x.y;
+              bq[nt][4 * v + 2] = x.z;
+              bq[nt][4 * v + 3] = x.w;
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) bq[nt][v] = 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = nt * 8 + 2 * j + e;
+            lim0[nt][e] = col < R ? seq - a.query_len + col / a.heads : 1 << 30;
+          }
         }
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          ok = false;
-          break;
-        }
-        if (mine) {
+        for (uint32_t k = first; k < nseg; k += kCompWarps) {
+          const uint32_t p = pi + k;
+          const uint32_t st = p % S, rnd = p / S;
+          const int b = b0 + static_cast<int>(k);
+          if (!warp_wait(&full[st], rnd & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           // Every lane observes the completed phase itself before reading
           // what the copies wrote.
-          mbar_try_wait(&raw_full[rs], rr & 1);
-          const uint8_t* raw = sRaw + rs * kRawStride;
-          const uint8_t* crow = raw + tok * 64;
-          uint4 cw[4];
+          mbar_try_wait(&full[st], rnd & 1);
+          const uint8_t* raw = sRaw + st * kStageBytes;
+          int lim[NT][2];
+          bool masked = false;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) cw[c] = *reinterpret_cast<const uint4*>(crow + ((c ^ swz) << 4));
-          const uint2 scw = *reinterpret_cast<const uint2*>(raw + kCodeBytes + tok * 8);
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              lim[nt][e] = lim0[nt][e] - b * kBlock;
+              masked |= lim[nt][e] < kBlock - 1;
+            }
+          masked = __any_sync(0xffffffffu, masked);
+          float m[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) m[nt][0] = m[nt][1] = -INFINITY;
+#pragma unroll 1   // unrolled by 2: 0.307 ms, fully: 0.325 ms (instruction fetch)
+          for (int sl = 0; sl < 8; ++sl) {
+            const int r0 = sl * 16 + g, r1 = r0 + 8;
+            const uint4 ca = *reinterpret_cast<const uint4*>(raw + r0 * 64 + 16 * j);
+            const uint4 cb = *reinterpret_cast<const uint4*>(raw + r1 * 64 + 16 * j);
+            const uint32_t sa = *reinterpret_cast<const uint16_t*>(raw + kCodeBytes + r0 * 8 + 2 * j);
+            const uint32_t sb = *reinterpret_cast<const uint16_t*>(raw + kCodeBytes + r1 * 8 + 2 * j);
+            const uint4 ta0 = sTab[(sa & 0xFFu) * NC + copy], ta1 = sTab[(sa >> 8) * NC + copy];
+            const uint4 tb0 = sTab[(sb & 0xFFu) * NC + copy], tb1 = sTab[(sb >> 8) * NC + copy];
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int qw = 0; qw < 4; ++qw) {
+              const uint32_t wa = qw == 0 ? ca.x : qw == 1 ? ca.y : qw == 2 ? ca.z : ca.w;
+              const uint32_t wb = qw == 0 ? cb.x : qw == 1 ? cb.y : qw == 2 ? cb.z : cb.w;
+              const uint4 da = dequant8(wa, qw < 2 ? ta0 : ta1);
+              const uint4 db = dequant8(wb, qw < 2 ? tb0 : tb1);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_16816(acc[nt], da.x, db.x, da.y, db.y, bq[nt][4 * qw], bq[nt][4 * qw + 1]);
+                mma_16816(acc[nt], da.z, db.z, da.w, db.w, bq[nt][4 * qw + 2], bq[nt][4 * qw + 3]);
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (masked) {
+                // Columns (query rows) see tokens 0..lim of the block.
+                acc[nt][0] = r0 <= lim[nt][0] ? acc[nt][0] : -INFINITY;
+                acc[nt][1] = r0 <= lim[nt][1] ? acc[nt][1] : -INFINITY;
+                acc[nt][2] = r1 <= lim[nt][0] ? acc[nt][2] : -INFINITY;
+                acc[nt][3] = r1 <= lim[nt][1] ? acc[nt][3] : -INFINITY;
+              }
+              m[nt][0] = fmax3(m[nt][0], acc[nt][0], acc[nt][2]);
+              m[nt][1] = fmax3(m[nt][1], acc[nt][1], acc[nt][3]);
+            }
+          }
+          // Max over the block's tokens: the eight lanes of each j.
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float v = m[nt][e];
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+              m[nt][e] = v;
+            }
+          if (lane < 4) {
+            float* slot = sScore + st * kLanes;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              slot[nt * 8 + 2 * lane] = m[nt][0];
+              slot[nt * 8 + 2 * lane + 1] = m[nt][1];
+            }
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&raw_empty[rs]);
-          uint8_t* h0 = sH0 + st * kSlotHalf + row_off;
-          uint8_t* h1 = sH1 + st * kSlotHalf + row_off;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            // Scale group g: elements 16g .. 16g+15, code words 2g, 2g+1,
-            // output chunks 2g, 2g+1 (8 elements each) of the 16 in the row.
-            const uint32_t sb = ((g < 4 ? scw.x : scw.y) >> (8 * (g & 3))) & 0xFFu;
-            const uint4 t = sTab[sb * NC + copy];
-            const uint4 c = cw[g >> 1];
-            const uint32_t w0 = (g & 1) ? c.z : c.x, w1 = (g & 1) ? c.w : c.y;
-            uint8_t* hb = g < 4 ? h0 : h1;
-            const int c0 = (2 * g) & 7, c1 = (2 * g + 1) & 7;
-            *reinterpret_cast<uint4*>(hb + ((c0 ^ (tok & 7)) << 4)) = dequant8(w0, t);
-            *reinterpret_cast<uint4*>(hb + ((c1 ^ (tok & 7)) << 4)) = dequant8(w1, t);
-          }
-          fence_proxy_async_smem();
+          if (lane == 0) mbar_arrive(&done[st]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&slot_full[st]);
       }
+      pi += nseg;
     }
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc2 = idesc_bf16_f32(MQ, 2 * kBlock);
-      constexpr uint32_t idesc1 = idesc_bf16_f32(MQ, kBlock);
-      const uint32_t qaddr = smem_u32(sQ);
-      int seg = 0;
-      uint32_t ut = 0;
-      bool ok = true;
-      while (ok && walker.next(a, req, b0, b1, nb, preq)) {
-        ok = mbar_wait(q_full, seg & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        for (int b = b0; b < b1; b += 2) {
-          const bool two = b + 1 < b1;
-          const uint32_t st = ut % P, rnd = ut / P;
-          ok = mbar_wait(&slot_full[st], rnd & 1, abort_flag);
-          if (!ok) break;
-          const uint32_t ab = ut % kAccBufs, ar = ut / kAccBufs;
-          if (ar > 0) ok = mbar_wait(&acc_empty[ab], (ar - 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k0 = smem_u32(sH0 + st * kSlotHalf), k1 = smem_u32(sH1 + st * kSlotHalf);
-          const uint32_t d = tmem_base + ab * kAccCols;
-          const uint32_t idesc = two ? idesc2 : idesc1;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_kmajor_sw128(qaddr + (k >> 2) * (MQ * 128) + (k & 3) * 32);
-            const uint64_t bd = sdesc_kmajor_sw128((k < 4 ? k0 : k1) + (k & 3) * 32);
-            mma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-          }
-          mma_commit(&slot_empty[st]);
-          mma_commit(&acc_full[ab]);
-          ++ut;
-        }
-        if (!ok) break;
-        mma_commit(q_empty);
-        ++seg;
-      }
-      // Wait until every MMA issued above has finished before TMEM is freed.
-      mma_commit(done_bar);
-      int dummy = 0;
-      mbar_wait(done_bar, 0, &dummy);
-    }
-    __syncwarp();
-  } else if (warp == kEpiWarp) {
-    // ------------------------------------------------------------- epilogue
-    const int n = lane;                   // query row (TMEM lane)
+  } else if (warp == kSelWarp) {
+    // ------------------------------------------------------------- selector
+    const int n = lane;                   // query row
     const int R = a.rows_per_req;
     const int my_j = n < R ? n / a.heads : 0;
     const int my_h = n < R ? n - my_j * a.heads : 0;
     const bool select = a.mode == kModeSelect;
     // Requests with no blocks first, then dry runs of both merge paths
-    // (decode_common.cuh), all before the first accumulator is ready.
+    // (decode_common.cuh), all before the first scores are ready.
     fill_empty_requests(a, lane);
     if (select) {
       const MergeGeom none{0, 1, true};
@@ -459,47 +419,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       merge_request<TK, 1>(a, 0, 0, 1, none, 1, sList, lane, true, true);
     }
     RegList<TK> list;
-    uint32_t ut = 0;
+    uint32_t pi = 0;
     bool ok = true;
     while (ok && walker.next(a, req, b0, b1, nb, preq)) {
       const int seq = req_len(a, req);
       const int pos = seq - a.query_len + my_j;
-      const MergeGeom geo = merge_geom(nb, preq, total);
       const int c = pos >= 0 ? (pos >> 7) : -1;
       const int64_t row = static_cast<int64_t>(req) * a.query_len + my_j;
       const int32_t* trow = a.table + static_cast<int64_t>(req) * a.table_stride;
+      const MergeGeom geo = merge_geom(nb, preq, total);
       list.clear();
-      int pg = 0;  // page ids 32 at a time, one per lane (units never straddle two 32s)
-      for (int bu = b0; bu < b1; bu += 2, ++ut) {
-        const bool two = bu + 1 < b1;
-        if (((bu - b0) & 31) == 0) pg = bu + lane < b1 ? __ldg(trow + bu + lane) : 0;
-        const int page0 = __shfl_sync(0xffffffffu, pg, (bu - b0) & 31);
-        const int page1 = __shfl_sync(0xffffffffu, pg, (bu + 1 - b0) & 31);
-        const uint32_t ab = ut % kAccBufs, ar = ut / kAccBufs;
-        if (!warp_wait(&acc_full[ab], ar & 1, abort_flag)) {
+      int pg = 0;  // page ids 32 at a time, one per lane
+      for (int b = b0; b < b1; ++b, ++pi) {
+        if (((b - b0) & 31) == 0) pg = b + lane < b1 ? __ldg(trow + b + lane) : 0;
+        const int page = __shfl_sync(0xffffffffu, pg, (b - b0) & 31);
+        const uint32_t st = pi % S, rnd = pi / S;
+        if (!warp_wait(&done[st], rnd & 1, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const float m0 = acc_row_max(tmem_base + ab * kAccCols, pos - bu * kBlock);
-        const float m1 =
-            two ? acc_row_max(tmem_base + ab * kAccCols + kBlock, pos - (bu + 1) * kBlock) : -INFINITY;
-        tc_fence_before();
+        mbar_try_wait(&done[st], rnd & 1);   // each lane observes the phase before reading
+        const float v = sScore[st * kLanes + n];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        if (lane == 0) mbar_arrive(&empty[st]);
         if (n < R) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int b = bu + e;
-            if (e == 1 && !two) break;
-            const int page = e ? page1 : page0;
-            const float s =
-                (page >= 0 && page < a.num_pages) ? (e ? m1 : m0) * a.sm_scale : -INFINITY;
-            if (!select) {
-              a.score[my_h * a.s_head + row * a.s_row + b] = s;
-            } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
-              list.offer(make_key(s, b));
-            }
+          const float s = (page >= 0 && page < a.num_pages) ? v * a.sm_scale : -INFINITY;
+          if (!select) {
+            a.score[my_h * a.s_head + row * a.s_row + b] = s;
+          } else if (b <= c && b >= a.init_blocks && b <= c - a.local_blocks) {
+            list.offer(make_key(s, b));
           }
         }
       }
@@ -515,40 +463,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && misc->abort) atomicOr(a.status, MM3IDX_DEV_TIMEOUT);
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
 }
 
-template <int TK>
-cudaError_t launch_t(const CUtensorMap& cmap, const DecodeArgs& a, int grid, cudaStream_t s) {
+template <int TK, int NT>
+cudaError_t launch_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   using C = Cfg<TK>;
-  cudaError_t e = cudaFuncSetAttribute(decode_fp4_kernel<TK>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  const int smem = C::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(decode_fp4_kernel<TK, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.blockDim = dim3(threads_of<NT>());
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fp4_kernel<TK>, cmap, a);
+  return cudaLaunchKernelEx(&cfg, decode_fp4_kernel<TK, NT>, a);
+}
+
+template <int TK>
+cudaError_t launch_tk(const DecodeArgs& a, int grid, cudaStream_t s) {
+  if (a.rows_per_req <= 8) return launch_t<TK, 1>(a, grid, s);
+  if (a.rows_per_req <= 16) return launch_t<TK, 2>(a, grid, s);
+  return launch_t<TK, 4>(a, grid, s);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_nvfp4(const CUtensorMap& cmap, const DecodeArgs& a, int grid,
-                                cudaStream_t s) {
-  if (decode_tk(a.topk) == 16) return launch_t<16>(cmap, a, grid, s);
-  return launch_t<32>(cmap, a, grid, s);
+cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s) {
+  if (decode_tk(a.topk) == 16) return launch_tk<16>(a, grid, s);
+  return launch_tk<32>(a, grid, s);
 }
 
 }  // namespace mm3idx

@@ -139,10 +139,7 @@ struct SparseTableArgs {
 
 // Launchers; each returns a cudaError_t of the launch.
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const DecodeArgs& a, int grid, cudaStream_t s);
-// cmap: the NVFP4 codes as [pages*128, 64] bytes, 64-byte boxes of 128 rows,
-// 64-byte swizzle.
-cudaError_t launch_decode_nvfp4(const CUtensorMap& cmap, const DecodeArgs& a, int grid,
-                                cudaStream_t s);
+cudaError_t launch_decode_nvfp4(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const PrefillArgs& a,
                            int grid, cudaStream_t s);
 // The merge of the selecting prefill's lists; a programmatic dependent of it.
