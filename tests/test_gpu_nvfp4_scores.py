@@ -38,6 +38,7 @@ SCORE_CASES = [
     (3, 4, 8, 4, 129, 5000),
     (4, 9, 2, 2, 16000, 40000),
     (5, 2, 16, 2, 3000, 9000),
+    (8, 4, 3, 4, 700, 9000),        # 12 rows: two 8-row query tiles
     # heads * qlen > 32: bf16 copy + tensor-core scorer
     (6, 2, 300, 1, 300, 2000),
     (7, 3, 257, 2, 700, 3000),

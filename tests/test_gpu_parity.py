@@ -188,10 +188,25 @@ def test_topk_selector_bit_exact_on_same_scores(mm):
 
 # ------------------------------------------------------------------ NVFP4
 
-@pytest.mark.parametrize("seed", [1, 2, 3])
-def test_nvfp4_decode_matches_oracle(mm, seed):
-    wl = W.random_case(seed, num_reqs=5, query_len=4, heads=1, topk=16, init_blocks=1,
-                       local_blocks=2, min_len=500, max_len=20000, kv_format="nvfp4")
+NVFP4_DECODE_CASES = [
+    # seed, query_len, heads, topk, init, local: rows per request 1..32 cover
+    # one, two and four 8-row query tiles of the kernel, 16- and 32-key lists
+    (1, 4, 1, 16, 1, 2),
+    (2, 4, 1, 16, 1, 2),
+    (3, 4, 1, 16, 1, 2),
+    (4, 1, 1, 4, 1, 1),
+    (5, 3, 4, 16, 1, 2),     # 12 rows
+    (6, 8, 2, 32, 2, 3),     # 16 rows, 32-key lists
+    (7, 4, 8, 24, 1, 2),     # 32 rows, 32-key lists
+]
+
+
+@pytest.mark.parametrize("case", NVFP4_DECODE_CASES, ids=lambda c: f"seed{c[0]}")
+def test_nvfp4_decode_matches_oracle(mm, case):
+    seed, qlen, heads, topk, init, local = case
+    wl = W.random_case(seed, num_reqs=5, query_len=qlen, heads=heads, topk=topk,
+                       init_blocks=init, local_blocks=local, min_len=500, max_len=20000,
+                       kv_format="nvfp4")
     s, want = oracle.problem(wl)
     got = run_decode(mm, wl)
     check_ids(got, want, s, wl, where=f"nvfp4 seed{seed}")
