@@ -128,8 +128,9 @@ __device__ __forceinline__ uint32_t xor_signs(uint32_t a, uint32_t b) {
 // Eight e2m1 codes (nibble k = element k, sign in bit 3) -> four bf16x2
 // words (element 2i in the low half of word i).
 __device__ __forceinline__ uint4 dequant8(uint32_t codes, const uint4& t) {
-  const uint32_t sel0 = codes & 0x7777u;
-  const uint32_t sel1 = (codes >> 16) & 0x7777u;
+  // prmt reads its selector from bits 0-15 only: one mask serves both halves.
+  const uint32_t sel0 = codes & 0x77777777u;
+  const uint32_t sel1 = sel0 >> 16;
   const uint32_t lo0 = prmt(t.x, t.y, sel0), hi0 = prmt(t.z, t.w, sel0);
   const uint32_t lo1 = prmt(t.x, t.y, sel1), hi1 = prmt(t.z, t.w, sel1);
   // Bit 7 of byte k of s0 (s1) is the sign of element k (k + 4): the sign
