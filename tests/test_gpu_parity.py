@@ -213,6 +213,25 @@ def test_nvfp4_decode_matches_oracle(mm, case):
     assert mm.get_device_error() == 0
 
 
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: f"seed{c[0]}")
+def test_nvfp4_decode_sweep_matches_oracle(mm, case):
+    """The bf16 decode sweep (tiny and single-block requests, fewer blocks
+    than CTAs, 1-16 rows per request, topk 4-32) over NVFP4 pages: ids and
+    the score call's scores against the oracle."""
+    seed, reqs, qlen, heads, topk, init, local, lo, hi = case
+    wl = W.random_case(100 + seed, num_reqs=reqs, query_len=qlen, heads=heads, topk=topk,
+                       init_blocks=init, local_blocks=local, min_len=lo, max_len=hi,
+                       kv_format="nvfp4")
+    s, want = oracle.problem(wl)
+    check_ids(run_decode(mm, wl), want, s, wl, where=f"nvfp4 sweep seed{seed}")
+    d = to_device(wl)
+    sc = mm.score_nvfp4(d["q"], d["codes"], d["scales"], d["table"], d["lens"],
+                        query_len=wl.query_len, max_seq_len=wl.max_seq_len,
+                        sm_scale=wl.sm_scale).cpu().numpy()
+    check_scores(sc, s, f"nvfp4 sweep scores seed{seed}")
+    assert mm.get_device_error() == 0
+
+
 def test_nvfp4_equals_bf16_path_on_dequantised_cache(mm):
     """The NVFP4 kernel's dequantised keys are exact bf16 values, so scoring the
     oracle-dequantised cache on the bf16 path must give the same ids."""
