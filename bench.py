@@ -245,15 +245,9 @@ def bench_decode(mm, torch, wl, steps, warmup, flush, stream, pk, min_warm_s=0.0
     return res, d, out, ws, kw, sources
 
 
-def bench_e2e_graph(mm, torch, wl, d, kw, steps, warmup, stream):
-    """End to end as a serving loop runs it: one step = the host -> device
-    copy of the step's packed inputs (pinned), the decode through the public
-    API, and the device -> host copy of its ids, captured once as a CUDA
-    graph and replayed every step (the library's calls are capturable; this
-    takes the per-step Python and launch overhead off the step).  No L2
-    flush: the key cache the decode streams (about 283 MB) is larger than
-    the L2.  Time = the whole run of `steps` replays, host clock, device
-    synchronised on both sides."""
+def _packed_inputs(torch, wl, dev, n_slots):
+    """The step's queries, block table and lengths packed in one pinned host
+    buffer, and n_slots device buffers with views of the three."""
     parts = [wl.q.view(np.uint8).reshape(-1), wl.block_table.view(np.uint8).reshape(-1),
              wl.seq_lens.view(np.uint8).reshape(-1)]
     offs, n = [], 0
@@ -263,42 +257,99 @@ def bench_e2e_graph(mm, torch, wl, d, kw, steps, warmup, stream):
     host = torch.empty(n, dtype=torch.uint8).pin_memory()
     for p, o in zip(parts, offs):
         host[o:o + p.nbytes] = torch.from_numpy(p)
+    slots = []
+    for _ in range(n_slots):
+        buf = torch.empty(n, dtype=torch.uint8, device=dev)
+        q = buf[offs[0]:offs[0] + parts[0].nbytes].view(torch.bfloat16).view(wl.q.shape)
+        table = buf[offs[1]:offs[1] + parts[1].nbytes].view(torch.int32).view(wl.block_table.shape)
+        lens = buf[offs[2]:offs[2] + parts[2].nbytes].view(torch.int32).view(wl.seq_lens.shape)
+        slots.append((buf, q, table, lens))
+    return host, slots, int(sum(p.nbytes for p in parts))
+
+
+def bench_e2e_graph(mm, torch, wl, d, kw, steps, warmup, stream, k_steps=4):
+    """End to end as a pipelined serving loop runs it: every step copies its
+    packed inputs host -> device (pinned), runs the decode through the public
+    API and copies its ids device -> host.  k_steps consecutive steps (own
+    input and output buffers each) are captured once as one CUDA graph: the
+    decodes in order on the main stream, each step's copies on a second
+    stream, so that a step's H2D copy and D2H read overlap its neighbours'
+    decodes.  `serial` is one step per graph, copies and decode in order on
+    one stream.  No L2 flush: the key cache the decode streams (about 283 MB)
+    is larger than the L2.  Time = the whole run, host clock, device
+    synchronised on both sides."""
     dev = d["q"].device
-    buf = torch.empty(n, dtype=torch.uint8, device=dev)
-    q = buf[offs[0]:offs[0] + parts[0].nbytes].view(torch.bfloat16).view(d["q"].shape)
-    table = buf[offs[1]:offs[1] + parts[1].nbytes].view(torch.int32).view(d["table"].shape)
-    lens = buf[offs[2]:offs[2] + parts[2].nbytes].view(torch.int32).view(d["lens"].shape)
-    out = torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
-    o_h = torch.empty(out.shape, dtype=torch.int32).pin_memory()
+    host, slots, h2d = _packed_inputs(torch, wl, dev, k_steps)
+    outs = [torch.empty((wl.heads, wl.rows, wl.topk), dtype=torch.int32, device=dev)
+            for _ in range(k_steps)]
+    o_hs = [torch.empty(o.shape, dtype=torch.int32).pin_memory() for o in outs]
     ws = mm.new_workspace(mm.OP_DECODE, wl.heads, wl.num_reqs, wl.query_len, wl.max_seq_len,
                           wl.topk, dev)
     kw = {k: v for k, v in kw.items() if k not in ("out", "workspace", "stream")}
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        mm.decode(q, d["cache"], table, lens, out=out, workspace=ws, stream=stream, **kw)  # warm
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            buf.copy_(host, non_blocking=True)
-            mm.decode(q, d["cache"], table, lens, out=out, workspace=ws,
-                      stream=torch.cuda.current_stream(), **kw)
-            o_h.copy_(out, non_blocking=True)
+    copy = torch.cuda.Stream(device=dev)
+
+    def run(g, n_rep):
         for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(steps):
+        for _ in range(n_rep):
             g.replay()
         torch.cuda.synchronize()
-        el = time.perf_counter() - t0
-    assert np.array_equal(o_h.numpy(), out.cpu().numpy())
+        return time.perf_counter() - t0
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        _, q0, t0_, l0 = slots[0]
+        mm.decode(q0, d["cache"], t0_, l0, out=outs[0], workspace=ws, stream=stream, **kw)  # warm
+        torch.cuda.synchronize()
+        # serial: one step per graph
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            slots[0][0].copy_(host, non_blocking=True)
+            mm.decode(q0, d["cache"], t0_, l0, out=outs[0], workspace=ws,
+                      stream=torch.cuda.current_stream(), **kw)
+            o_hs[0].copy_(outs[0], non_blocking=True)
+        el1 = run(g1, steps)
+        # pipelined: k_steps per graph
+        gk = torch.cuda.CUDAGraph()
+        n_rep = max(1, steps // k_steps)
+        with torch.cuda.graph(gk, stream=stream):
+            main = torch.cuda.current_stream()
+            copy.wait_stream(main)   # fork the copy stream into the capture
+            ins = []
+            for i in range(k_steps):
+                with torch.cuda.stream(copy):
+                    slots[i][0].copy_(host, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(copy)
+                ins.append(ev)
+            for i in range(k_steps):
+                main.wait_event(ins[i])
+                _, q, tb, ln = slots[i]
+                mm.decode(q, d["cache"], tb, ln, out=outs[i], workspace=ws, stream=main, **kw)
+                done = torch.cuda.Event()
+                done.record(main)
+                copy.wait_event(done)
+                with torch.cuda.stream(copy):
+                    o_hs[i].copy_(outs[i], non_blocking=True)
+            main.wait_stream(copy)
+        elk = run(gk, n_rep)
+    want = outs[0].cpu().numpy()
+    for o_h in o_hs:
+        assert np.array_equal(o_h.numpy(), want)
     assert mm.get_device_error(stream) == 0, "device status word set"
-    return dict(value=wl.rows * steps / el, unit="rows/s",
-                h2d_bytes_per_step=int(sum(p.nbytes for p in parts)),
-                d2h_bytes_per_step=int(o_h.nbytes), steps=steps, ms_per_step=el / steps * 1e3,
+    total = n_rep * k_steps
+    return dict(value=wl.rows * total / elk, unit="rows/s",
+                h2d_bytes_per_step=h2d, d2h_bytes_per_step=int(o_hs[0].nbytes),
+                steps=total, ms_per_step=elk / total * 1e3,
                 timing="host clock around the whole run, device synchronised on both sides",
-                copies="per step one H2D of the packed inputs and one D2H of the ids, "
-                       "with the decode, replayed from one CUDA graph")
+                copies=f"per step one H2D of the packed inputs and one D2H of the ids; "
+                       f"{k_steps} steps per CUDA graph, each step's copies on a second stream "
+                       f"overlapping its neighbours' decodes",
+                serial=dict(value=wl.rows * steps / el1, unit="rows/s", steps=steps,
+                            ms_per_step=el1 / steps * 1e3,
+                            copies="one step per CUDA graph: H2D, decode, D2H in order on one stream"))
 
 
 def bench_e2e(mm, torch, wl, d, out, ws, kw, steps, warmup, flush, stream):
