@@ -199,24 +199,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16 bf16) is read from TMEM, lane m
-// holding row m as 8 columns of packed bf16 pairs.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Copy a 128-row x 256-bit block described by an shared-memory matrix
-// descriptor into TMEM lanes 0..127, 8 columns starting at taddr.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -224,29 +206,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp receives
-// lane (taddr.lane + i), columns taddr.col .. +15.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-
-// Wait for this thread's tcgen05.ld results; the registers are passed through
-// so the compiler cannot use them before the wait.
-__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns.
@@ -272,66 +231,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),       \
       "+r"(r[31])
 
-__device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r) : : "memory");
-}
-
 // One wait covering two outstanding 32-column loads.
 __device__ __forceinline__ void tmem_ld_wait32x2(uint32_t (&r)[32], uint32_t (&w)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r) : : "memory");
   asm volatile("" : MM3IDX_PLUS32(w) : : "memory");
 }
 
-// One wait covering four outstanding 32-column loads.
-__device__ __forceinline__ void tmem_ld_wait32x4(uint32_t (&r0)[32], uint32_t (&r1)[32],
-                                                 uint32_t (&r2)[32], uint32_t (&r3)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r0) : : "memory");
-  asm volatile("" : MM3IDX_PLUS32(r1) : : "memory");
-  asm volatile("" : MM3IDX_PLUS32(r2) : : "memory");
-  asm volatile("" : MM3IDX_PLUS32(r3) : : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns stored from registers: thread i
-// of the warp writes lane (taddr.lane + i), columns taddr.col .. +31.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-// Wait until this thread's tcgen05.st writes have been performed.
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Maximum of v over the 32 lanes of the warp (all lanes active, no NaN).
-__device__ __forceinline__ float warp_max_f32(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-// Fetch-and-add with acquire-release semantics at GPU scope: orders this
-// thread's earlier writes (and those it has observed) before the add, and the
-// writes released by earlier adds before this thread's later reads.
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 // --------------------------------------------------------------- misc helpers
-
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // Order-preserving map from fp32 to uint32 (after folding -0 into +0), so that
 // unsigned comparison of the images equals float comparison.
