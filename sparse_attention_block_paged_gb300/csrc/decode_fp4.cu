@@ -23,7 +23,7 @@
 //   * warp 1   : producer.  Per page, bulk copies of the 8 KB of codes and
 //                the 1 KB of scales into a ring of raw stages, the pages
 //                further ahead pulled into L2 first.
-//   * warps 2-9: compute.  Warp w takes pages w, w+8, ... of the CTA's
+//   * warps 2-11: compute.  Warp w takes pages w, w+10, ... of the CTA's
 //                stream: eight slabs of 16 tokens, each eight mma.sync per
 //                row tile over the dequantised codes, then the causal row
 //                max of the block (masked only in a request's last blocks),
@@ -50,10 +50,12 @@ constexpr int kCodeBytes = kBlock * kD / 2;    // 8 KB: 128 tokens x 64 B
 constexpr int kScaleBytes = kBlock * kD / 16;  // 1 KB: 128 tokens x 8 B
 constexpr int kStageBytes = kCodeBytes + kScaleBytes;
 constexpr int kSelWarp = 0, kProdWarp = 1, kCompWarp0 = 2;
-// Compute warps.  Measured on the 128-request NVFP4 batch: twelve (under
-// the 128-register cap of 14 warps) 0.328 ms, eight 0.305 ms.
+// Compute warps: ten, so that the block's twelve warps are three per SM
+// sub-partition and keep the 168-register cap.  Measured on the 128-request
+// NVFP4 batch: eight 0.304 ms, ten 0.290 ms, twelve (fourteen warps, a
+// 128-register cap) 0.328 ms.
 template <int NT>
-constexpr int comp_warps() { return 8; }
+constexpr int comp_warps() { return 10; }
 template <int NT>
 constexpr int threads_of() { return (kCompWarp0 + comp_warps<NT>()) * 32; }
 constexpr int kAhead = 16;                     // pages pulled into L2 ahead of the ring (< 32)
