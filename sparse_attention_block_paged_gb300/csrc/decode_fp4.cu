@@ -53,7 +53,10 @@ constexpr int kSelWarp = 0, kProdWarp = 1, kCompWarp0 = 2;
 // Compute warps: ten, so that the block's twelve warps are three per SM
 // sub-partition and keep the 168-register cap.  Measured on the 128-request
 // NVFP4 batch: eight 0.304 ms, ten 0.290 ms, twelve (fourteen warps, a
-// 128-register cap) 0.328 ms.
+// 128-register cap) 0.328 ms.  Pages go round-robin; dealing more of them to
+// the warps on the two sub-partitions that also hold the selector and the
+// producer (a quarter of the pages per sub-partition) measured 0.305 ms: the
+// selector takes pages in order and waits on the warps given more.
 template <int NT>
 constexpr int comp_warps() { return 10; }
 template <int NT>
