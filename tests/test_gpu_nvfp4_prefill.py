@@ -39,7 +39,7 @@ CASES = [
     (1, 1, 700, 1, 4, 1, 1, 700, 700),          # whole-request prefill, ragged tail
     (2, 2, 300, 2, 16, 1, 2, 300, 2000),        # chunked: prefix + 300 new tokens
     (3, 3, 129, 1, 8, 2, 2, 129, 5000),
-    (4, 1, 1000, 4, 32, 2, 3, 3000, 3000),
+    (4, 1, 1000, 4, 32, 2, 3, 9000, 9000),      # 63-71 blocks a row: 32-key lists
 ]
 
 
