@@ -130,9 +130,25 @@ __device__ __forceinline__ int64_t units_before(const ReqGeom& g, int qt) {
   return n;
 }
 
+// In score mode a query tile occupies two positions ahead of its units in
+// the list the CTAs share out: starting a tile costs a CTA a query-tile load
+// that the MMAs wait for, which its unit count does not show, and the first
+// CTAs' shares span dozens of small tiles (a clock64 trace of the 32K causal
+// prefill: the CTA with 20 tiles waited 253 cycles a unit for query tiles,
+// the median CTA 17, and ended 12 us after the median).  Score call on the
+// 32K prefill: 115.4 us without the cost, 104.7 / 102.6 / 103.3 / 104.9 us
+// with 1 / 2 / 3 / 4 positions.  The selecting kernel's epilogue is its
+// bottleneck and hides the query loads, so there tiles cost nothing (with a
+// cost of one the fused steps measured 1-5 % slower).
+__device__ __forceinline__ int64_t pos_before(const ReqGeom& g, int qt, int cost) {
+  return units_before(g, qt) + static_cast<int64_t>(cost) * qt;
+}
+
 // Iterates this CTA's share of the unit list (request, head, query tile,
 // pair of key blocks).  The list holds exactly each request's units, so the
 // shares are computed on the device: total() and init() are warp-collective.
+// Shares are ranges of positions (units plus the tiles' costs); a share's
+// units are those whose positions it holds.
 // The state is kept small: the epilogue's loop also holds a 128-column
 // accumulator row in registers.
 struct UnitIter {
@@ -140,10 +156,12 @@ struct UnitIter {
   int req = 0, head = 0, qt = 0, p = 0, np = 0, nvis = 0;
   int tile = 0;     // index of the (request, head, tile) in the batch
   int64_t u = 0;    // index of the unit in the batch's list
+  int64_t ulo = 0, uhi = 0;  // the share's units [ulo, uhi)
+  int cost = 0;              // positions a query tile takes ahead of its units
   ReqGeom g;
 
-  // Total units of the batch (all lanes get it); *tiles gets its tiles.
-  __device__ static int64_t total(const PrefillArgs& a, int* tiles = nullptr) {
+  // Total positions of the batch (all lanes get it); *tiles gets its tiles.
+  __device__ static int64_t total(const PrefillArgs& a, int cost, int* tiles = nullptr) {
     const int lane = threadIdx.x & 31;
     int64_t sum = 0;
     int nt = 0;
@@ -151,7 +169,7 @@ struct UnitIter {
       const int i = base + lane;
       if (i < a.num_reqs) {
         const ReqGeom gi = req_geom(a, i);
-        sum += units_before(gi, gi.qtiles);
+        sum += pos_before(gi, gi.qtiles, cost);
         nt += gi.qtiles;
       }
     }
@@ -169,62 +187,84 @@ struct UnitIter {
     np = max(1, (nvis + 1) >> 1);
   }
 
-  // Position at unit lo of the list; the share ends at hi.
-  __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi) {
-    left = static_cast<int>(hi - lo);
-    u = lo;
-    if (left <= 0) return;
+  // The index of the first unit at position x or later (the batch's unit
+  // count when there is none), with its request, head, tile and place.
+  __device__ int64_t unit_at(const PrefillArgs& a, int64_t x, int& r, int& hd, int& t, int& pp,
+                             int& tl) {
     const int lane = threadIdx.x & 31;
-    int64_t acc = 0;  // units of the requests before `base`
-    int tacc = 0;     // tiles of the requests before `base`
+    int64_t pacc = 0, uacc = 0;  // positions and units of the requests before `base`
+    int tacc = 0;                // tiles of the requests before `base`
+    r = a.num_reqs;
     for (int base = 0; base < a.num_reqs; base += 32) {
       const int i = base + lane;
-      int64_t mine = 0;
-      int tmine = 0;
+      int64_t pm = 0, um = 0;
+      int tm = 0;
       if (i < a.num_reqs) {
         const ReqGeom gi = req_geom(a, i);
-        mine = units_before(gi, gi.qtiles) * a.heads;
-        tmine = gi.qtiles * a.heads;
+        pm = pos_before(gi, gi.qtiles, cost) * a.heads;
+        um = units_before(gi, gi.qtiles) * a.heads;
+        tm = gi.qtiles * a.heads;
       }
-      int64_t incl = mine;
-      int tincl = tmine;
+      int64_t pin = pm, uin = um;
+      int tin = tm;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        const int ty = __shfl_up_sync(0xffffffffu, tincl, o);
+        const int64_t py = __shfl_up_sync(0xffffffffu, pin, o);
+        const int64_t uy = __shfl_up_sync(0xffffffffu, uin, o);
+        const int ty = __shfl_up_sync(0xffffffffu, tin, o);
         if (lane >= o) {
-          incl += y;
-          tincl += ty;
+          pin += py;
+          uin += uy;
+          tin += ty;
         }
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > lo);
+      const unsigned hit = __ballot_sync(0xffffffffu, pacc + pin > x);
       if (hit != 0u) {
         const int l = __ffs(hit) - 1;
-        req = base + l;
-        acc += __shfl_sync(0xffffffffu, incl - mine, l);
-        tacc += __shfl_sync(0xffffffffu, tincl - tmine, l);
+        r = base + l;
+        pacc += __shfl_sync(0xffffffffu, pin - pm, l);
+        uacc += __shfl_sync(0xffffffffu, uin - um, l);
+        tacc += __shfl_sync(0xffffffffu, tin - tm, l);
         break;
       }
-      acc += __shfl_sync(0xffffffffu, incl, 31);
-      tacc += __shfl_sync(0xffffffffu, tincl, 31);
+      pacc += __shfl_sync(0xffffffffu, pin, 31);
+      uacc += __shfl_sync(0xffffffffu, uin, 31);
+      tacc += __shfl_sync(0xffffffffu, tin, 31);
     }
-    g = req_geom(a, req);
-    const int64_t uph = units_before(g, g.qtiles);  // units per head
-    int64_t off = lo - acc;
-    head = static_cast<int>(off / uph);
-    off -= head * uph;
-    // the tile holding unit `off`: the last qt with units_before(qt) <= off
-    int t_lo = 0, t_hi = g.qtiles - 1;
+    if (r >= a.num_reqs) return uacc;
+    const ReqGeom gr = req_geom(a, r);
+    const int64_t pph = pos_before(gr, gr.qtiles, cost), uph = units_before(gr, gr.qtiles);
+    int64_t off = x - pacc;
+    hd = static_cast<int>(off / pph);
+    off -= hd * pph;
+    // the tile holding position `off`: the last qt with pos_before(qt) <= off
+    int t_lo = 0, t_hi = gr.qtiles - 1;
     while (t_lo < t_hi) {
       const int mid = (t_lo + t_hi + 1) >> 1;
-      if (units_before(g, mid) <= off) t_lo = mid;
+      if (pos_before(gr, mid, cost) <= off) t_lo = mid;
       else t_hi = mid - 1;
     }
-    qt = t_lo;
-    p = static_cast<int>(off - units_before(g, qt));
-    tile = tacc + head * g.qtiles + qt;
+    t = t_lo;
+    pp = static_cast<int>(max(off - pos_before(gr, t, cost) - cost, int64_t{0}));  // past the tile's cost
+    tl = tacc + hd * gr.qtiles + t;
+    return uacc + hd * uph + units_before(gr, t) + pp;
+  }
+
+  // Position at the share [lo, hi) of the list (in positions, `cost` per
+  // tile): its first unit, and the count of its units.
+  __device__ void init(const PrefillArgs& a, int64_t lo, int64_t hi, int tile_cost) {
+    cost = tile_cost;
+    int r1, h1, t1, p1, tl1;
+    const int64_t u_lo = unit_at(a, lo, req, head, qt, p, tile);
+    const int64_t u_hi = unit_at(a, hi, r1, h1, t1, p1, tl1);
+    left = static_cast<int>(u_hi - u_lo);
+    u = ulo = u_lo;
+    uhi = u_hi;
+    if (left <= 0) return;
+    g = req_geom(a, req);
     load_tile();
   }
+
   __device__ __forceinline__ bool valid() const { return left > 0; }
   // Next unit; true when it starts a new query tile.
   __device__ __forceinline__ bool advance(const PrefillArgs& a) {
@@ -250,12 +290,13 @@ struct UnitIter {
   }
 };
 
-// Whether CTA c's share [total*c/G, total*(c+1)/G) holds any unit.
+// Whether CTA c's share [total*c/G, total*(c+1)/G) of the positions is not
+// empty.
 __device__ __forceinline__ bool has_units(int c, int64_t total, int64_t G) {
   return total * (c + 1) / G > total * c / G;
 }
 
-// The CTA whose share [total*c/G, total*(c+1)/G) holds unit x.
+// The CTA whose share [total*c/G, total*(c+1)/G) holds position x.
 __device__ __forceinline__ int cta_of(int64_t x, int64_t total, int64_t G) {
   return static_cast<int>(((x + 1) * G - 1) / total);
 }
@@ -319,18 +360,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // selection's merge CTAs would sit on the SMs waiting, beside this grid,
   // which measured 20 % slower; they launch when this grid completes.
 
-  // This CTA's equal share of the batch's units (every warp computes it).
+  // This CTA's equal share of the batch's positions (every warp computes it).
+  constexpr int kTileCost = kSelect ? 0 : 2;
   UnitIter U;
   int64_t total = 0, share_lo = 0, share_hi = 0;
   const int64_t G = gridDim.x;
   if (warp != 1) {
     int tiles = 0;
-    total = UnitIter::total(a, &tiles);
+    total = UnitIter::total(a, kTileCost, &tiles);
     // the selection's merge reads the batch's tile count from the first record
     if (kSelect && blockIdx.x == 0 && warp == 0 && lane == 0) a.tile_rec[0] = tiles;
     share_lo = total * blockIdx.x / G;
     share_hi = total * (blockIdx.x + 1) / G;
-    U.init(a, share_lo, share_hi);
+    U.init(a, share_lo, share_hi, kTileCost);
   }
 
   if (a.cu != nullptr && blockIdx.x == 0 && warp == 0) {
@@ -580,9 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < TK; ++k) dst[k * 128] = list.v[k];
           }
           const int64_t tfirst = U.u - U.p, tlast = tfirst + U.np - 1;
-          if (warp == 2 && lane == 0 && tfirst >= share_lo) {
+          if (warp == 2 && lane == 0 && tfirst >= U.ulo) {
             int32_t* rec = a.tile_rec + (static_cast<int64_t>(U.tile) + 1) * kTileRecInts;
-            rec[1] = tlast < share_hi ? static_cast<int>(blockIdx.x) : cta_of(tlast, total, G);
+            // the tile's last unit sits at position tlast + cost * (tile + 1)
+            rec[1] = tlast < U.uhi ? static_cast<int>(blockIdx.x)
+                                   : cta_of(tlast + static_cast<int64_t>(U.cost) * (U.tile + 1),
+                                            total, G);
             rec[2] = U.head;
             rec[3] = U.g.qbeg;
             rec[4] = U.g.ql;
@@ -654,7 +699,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 1) prefill_merge_kernel(cons
   } else {
     RegList<TK> m;
     m.clear();
-    // With at least as many units as CTAs every share holds some (no check).
+    // With at least as many positions as CTAs every share holds some, and a
+    // CTA between c0 and c1 holds units of this tile (a tile's cost
+    // positions come before its first unit): no check.
     const bool dense = total >= a.grid;
     for (int cj = c0; cj <= c1; ++cj) {
       if (!dense && !has_units(cj, total, a.grid)) continue;
