@@ -528,6 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* srow = nullptr;   // score mode: the row's scores
     int f_lo = 0, l_lo = 0;  // select mode: the row's forced blocks [0, f_lo), [l_lo, c]
     RegList<TK> list;  // select mode: best non-forced keys of the tile so far
+    // 32-key lists take offers eight at a time (newest first, 0 = none): a
+    // warp's 32 rows rarely all decline an offer, so one insertion per offer
+    // moves all 32 slots nearly every unit.  The accumulator is then read 32
+    // columns at a time to leave registers for the batch.
+    constexpr bool kBatch = kSelect && TK == 32;
+    constexpr bool kNarrow = kSelect && TK == 32;
+    uint64_t batch[8];
+    int nbatch = 0;  // offers in the batch (the same for the warp)
     bool new_tile = true;
     for (; ok && U.valid(); new_tile = U.advance(a)) {
       if (new_tile) {
@@ -540,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           f_lo = F.f_lo;
           l_lo = F.l_lo;
           list.clear();
+          if constexpr (kBatch) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) batch[j] = 0ull;
+            nbatch = 0;
+          }
         } else {
           srow = a.score + U.head * a.s_head + row * a.s_row;
         }
@@ -565,6 +578,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mine) {
           const uint32_t taddr =
               tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * 256 + team * 128;
+          if constexpr (kNarrow) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              uint32_t v0[32];
+              tmem_ld32(taddr + 32 * h, v0);
+              tmem_ld_wait32(v0);
+              if (lim >= 127) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                  m0 = fmax3(m0, __uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
+                  m1 = fmax3(m1, __uint_as_float(v0[k + 2]), __uint_as_float(v0[k + 3]));
+                }
+              } else if (lim >= 0) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                  if (32 * h + k <= lim) m0 = fmaxf(m0, __uint_as_float(v0[k]));
+              }
+            }
+          } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t v0[32], v1[32];
@@ -587,11 +619,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        if (mine && row_ok) {
+        if constexpr (kBatch) {
+          uint64_t key = 0ull;
+          if (mine && row_ok && b >= f_lo && b < l_lo) {
+            const float score =
+                (page >= 0 && page < a.num_pages) ? fmaxf(m0, m1) * a.sm_scale : -INFINITY;
+            key = make_key(score, b);
+          }
+#pragma unroll
+          for (int j = 7; j > 0; --j) batch[j] = batch[j - 1];
+          batch[0] = key;
+          if (++nbatch == 8) {
+            list.merge8(batch);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) batch[j] = 0ull;
+            nbatch = 0;
+          }
+        } else if (mine && row_ok) {
           const float score =
               (page >= 0 && page < a.num_pages) ? fmaxf(m0, m1) * a.sm_scale : -INFINITY;
           if constexpr (kSelect) {
@@ -613,6 +662,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // holds the tile's first unit also leaves the tile's record.  A
         // dependent kernel merges the lists after this one.
         if (U.p == U.np - 1 || U.left == 1) {
+          if constexpr (kBatch) {
+            if (nbatch > 0) {
+              list.merge8(batch);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) batch[j] = 0ull;
+              nbatch = 0;
+            }
+          }
           if (U.nvis > a.topk) {
             // Key-major slot [TK][128 rows]: a warp's 32 rows store 256
             // contiguous bytes per key.

@@ -231,6 +231,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),       \
       "+r"(r[31])
 
+// The wait for one outstanding 32-column load.
+__device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r) : : "memory");
+}
+
 // One wait covering two outstanding 32-column loads.
 __device__ __forceinline__ void tmem_ld_wait32x2(uint32_t (&r)[32], uint32_t (&w)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : MM3IDX_PLUS32(r) : : "memory");

@@ -16,9 +16,9 @@
 // at a time (eight per lane), as unique 64-bit keys (score bits above the
 // block id, so higher score then lower id wins).  The best m so far ride
 // along in lanes 0..m-1.  Per chunk:
-//   1. each lane's largest score; m rounds of a warp-wide max give T, the
-//      m-th largest of these 32 -- at least m scores are >= T, so every key
-//      of the top m has a score >= T;
+//   1. each lane's largest score (its best four when m > 16); m rounds of a
+//      warp-wide max give T, the m-th largest of these -- at least m scores
+//      are >= T, so every key of the top m has a score >= T;
 //   2. the keys with scores >= T (typically about m + a few) are compacted
 //      into one key per lane through shared memory and sorted; lanes 0..m-1
 //      keep the best;
@@ -157,24 +157,60 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
         const int idx = base + p * 32 + lane;
         v[p] = idx < F.l_lo ? __ldg(srow + idx) : -INFINITY;
       }
-      // This lane's largest score (ordered bits; 0 = none) among its
-      // candidates and its best-so-far key.
-      float fm = v[0];
-#pragma unroll
-      for (int p = 1; p < kPer; ++p) fm = fmaxf(fm, v[p]);
-      const bool any = base + lane < F.l_lo;
-      uint32_t lm = any ? ordered_bits(fm) : 0u;
       const uint32_t rs = static_cast<uint32_t>(run >> 32);
-      lm = rs > lm ? rs : lm;
-      // T: the m-th largest of the 32 lane maxima (equal maxima leave
-      // together, which only lowers T).  At least m lanes hold a score (the
-      // best-so-far list, or, in the first chunk, more than m candidates).
-      uint32_t rem = lm, T = lm;
-      for (int r = 0; r < m; ++r) {
-        const uint32_t mx = __reduce_max_sync(kFull, rem);
-        if (mx == 0u) break;
-        T = mx;
-        if (rem == mx) rem = 0u;
+      uint32_t T;
+      if (m <= 16) {
+        // This lane's largest score (ordered bits; 0 = none) among its
+        // candidates and its best-so-far key.
+        float fm = v[0];
+#pragma unroll
+        for (int p = 1; p < kPer; ++p) fm = fmaxf(fm, v[p]);
+        const bool any = base + lane < F.l_lo;
+        uint32_t lm = any ? ordered_bits(fm) : 0u;
+        lm = rs > lm ? rs : lm;
+        // T: the m-th largest of the 32 lane maxima (equal maxima leave
+        // together, which only lowers T).  At least m lanes hold a score (the
+        // best-so-far list, or, in the first chunk, more than m candidates).
+        uint32_t rem = lm;
+        T = lm;
+        for (int r = 0; r < m; ++r) {
+          const uint32_t mx = __reduce_max_sync(kFull, rem);
+          if (mx == 0u) break;
+          T = mx;
+          if (rem == mx) rem = 0u;
+        }
+      } else {
+        // Larger m: the m-th largest of the lanes' four best scores each
+        // (a subset of the chunk's scores and the best-so-far keys, so at
+        // least m scores reach it).  With the lane maxima alone, about 60 of
+        // 256 N(0,1) scores reach the 29th-largest lane maximum and the
+        // selection falls back to m rounds of a 64-bit warp max; the
+        // 29th-largest of the lanes' best four lets about 29 through.
+        uint32_t c[4] = {0u, 0u, 0u, 0u};   // descending
+        auto ins = [&](uint32_t x) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t hi = c[k] > x ? c[k] : x, lo = c[k] > x ? x : c[k];
+            c[k] = hi;
+            x = lo;
+          }
+        };
+#pragma unroll
+        for (int p = 0; p < kPer; ++p)
+          if (base + p * 32 + lane < F.l_lo) ins(ordered_bits(v[p]));
+        ins(rs);
+        T = c[0];
+        for (int r = 0; r < m; ++r) {
+          const uint32_t mx = __reduce_max_sync(kFull, c[0]);
+          if (mx == 0u) break;
+          T = mx;
+          if (c[0] == mx) {   // this lane's best leaves (equal ones together)
+            c[0] = c[1];
+            c[1] = c[2];
+            c[2] = c[3];
+            c[3] = 0u;
+          }
+        }
       }
       const bool run_in = run != 0ull && rs >= T;
       uint32_t hit = 0;  // bit p: v[p] survives

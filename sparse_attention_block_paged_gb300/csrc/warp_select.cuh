@@ -73,6 +73,32 @@ struct RegList {
   __device__ __forceinline__ void merge_sorted(const uint64_t (&b)[TK]) {
 #pragma unroll
     for (int k = 0; k < TK; ++k) v[k] = v[k] > b[TK - 1 - k] ? v[k] : b[TK - 1 - k];
+    clean();
+  }
+  // The same for eight keys in any order (zeros for none): b is sorted first
+  // (an optimal 19-comparator network for eight inputs, Knuth, The Art of
+  // Computer Programming vol. 3, 5.3.4), then taken as b padded with zeros:
+  // only the last eight slots meet a nonzero key.  About 107 compare-
+  // exchanges for eight keys, where eight insertions move all TK slots each.
+  __device__ __forceinline__ void merge8(uint64_t (&b)[8]) {
+    constexpr int kNet[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                                 {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                                 {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int n = 0; n < 19; ++n) {
+      const uint64_t x = b[kNet[n][0]], y = b[kNet[n][1]];
+      b[kNet[n][0]] = x > y ? x : y;
+      b[kNet[n][1]] = x > y ? y : x;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = TK - 8 + j;
+      v[k] = v[k] > b[7 - j] ? v[k] : b[7 - j];
+    }
+    clean();
+  }
+  // Sort a bitonic list descending (half-cleaners, TK/2 apart down to 1).
+  __device__ __forceinline__ void clean() {
 #pragma unroll
     for (int half = TK / 2; half > 0; half >>= 1) {
 #pragma unroll

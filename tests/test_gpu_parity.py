@@ -169,21 +169,32 @@ def test_fused_prefill_selection_equals_two_kernels(mm, topk, init, local):
     assert mm.get_device_error() == 0
 
 
-def test_topk_selector_bit_exact_on_same_scores(mm):
-    """Given the same fp32 scores, selection must agree bit for bit."""
+@pytest.mark.parametrize("topk,ties", [(16, "some"), (4, "some"), (24, "some"), (32, "some"),
+                                       (32, "none"), (20, "many"), (32, "all")])
+def test_topk_selector_bit_exact_on_same_scores(mm, topk, ties):
+    """Given the same fp32 scores, selection must agree bit for bit.  The
+    selector thresholds each 256-block chunk on the lane maxima (topk - forced
+    <= 16) or on the lanes' best four (above); "many" and "all" put more than
+    32 scores at the threshold, which takes its one-at-a-time path."""
     import torch
-    rng = np.random.default_rng(5)
-    seq = rng.integers(1, 9000, size=37).astype(np.int32)
-    qlen, heads, topk = 3, 2, 16
+    rng = np.random.default_rng(5 + topk)
+    seq = rng.integers(1, 20000 if topk > 16 else 9000, size=37).astype(np.int32)
+    qlen, heads = 3, 2
     seq = np.maximum(seq, qlen)
     msl = int(seq.max())
     W_ = -(-msl // 128)
     sc = rng.standard_normal((heads, len(seq) * qlen, W_)).astype(np.float32)
-    sc[:, :, ::7] = sc[:, :, 3:4]          # plenty of exact ties
+    if ties == "some":
+        sc[:, :, ::7] = sc[:, :, 3:4]          # plenty of exact ties
+    elif ties == "many":
+        sc[:, :, ::3] = np.float32(2.5)        # a third of the blocks tie near the top
+    elif ties == "all":
+        sc[:] = np.float32(0.75)               # the lowest ids win
     want = oracle.select_problem(sc.astype(np.float64), seq, qlen, topk, 1, 2)
     got = mm.topk(torch.from_numpy(sc).cuda(), torch.from_numpy(seq).cuda(), query_len=qlen,
                   max_seq_len=msl, topk=topk, init_blocks=1, local_blocks=2)
     np.testing.assert_array_equal(got.cpu().numpy(), want)
+    assert mm.get_device_error() == 0
 
 
 # ------------------------------------------------------------------ NVFP4
