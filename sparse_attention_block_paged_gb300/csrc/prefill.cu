@@ -104,7 +104,7 @@ __device__ __forceinline__ ReqGeom req_geom(const PrefillArgs& a, int i) {
 }
 
 // Units of one query tile: its visible blocks in pairs; at least one, so
-// that every tile's rows get their -inf fill.
+// that every tile is visited (in select mode, its record for the merge).
 __device__ __forceinline__ int tile_units(const ReqGeom& g, int qt) {
   return max(1, (tile_blocks(g.prefix, qt, g.ql) + 1) >> 1);
 }
@@ -652,9 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it;
         acc ^= 1u;
       }
-      // The tile's last scheduled unit: blocks past the visible ones hold
-      // -inf.  Each warp of team 0 fills its 32 rows one row at a time, lanes
-      // on consecutive blocks, so the stores coalesce.
       if constexpr (kSelect) {
         // The last unit of the tile in this CTA's share: the warp's 32 lists
         // (of this team's blocks) go to the tile's slot in the workspace,
