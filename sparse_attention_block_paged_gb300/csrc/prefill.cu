@@ -752,11 +752,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 1) prefill_merge_kernel(cons
     for (int t = 0; t < a.topk; ++t) srow[t] = t <= c ? t : -1;
   } else {
     RegList<TK> m;
-    m.clear();
     // With at least as many positions as CTAs every share holds some, and a
     // CTA between c0 and c1 holds units of this tile (a tile's cost
     // positions come before its first unit): no check.
     const bool dense = total >= a.grid;
+    bool first = true;   // the first list is taken as it is
     for (int cj = c0; cj <= c1; ++cj) {
       if (!dense && !has_units(cj, total, a.grid)) continue;
       // The two teams' slots, key-major: the warp's 32 rows read 256
@@ -769,17 +769,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 1) prefill_merge_kernel(cons
         l0[k] = __ldcg(s0 + k * 128);
         l1[k] = __ldcg(s1 + k * 128);
       }
-      m.merge_sorted(l0);
+      if (first) {
+#pragma unroll
+        for (int k = 0; k < TK; ++k) m.v[k] = l0[k];
+        first = false;
+      } else {
+        m.merge_sorted(l0);
+      }
       m.merge_sorted(l1);
     }
+    if (first) m.clear();   // no CTA held units of the tile (a malformed record)
     write_row_lane<TK>(m.v, c, a.init_blocks, a.local_blocks, a.topk, srow);
   }
   __syncwarp();
+  // Row by row, lane = column (topk <= 32): contiguous stores, conflict-free
+  // shared-memory reads.
   int32_t* out = a.ids + head * a.i_head + static_cast<int64_t>(qbeg + row0) * a.i_row;
-  for (int idx = lane; idx < nrows * a.topk; idx += 32) {
-    const int rr = idx / a.topk, k = idx - rr * a.topk;
-    out[rr * a.i_row + k] = s_rows[wib][rr][k];
-  }
+  if (lane < a.topk)
+    for (int rr = 0; rr < nrows; ++rr) out[rr * a.i_row + lane] = s_rows[wib][rr][lane];
 }
 
 template <bool kSelect, int TK>

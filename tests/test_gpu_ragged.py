@@ -48,6 +48,9 @@ CASES = [
     (3, [1000, 0, 0, 700], [0, 5, 9, 3000], 1, 8, 2, 2),
     (4, [128, 128, 128], [128, 0, 383], 4, 32, 2, 3),
     (5, [2000, 31, 500, 1, 64, 900], [6000, 0, 2500, 10000, 64, 12], 2, 16, 1, 2),
+    # 32-key lists (batched offers) over CTA shares that start and end
+    # inside tiles of several requests
+    (6, [500, 3, 900, 257], [9000, 12000, 4000, 6000], 1, 27, 1, 2),
 ]
 
 
