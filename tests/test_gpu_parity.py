@@ -366,6 +366,16 @@ def test_full_size_prefill_topk32_sampled(mm):
     ids = run_prefill(mm, wl)
     assert mm.get_device_error() == 0
     _prefill_rows_check(wl, prefill_sample_rows(wl.rows), ids, where="prefill topk32")
+    # Every row: the score call followed by the standalone selector (its
+    # lanes' best-four threshold at topk 32) picks the same ids bit for bit.
+    d = to_device(wl)
+    sc = mm.score(d["q"], d["cache"], d["table"], d["lens"], query_len=wl.query_len,
+                  max_seq_len=wl.max_seq_len, sm_scale=wl.sm_scale)
+    two = mm.topk(sc, d["lens"], query_len=wl.query_len, max_seq_len=wl.max_seq_len,
+                  topk=wl.topk, init_blocks=wl.init_blocks,
+                  local_blocks=wl.local_blocks).cpu().numpy()
+    assert mm.get_device_error() == 0
+    np.testing.assert_array_equal(ids, two)
 
 
 def test_full_size_nvfp4_prefill_sampled(mm):
