@@ -52,10 +52,7 @@ __device__ __forceinline__ int req_blocks(const DecodeArgs& a, int i) {
 // split, a cross-CTA merge, which the blocks alone do not count.  The extra
 // positions come first and hold no work.  Measured on one GB300 over 0-20:
 // 6 gave high-batch 171 -> 163 us; the spec-decode batch is within noise
-// over 0-12 (57.3-58.7 us, graph replays, two sweeps), although its CTAs
-// inside one long request stream three more units than those with two
-// requests: while every CTA streams the kernel is bound by HBM, and the
-// bandwidth goes to the CTAs still streaming.  Larger values lose again.
+// over 0-12 (57.3-58.6 us, graph replays); larger values lose again.
 constexpr int kSegCost = 6;
 
 __device__ __forceinline__ int req_slots(const DecodeArgs& a, int i) {
