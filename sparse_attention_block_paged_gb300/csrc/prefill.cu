@@ -138,8 +138,13 @@ __device__ __forceinline__ int64_t units_before(const ReqGeom& g, int qt) {
 // the median CTA 17, and ended 12 us after the median).  Score call on the
 // 32K prefill: 115.4 us without the cost, 104.7 / 102.6 / 103.3 / 104.9 us
 // with 1 / 2 / 3 / 4 positions.  The selecting kernel's epilogue is its
-// bottleneck and hides the query loads, so there tiles cost nothing (with a
-// cost of one the fused steps measured 1-5 % slower).
+// bottleneck and hides the query loads, so with 16-key lists tiles cost
+// nothing (with a cost of one the fused steps measured 1-5 % slower).  With
+// 32-key lists the end of a tile costs the epilogue the partial batch's
+// merge and the 32-key list stores, about two units' work (a clock64 trace
+// of the 32K prefill at topk 32: CTAs ended at a median of 110.8 us, the
+// last at 132.4 us); two positions a tile: step 153.3 -> 137.9 us (1 / 2 /
+// 3 / 4 positions: 139.3 / 137.9 / 138.7 / 139.7 us).
 __device__ __forceinline__ int64_t pos_before(const ReqGeom& g, int qt, int cost) {
   return units_before(g, qt) + static_cast<int64_t>(cost) * qt;
 }
@@ -361,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which measured 20 % slower; they launch when this grid completes.
 
   // This CTA's equal share of the batch's positions (every warp computes it).
-  constexpr int kTileCost = kSelect ? 0 : 2;
+  constexpr int kTileCost = kSelect ? (TK == 32 ? 2 : 0) : 2;
   UnitIter U;
   int64_t total = 0, share_lo = 0, share_hi = 0;
   const int64_t G = gridDim.x;
