@@ -138,8 +138,11 @@ __device__ __forceinline__ int64_t units_before(const ReqGeom& g, int qt) {
 // the median CTA 17, and ended 12 us after the median).  Score call on the
 // 32K prefill: 115.4 us without the cost, 104.7 / 102.6 / 103.3 / 104.9 us
 // with 1 / 2 / 3 / 4 positions.  The selecting kernel's epilogue is its
-// bottleneck and hides the query loads, so with 16-key lists tiles cost
-// nothing (with a cost of one the fused steps measured 1-5 % slower).  With
+// bottleneck and hides most of the query loads: with 16-key lists a tile
+// takes one position in uniform batches (32K causal prefill step 121.9 ->
+// 119.7 us, NVFP4 prefill 127.5 -> 126.0 us, three runs each on one box;
+// two positions measured no better) and none in ragged ones (the chunked
+// batch measured 94.3 us without, 96.1 us with one).  With
 // 32-key lists the end of a tile costs the epilogue the partial batch's
 // merge and the 32-key list stores, about two units' work (a clock64 trace
 // of the 32K prefill at topk 32: CTAs ended at a median of 110.8 us, the
@@ -366,18 +369,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which measured 20 % slower; they launch when this grid completes.
 
   // This CTA's equal share of the batch's positions (every warp computes it).
-  constexpr int kTileCost = kSelect ? (TK == 32 ? 2 : 0) : 2;
+  const int tile_cost = kSelect ? (TK == 32 ? 2 : (a.cu == nullptr ? 1 : 0)) : 2;
   UnitIter U;
   int64_t total = 0, share_lo = 0, share_hi = 0;
   const int64_t G = gridDim.x;
   if (warp != 1) {
     int tiles = 0;
-    total = UnitIter::total(a, kTileCost, &tiles);
+    total = UnitIter::total(a, tile_cost, &tiles);
     // the selection's merge reads the batch's tile count from the first record
     if (kSelect && blockIdx.x == 0 && warp == 0 && lane == 0) a.tile_rec[0] = tiles;
     share_lo = total * blockIdx.x / G;
     share_hi = total * (blockIdx.x + 1) / G;
-    U.init(a, share_lo, share_hi, kTileCost);
+    U.init(a, share_lo, share_hi, tile_cost);
   }
 
   if (a.cu != nullptr && blockIdx.x == 0 && warp == 0) {
