@@ -362,9 +362,7 @@ int mm3idx_prefill_ragged(const mm3idx_problem_t *p, const int32_t *cu_seqlens_q
  * one row per query row of the whole batch.  Workspace:
  * mm3idx_forward_workspace_bytes(...) bytes, 256-byte aligned, zero-filled
  * before its first use (its decode part follows mm3idx_decode's rules).
- * The decode kernel runs first; the prefill's first kernel is launched as a
- * programmatic dependent of it, so that it starts on the SMs the decode
- * frees, and completes only after the decode has.
+ * The decode kernel runs first, then the prefill's kernels, in stream order.
  */
 int mm3idx_forward(const mm3idx_problem_t *p, int32_t num_decodes,
                    const int32_t *prefill_cu_seqlens_q, int32_t prefill_total_q,

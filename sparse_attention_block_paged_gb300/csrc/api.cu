@@ -359,9 +359,8 @@ struct PrefillSelect {
 
 int prefill_scores(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_q, float* out,
                    int64_t head_stride, int64_t row_stride, int sms, int32_t* status,
-                   cudaStream_t s, const PrefillSelect* sel = nullptr, bool overlap = false) {
+                   cudaStream_t s, const PrefillSelect* sel = nullptr) {
   PrefillArgs a{};
-  a.overlap = overlap ? 1 : 0;
   if (sel) {
     a.topk = sel->topk;
     a.init_blocks = sel->init_blocks;
@@ -460,7 +459,7 @@ int score_then_fill(const mm3idx_problem_t* p, const int32_t* cu, int32_t total_
 // range, so the bf16 scorer treats that block as it treats a bad page (no
 // visible tokens).  Requires num_reqs * cdiv(max_seq_len,128) <= INT_MAX / 128.
 int dequant_copy(const mm3idx_problem_t* p, uint8_t* dst, DeviceInfo* dev, cudaStream_t s,
-                 mm3idx_problem_t* q, bool overlap = false) {
+                 mm3idx_problem_t* q) {
   const int64_t width = cdiv(p->max_seq_len, kBlock);
   const int64_t slots = static_cast<int64_t>(p->num_reqs) * width;
   DequantArgs d{};
@@ -476,7 +475,6 @@ int dequant_copy(const mm3idx_problem_t* p, uint8_t* dst, DeviceInfo* dev, cudaS
   d.pages_out = reinterpret_cast<uint16_t*>(dst);
   d.table_out = reinterpret_cast<int32_t*>(dst + slots * kBlock * kD * 2);
   d.status = dev->status;
-  d.overlap = overlap ? 1 : 0;
   int rc = cuda_status(launch_dequant_pages(d, dev->sms, s));
   if (rc) return rc;
   *q = *p;
@@ -571,13 +569,11 @@ int run_topk(const float* score, int64_t sh, int64_t sr, int32_t heads, const in
 // Prefill: the scorer selects as it goes (no score tensor), a dependent
 // kernel merges its lists.  NVFP4 keys are first dequantised, once per
 // page, into a bf16 copy in the workspace.  cu == nullptr: query_len rows
-// per request; else ragged (total_q rows).  overlap: the first kernel is
-// launched as a programmatic dependent of the one before it (see
-// PrefillArgs::overlap).
+// per request; else ragged (total_q rows).
 int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_t total_q,
                 int32_t topk, int32_t init_blocks, int32_t local_blocks, int32_t* out,
                 int64_t out_head_stride, int64_t out_row_stride, void* workspace,
-                size_t workspace_bytes, void* stream, bool overlap = false) {
+                size_t workspace_bytes, void* stream) {
   int rc = check_problem(p, nvfp4);
   if (rc) return rc;
   if ((rc = check_topk(topk, init_blocks, local_blocks))) return rc;
@@ -608,8 +604,7 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t part_a = align256(prefill_part_a(dev->sms, p->heads, p->num_reqs, p->query_len, topk));
   mm3idx_problem_t q = *p;
-  if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q, overlap))) return rc;
-  const bool scorer_overlap = overlap && !nvfp4;   // after a dequant, the scorer reads its output
+  if (nvfp4 && (rc = dequant_copy(p, ws + part_a, dev, s, &q))) return rc;
   const int64_t tiles = prefill_tiles_bound(p->heads, p->num_reqs,
                                             static_cast<int64_t>(p->num_reqs) * p->query_len);
   PrefillSelect sel{};
@@ -623,8 +618,7 @@ int run_prefill(const mm3idx_problem_t* p, bool nvfp4, const int32_t* cu, int32_
   sel.tiles = tiles;
   sel.partials = reinterpret_cast<uint64_t*>(
       ws + align256(static_cast<size_t>(tiles + 1) * kTileRecInts * 4));
-  return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel,
-                        scorer_overlap);
+  return prefill_scores(&q, cu, total_q, nullptr, 0, 0, dev->sms, dev->status, s, &sel);
 }
 
 // Every warp waits on the first phase of a barrier that nothing arrives at,
@@ -885,8 +879,10 @@ int mm3idx_forward(const mm3idx_problem_t* p, int32_t num_decodes,
       return rc;
   }
   if (num_prefills == 0 || prefill_total_q == 0) return MM3IDX_OK;
-  // The prefill part: the remaining requests and rows, launched to start on
-  // the SMs the decode frees.
+  // The prefill part: the remaining requests and rows, after the decode in
+  // stream order.  (Launched as a programmatic dependent of the decode, to
+  // start on the SMs its CTAs free, the prefill measured 4 % slower: its CTAs'
+  // equal shares started unevenly.)
   mm3idx_problem_t f = *p;
   f.num_reqs = num_prefills;
   f.query_len = prefill_max_query_len;
@@ -895,8 +891,7 @@ int mm3idx_forward(const mm3idx_problem_t* p, int32_t num_decodes,
   f.seq_lens = p->seq_lens + num_decodes;
   return run_prefill(&f, nvfp4, prefill_cu_seqlens_q, prefill_total_q, topk, init_blocks,
                      local_blocks, out + dec_rows * out_row_stride, out_head_stride,
-                     out_row_stride, ws + dec_ws, workspace_bytes - dec_ws, stream,
-                     /*overlap=*/num_decodes > 0);
+                     out_row_stride, ws + dec_ws, workspace_bytes - dec_ws, stream);
 }
 
 int mm3idx_get_device_error(void* stream, int32_t* code) {

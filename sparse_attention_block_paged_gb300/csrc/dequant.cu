@@ -84,9 +84,6 @@ __global__ void __launch_bounds__(kThreads) dequant_pages_kernel(const DequantAr
       dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
-  // Overlapping launch (DequantArgs::overlap): complete only once the kernel
-  // before it has.
-  if (a.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -100,11 +97,6 @@ cudaError_t launch_dequant_pages(const DequantArgs& a, int num_sms, cudaStream_t
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, dequant_pages_kernel, a);
 }
 

@@ -64,11 +64,6 @@ struct PrefillArgs {
   uint64_t* partials;         // [2 * (grid + tiles)] slots of [prefill_tk(topk) keys][128 rows]
   int32_t* tile_rec;          // [1 + tiles][kTileRecInts]: [0][0] = tile count, then one per tile
   int32_t* status;
-  // Launched as a programmatic dependent of the kernel before it (a decode
-  // of the same batch, whose results it does not read): it starts on the
-  // SMs that kernel frees, and waits for that kernel's completion only at its
-  // end, so that its own completion still implies the other's.
-  int32_t overlap;
 };
 
 // Per query tile, written by the selecting prefill kernel for the merge:
@@ -116,7 +111,6 @@ struct DequantArgs {
   uint16_t* pages_out;        // bf16 [num_reqs * width, 128, 128]
   int32_t* table_out;         // [num_reqs, width]: slot ids (identity)
   int32_t* status;
-  int32_t overlap;            // as PrefillArgs::overlap
 };
 
 // The sparse page table of one head's ids (see sparse_table.cu).

@@ -712,8 +712,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  // Overlapping launch: complete only once the kernel before it has.
-  if (a.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -808,11 +806,6 @@ cudaError_t launch_prefill_t(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, prefill_kernel<kSelect, TK>, qmap, kmap, a);
 }
 
