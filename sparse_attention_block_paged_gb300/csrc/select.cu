@@ -186,12 +186,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
         // 256 N(0,1) scores reach the 29th-largest lane maximum and the
         // selection falls back to m rounds of a 64-bit warp max; the
         // 29th-largest of the lanes' best four lets about 29 through.
-        uint32_t c[4] = {0u, 0u, 0u, 0u};   // descending
+        uint32_t best4[4] = {0u, 0u, 0u, 0u};   // descending
         auto ins = [&](uint32_t x) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t hi = c[k] > x ? c[k] : x, lo = c[k] > x ? x : c[k];
-            c[k] = hi;
+            const uint32_t hi = best4[k] > x ? best4[k] : x, lo = best4[k] > x ? x : best4[k];
+            best4[k] = hi;
             x = lo;
           }
         };
@@ -199,16 +199,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) select_kernel(const Se
         for (int p = 0; p < kPer; ++p)
           if (base + p * 32 + lane < F.l_lo) ins(ordered_bits(v[p]));
         ins(rs);
-        T = c[0];
+        T = best4[0];
         for (int r = 0; r < m; ++r) {
-          const uint32_t mx = __reduce_max_sync(kFull, c[0]);
+          const uint32_t mx = __reduce_max_sync(kFull, best4[0]);
           if (mx == 0u) break;
           T = mx;
-          if (c[0] == mx) {   // this lane's best leaves (equal ones together)
-            c[0] = c[1];
-            c[1] = c[2];
-            c[2] = c[3];
-            c[3] = 0u;
+          if (best4[0] == mx) {   // this lane's best leaves (equal ones together)
+            best4[0] = best4[1];
+            best4[1] = best4[2];
+            best4[2] = best4[3];
+            best4[3] = 0u;
           }
         }
       }
