@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float score =
               (page >= 0 && page < a.num_pages) ? fmaxf(m0, m1) * a.sm_scale : -INFINITY;
           if constexpr (kSelect) {
-            if (b >= f_lo && b < l_lo) list.offer_shallow(make_key(score, b));
+            if (b >= f_lo && b < l_lo) list.offer_ascending(make_key(score, b));
           } else {
             srow[b] = score;
           }
