@@ -49,7 +49,7 @@ L2_BYTES = 129 * 1024 * 1024
 # dram traffic to be reported
 DECODE_SOURCES = ["decode.cu", "decode_common.cuh", "ptx.cuh", "internal.h", "warp_select.cuh"]
 NVFP4_DECODE_SOURCES = ["decode_fp4.cu", "decode_common.cuh", "ptx.cuh", "internal.h",
-                        "warp_select.cuh"]
+                        "warp_select.cuh", "nvfp4.cuh"]
 PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "internal.h", "warp_select.cuh"]
 
 

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmm3idx.so")
 SOURCES = ["api.cu", "decode.cu", "decode_fp4.cu", "prefill.cu", "select.cu", "dequant.cu",
            "sparse_table.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "warp_select.cuh", "decode_common.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "warp_select.cuh", "decode_common.cuh", "nvfp4.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -9,38 +9,29 @@
 // workspace, and the bf16 tensor-core scorer runs on that copy through an
 // identity block table.  One CTA of 256 threads per page: thread t takes half
 // a token row (64 elements): 32 bytes of codes and 4 scale bytes in, 128
-// bytes of bf16 out, all coalesced.
+// bytes of bf16 out, all coalesced.  The elements go through the per-scale
+// byte-permute table of nvfp4.cuh (about two integer operations an element,
+// where CUDA's fp8 conversions per element took about twenty).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mm3idx.h"
 #include "internal.h"
+#include "nvfp4.cuh"
 
 namespace mm3idx {
 namespace {
 
 constexpr int kThreads = 256;
-
-// e2m1 magnitudes of codes 0..7 (OCP MX FP4: 0, 0.5, 1, 1.5, 2, 3, 4, 6).
-__device__ __forceinline__ float e2m1_magnitude(uint32_t m) {
-  const float sub = (m & 1u) ? 0.5f : 0.0f;
-  const uint32_t e = m >> 1;
-  return e == 0 ? sub : static_cast<float>(1u << (e - 1)) * ((m & 1u) ? 1.5f : 1.0f);
-}
-
-// bf16 bits of e4m3_rn_satfinite(e2m1(code) * scale); the product is exact
-// in fp32 and the e4m3 result is exact in fp16 and bf16.
-__device__ __forceinline__ uint32_t nvfp4_bf16_bits(uint32_t code, float scale) {
-  const float mag = e2m1_magnitude(code & 7u) * scale;
-  const float v = (code & 8u) ? -mag : mag;
-  const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-  const __half_raw h = __nv_cvt_fp8_to_halfraw(q, __NV_E4M3);
-  return __float_as_uint(__half2float(__half(h))) >> 16;
-}
+constexpr int kCopies = 4;   // table copies side by side (thread & 3 picks one)
 
 __global__ void __launch_bounds__(kThreads) dequant_pages_kernel(const DequantArgs a) {
+  __shared__ uint4 sTab[256 * kCopies];
+  build_fp4_table(sTab, kCopies, threadIdx.x, kThreads);
+  __syncthreads();
   const int t = threadIdx.x;
+  const int copy = t & (kCopies - 1);
   const int tok = t >> 1, half = t & 1;
   const int64_t slots = static_cast<int64_t>(a.num_reqs) * a.width;
   for (int64_t slot = blockIdx.x; slot < slots; slot += gridDim.x) {
@@ -67,21 +58,9 @@ __global__ void __launch_bounds__(kThreads) dequant_pages_kernel(const DequantAr
     const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
     for (int g = 0; g < 4; ++g) {  // scale group: 16 elements, 8 code bytes
-      const __half_raw sh = __nv_cvt_fp8_to_halfraw(
-          static_cast<__nv_fp8_storage_t>((sc >> (8 * g)) & 0xffu), __NV_E4M3);
-      const float s = __half2float(__half(sh));
-      uint32_t o[8];
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {  // 4 code bytes = 8 elements
-        const uint32_t word = cw[2 * g + w];
-#pragma unroll
-        for (int by = 0; by < 4; ++by) {
-          const uint32_t byte = (word >> (8 * by)) & 0xffu;
-          o[4 * w + by] = nvfp4_bf16_bits(byte & 15u, s) | (nvfp4_bf16_bits(byte >> 4, s) << 16);
-        }
-      }
-      dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      const uint4 tb = sTab[((sc >> (8 * g)) & 0xffu) * kCopies + copy];
+      dst[2 * g] = dequant8(cw[2 * g], tb);
+      dst[2 * g + 1] = dequant8(cw[2 * g + 1], tb);
     }
   }
 }
