@@ -59,14 +59,18 @@ struct RegList {
   // 119.5 -> 113.8 us, chunked batch 95.7 -> 91.2 us).  In a list sorted
   // descending, "v[k] ranks above key" holds exactly for k below the key's
   // place, so each new slot follows from the old slot, its predecessor and
-  // the key alone (about four dependent steps instead of TK).
+  // the key alone (about four dependent steps instead of TK).  Only the
+  // first N slots are kept (the rest stay as they are): a caller that needs
+  // at most N keys spends no work on the others.
+  template <int N = TK>
   __device__ __forceinline__ void offer_ascending(uint64_t key) {
+    static_assert(N >= 1 && N <= TK, "slots in use");
     const uint32_t ks = static_cast<uint32_t>(key >> 32);
-    if (ks <= static_cast<uint32_t>(v[TK - 1] >> 32)) return;
+    if (ks <= static_cast<uint32_t>(v[N - 1] >> 32)) return;
     bool above_prev = true;  // v[k-1] ranks above key, with v[-1] above every key
     uint64_t prev = 0ull;
 #pragma unroll
-    for (int k = 0; k < TK; ++k) {
+    for (int k = 0; k < N; ++k) {
       const uint64_t cur = v[k];
       const bool above = static_cast<uint32_t>(cur >> 32) >= ks;
       v[k] = above ? cur : (above_prev ? key : prev);

@@ -149,10 +149,14 @@ def test_prefill_matches_oracle(mm, case):
 
 
 @pytest.mark.parametrize("topk,init,local", [(16, 1, 2), (4, 0, 0), (9, 3, 2), (32, 1, 2),
-                                             (17, 0, 0), (25, 4, 3)])
+                                             (17, 0, 0), (25, 4, 3),
+                                             # 16-key lists keeping 8, 12, 14, 15, 16 slots
+                                             (12, 2, 2), (16, 2, 2), (16, 1, 1), (16, 0, 1),
+                                             (16, 0, 0)])
 def test_fused_prefill_selection_equals_two_kernels(mm, topk, init, local):
     """The prefill kernel selects as it scores (16-key lists for topk <= 16,
-    else 32).  Its ids must be those of the score kernel followed by the
+    else 32; of a 16-key list only the topk - init - local slots a row can
+    need are kept).  Its ids must be those of the score kernel followed by the
     selector, bit for bit (the same fp32 scores and the same keys)."""
     wl = W.random_case(70 + topk, num_reqs=3, query_len=700, heads=2, topk=topk,
                        init_blocks=init, local_blocks=local, min_len=700,
