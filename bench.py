@@ -43,6 +43,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode score+top-k rows/s & HBM GB/s; prefill index TFLOP/s vs peak"
 HEADLINE = "spec_decode"
+# the headline batch, as both arms (ours and the oracle's) name it
+HEADLINE_WORKLOAD = ("spec-decode batch: 64 requests x query_len 4, seq_lens U[4096,32768], "
+                     "1 index head, topk 16, init 1, local 2, pool 1.25x need (shuffled)")
 BLOCK = 128
 L2_BYTES = 129 * 1024 * 1024
 # kernel sources whose hash a committed ncu summary must match for its
@@ -740,8 +743,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded numpy draws, bf16 q/k ~ N(0,1))",
-        "config": {"workload": "spec-decode batch: 64 requests x query_len 4, seq_lens U[4096,32768], "
-                               "1 index head, topk 16, init 1, local 2, pool 1.25x need (shuffled)",
+        "config": {"workload": HEADLINE_WORKLOAD,
                    "rows_per_step": wl.rows, "key_bytes_per_step": wl.key_bytes(),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before each timed step (read of a 2x-L2 buffer), flush not timed"},
@@ -788,8 +790,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy draws)",
-        "config": {"workload": "spec-decode batch: 64 requests x query_len 4, seq_lens U[4096,32768], "
-                               "1 index head, topk 16, init 1, local 2",
+        "config": {"workload": HEADLINE_WORKLOAD,
                    "sample_per_step": f"{per_step} requests ({per_step * wl.query_len} rows)"},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} requests per step, {args.steps} steps"},
